@@ -1,0 +1,503 @@
+#!/usr/bin/env python3
+"""Throughput of the CP partial-attention hot path on one GB300 (and N replicas under torchrun).
+
+One step = one pass of the whole path over one batch of synthetic input:
+  prefill workloads (full, long, tiny): cp_partition -> cp_partial_attn_prefill (pass-KV)
+      -> cp_lse_merge;
+  chunked: cp_partition of the new tokens -> cp_kv_interleave_layout -> pass-Q partial
+      attention -> cp_lse_merge;
+  decode: cp_kv_interleave_layout -> cp_partial_attn_decode -> cp_lse_merge.
+Default workload: full prefill (1 x 8192 tokens, 16/2 heads, d=128, bf16, cp=2), metric
+causal TFLOP/s (4*d*Hq per visible (q, k) pair).  A decode measurement (GB/s of kv read) is
+added as "secondary".  Multi-GPU: every rank runs an independent replica (CP shards are logical,
+on one GPU each) -- weak scaling, no collective on the data path.
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 512 * 1024 * 1024
+
+
+# ------------------------------------------------------------------------------------- utils
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        def pick(*keys):
+            for k in keys:
+                if isinstance(d.get(k), (int, float)):
+                    return float(d[k]), "measured"
+            return None
+        hbm = pick("hbm_gbs")
+        tf = pick("bf16_tflops")
+        tfs = pick("bf16_tflops_sustained")
+        return {"hbm": hbm or (FALLBACK_HBM_GBS, "fallback"),
+                "bf16": tf or (FALLBACK_BF16_TFLOPS, "fallback"),
+                "bf16_sustained": tfs or tf or (FALLBACK_BF16_TFLOPS, "fallback")}
+    return {"hbm": (FALLBACK_HBM_GBS, "fallback"), "bf16": (FALLBACK_BF16_TFLOPS, "fallback"),
+            "bf16_sustained": (FALLBACK_BF16_TFLOPS, "fallback")}
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) kept with host timestamps; summarised over a window."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        def reader():
+            for line in self.proc.stdout:
+                self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for t, s in self.samples if t0 <= t <= t1]
+        note = "in window"
+        if not rows and self.samples:
+            mid = 0.5 * (t0 + t1)
+            rows = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+            note = "nearest sample (timed region shorter than the 200 ms sampling period)"
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w": statistics.median(pw) if pw else None, "samples": len(rows),
+                "note": note}
+
+
+# ------------------------------------------------------------------------------------- runners
+
+def causal_pairs_pass_kv(lens):
+    return sum(T * (T + 1) // 2 for T in lens)
+
+
+class PrefillRunner:
+    """pass-KV prefill: partition -> partial attention -> merge."""
+
+    def __init__(self, w, dev, cpa):
+        self.w, self.dev, self.cpa = w, dev, cpa
+        lens = [w.seq_len] * w.num_seqs
+        x = wl.prefill_inputs(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.dtype, w.seed)
+        self.host = {k: v.pin_memory() for k, v in x.items()}
+        self.lens = lens
+        self.N = sum(lens)
+        self.q = x["q"].to(dev)
+        self.k = x["k"].to(dev)
+        self.v = x["v"].to(dev)
+        self.cu = x["cu_seqlens"].to(dev)
+        cp, Hq, d = w.cp, w.num_q_heads, w.head_dim
+        self.part = torch.empty(cp, self.N, Hq, d, dtype=torch.float32, device=dev)
+        self.plse = torch.empty(cp, self.N, Hq, dtype=torch.float32, device=dev)
+        self.out = torch.empty(self.N, Hq, d, dtype=w.dtype, device=dev)
+        self.olse = torch.empty(self.N, Hq, dtype=torch.float32, device=dev)
+        self.perm = torch.empty(self.N, dtype=torch.int32, device=dev)
+        self.inv = torch.empty(self.N, dtype=torch.int32, device=dev)
+        self.so = torch.empty(cp + 1, dtype=torch.int32, device=dev)
+        self.cb = torch.empty(len(lens), 2 * cp + 1, dtype=torch.int32, device=dev)
+        self.flops = 4.0 * d * Hq * causal_pairs_pass_kv(lens)
+        self.launches_per_step = 3
+        self.out_host = torch.empty(self.out.shape, dtype=w.dtype).pin_memory()
+
+    def step(self, ev=None):
+        cpa, w = self.cpa, self.w
+        cpa.cp_partition(self.cu, w.cp, self.N, self.perm, self.inv, self.so, self.cb)
+        if ev is not None:
+            ev[0].record()
+        cpa.cp_partial_attn_prefill(self.q, self.cu, w.cp, k=self.k, v=self.v,
+                                    max_seqlen_q=max(self.lens), out=self.part, lse=self.plse)
+        if ev is not None:
+            ev[1].record()
+        cpa.cp_lse_merge(self.part, self.plse, out=self.out, out_lse=self.olse)
+
+    def e2e_step(self):
+        """Host buffers in, host result out: the same step with the copies inside."""
+        self.q.copy_(self.host["q"], non_blocking=True)
+        self.k.copy_(self.host["k"], non_blocking=True)
+        self.v.copy_(self.host["v"], non_blocking=True)
+        self.cu.copy_(self.host["cu_seqlens"], non_blocking=True)
+        self.step()
+        self.out_host.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        h2d = sum(t.numel() * t.element_size() for t in self.host.values())
+        return h2d, self.out.numel() * self.out.element_size()
+
+    def metric(self, seconds):
+        return self.flops / seconds / 1e12
+
+    def config(self):
+        return prefill_config(self.w)
+
+
+def prefill_config(w):
+    return {"workload": f"{w.name} prefill pass-KV: {w.num_seqs}x{w.seq_len} tokens, "
+                        f"{w.num_q_heads}/{w.num_kv_heads} heads, d={w.head_dim}, cp={w.cp}",
+            "seq_len": w.seq_len, "global_batch": w.num_seqs, "cp": w.cp,
+            "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "mode": "pass_kv"}
+
+
+class DecodeRunner:
+    """decode: interleave layout -> per-rank split partials -> merge."""
+
+    def __init__(self, w, dev, cpa, on_device_values=True):
+        self.w, self.dev, self.cpa = w, dev, cpa
+        lens = wl.decode_lengths(w.num_seqs, w.min_len, w.max_len, w.len_seed).tolist()
+        self.lens = lens
+        caps = [wl.block_capacity(L, w.cp, w.interleave, w.block_size) for L in lens]
+        tables, pool = wl.shuffled_block_tables(caps, w.cp, torch.Generator().manual_seed(w.table_seed))
+        Hq, Hkv, d, cp = w.num_q_heads, w.num_kv_heads, w.head_dim, w.cp
+        g = torch.Generator(device=dev).manual_seed(w.seed)
+        shape = (cp, pool, Hkv, w.block_size, d)
+        # kv values drawn on the device (same N(0,1) recipe; the bench checks no parity)
+        self.kc = torch.randn(shape, generator=g, device=dev, dtype=w.dtype)
+        self.vc = torch.randn(shape, generator=g, device=dev, dtype=w.dtype)
+        self.q = torch.randn(w.num_seqs, Hq, d, generator=g, device=dev, dtype=w.dtype)
+        self.tables = tables.to(dev)
+        self.seq_lens = torch.tensor(lens, dtype=torch.int32, device=dev)
+        cu = [0]
+        for L in lens:
+            cu.append(cu[-1] + L)
+        self.cu = torch.tensor(cu, dtype=torch.int32, device=dev)
+        self.ns, self.st = cpa.cp_decode_plan(w.num_seqs, Hkv, cp, w.interleave, w.block_size, max(lens))
+        P = cp * self.ns
+        self.part = torch.empty(P, w.num_seqs, Hq, d, dtype=torch.float32, device=dev)
+        self.plse = torch.empty(P, w.num_seqs, Hq, dtype=torch.float32, device=dev)
+        self.out = torch.empty(w.num_seqs, Hq, d, dtype=w.dtype, device=dev)
+        self.local_lens = torch.empty(cp, w.num_seqs, dtype=torch.int32, device=dev)
+        el = torch.tensor([], dtype=w.dtype).element_size()
+        pages = sum(-(-n // w.block_size) for L in lens
+                    for n in [(L // (w.interleave * cp)) * w.interleave
+                              + min(max(L % (w.interleave * cp) - r * w.interleave, 0), w.interleave)
+                              for r in range(cp)])
+        self.bytes = (sum(lens) * Hkv * d * 2 * el + 2 * w.num_seqs * Hq * d * el + pages * 4)
+        self.kv_bytes = sum(lens) * Hkv * d * 2 * el
+        self.launches_per_step = 3
+        self.pool = pool
+
+    def step(self, ev=None):
+        cpa, w = self.cpa, self.w
+        cpa.cp_kv_interleave_layout(self.cu, w.cp, w.interleave, 0, w.block_size,
+                                    local_lens=self.local_lens, want_slots=False)
+        if ev is not None:
+            ev[0].record()
+        cpa.cp_partial_attn_decode(self.q, self.kc, self.vc, self.tables, self.seq_lens, w.cp,
+                                   w.interleave, num_splits=self.ns, split_tokens=self.st,
+                                   out=self.part, lse=self.plse)
+        if ev is not None:
+            ev[1].record()
+        cpa.cp_lse_merge(self.part, self.plse, out=self.out, want_lse=False)
+
+    def metric(self, seconds):
+        return self.bytes / seconds / 1e9
+
+    def config(self):
+        w = self.w
+        return {"workload": f"decode: {w.num_seqs} seqs, ctx U[{w.min_len},{w.max_len}] "
+                            f"(sum {sum(self.lens)}), {w.num_q_heads}/{w.num_kv_heads} heads, "
+                            f"d={w.head_dim}, paged bs={w.block_size}, cp={w.cp}, I={w.interleave}",
+                "splits": self.ns, "split_tokens": self.st}
+
+
+def time_steps(runner, steps, warmup, flush, dev, stream, dominant=True, stretch_s=0.0):
+    """Per-step device time (CUDA events on the launching stream), L2 flushed between steps."""
+    for _ in range(warmup):
+        flush.zero_()
+        runner.step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    dom = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)] if dominant else [None] * steps
+    extra = 0
+    if stretch_s > 0:  # extra flush passes keep the GPU busy so clocks can be sampled
+        t = time.time()
+        for _ in range(20):
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        per_flush = max((time.time() - t) / 20, 1e-5)
+        extra = int(max(0, stretch_s / steps / per_flush - 1))
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(steps):
+        for _ in range(1 + extra):
+            flush.zero_()
+        starts[i].record(stream)
+        runner.step(dom[i])
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dom_ms = [a.elapsed_time(b) for a, b in dom] if dominant else []
+    return step_ms, dom_ms, (t0, t1)
+
+
+# ------------------------------------------------------------------------------------- oracle
+
+def oracle_sample(w, rows_per_step, seed):
+    """Time the float64 oracle on a bounded, stratified sample of query rows of the workload."""
+    from oracle import cp_oracle as orc
+    lens = [w.seq_len] * w.num_seqs
+    x = wl.prefill_inputs(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.dtype, w.seed)
+    bnd = orc.chunk_bounds(w.seq_len, w.cp).tolist()
+    rows = wl.sample_rows(w.seq_len, bnd, rows_per_step, seed)
+    t = time.time()
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], w.cp,
+                                1 / math.sqrt(w.head_dim), rows=rows)
+    orc.lse_merge(O, L)
+    dt = time.time() - t
+    flops = 4.0 * w.head_dim * w.num_q_heads * sum(r + 1 for r in rows)
+    return flops, dt, len(rows)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------------------------- main
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, dev):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    w = wl.WORKLOADS[args.workload]
+    if w.kind != "pass_kv":
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle reference arm times "
+                                                             "prefill workloads only"}))
+        return 0
+    rows = args.ref_rows
+    for i in range(args.warmup):
+        oracle_sample(w, max(rows // 8, 8), 9000 + i)
+    tot_flops, tot_t, nrows = 0.0, 0.0, 0
+    for i in range(args.steps):
+        f, t, n = oracle_sample(w, rows, 9100 + i)
+        tot_flops += f
+        tot_t += t
+        nrows += n
+    val = tot_flops / tot_t / 1e12
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": "causal GQA prefill TFLOP/s (pass-KV partial attention + LSE merge)",
+        "value": val, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": prefill_config(w),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} stratified query rows x all heads per step "
+                                   f"({nrows} rows total), float64 NumPy oracle"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="full", choices=["full", "long", "tiny", "decode"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    import context_gqa_attention_gb300 as cpa
+    cpa.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    pk = peaks()
+    w = wl.WORKLOADS[args.workload]
+    runner = DecodeRunner(w, dev, cpa) if w.kind == "decode" else PrefillRunner(w, dev, cpa)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    step_ms, dom_ms, (t0, t1) = time_steps(runner, args.steps, args.warmup, flush, dev, stream,
+                                           stretch_s=1.0)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.summary(t0, t1)
+    clocks.stop()
+
+    total_s = max_over_ranks(sum(step_ms) / 1e3, ws, dev)
+    value = runner.metric(total_s / args.steps) * ws
+    dom_s = statistics.mean(dom_ms) / 1e3
+
+    # end to end: host buffers, copies inside the timed region
+    if isinstance(runner, PrefillRunner):
+        for _ in range(3):
+            runner.e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            runner.e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, ws, dev)
+        h2d, d2h = runner.e2e_bytes()
+        e2e = {"value": runner.metric(e2e_s / args.steps) * ws, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        peak, src = pk["bf16"]
+        achieved = runner.flops / dom_s / 1e12
+        roof = {"bound": "tensor", "kernel": "cp_partial_attn_prefill (pass-KV)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{src} bf16 dense (burst)", "traffic": None,
+                "algorithmic": f"{runner.flops:.4e} causal FLOP per launch",
+                "launch_ms": dom_s * 1e3}
+        metric = "causal GQA prefill TFLOP/s (pass-KV partial attention + LSE merge)"
+        unit = "TFLOP/s"
+    else:
+        e2e = None
+        peak, src = pk["hbm"]
+        achieved = runner.kv_bytes / dom_s / 1e9
+        roof = {"bound": "hbm", "kernel": "cp_partial_attn_decode", "achieved": achieved,
+                "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{src} HBM copy", "traffic": None, "launch_ms": dom_s * 1e3}
+        metric = "decode KV-read GB/s (partial attention + LSE merge)"
+        unit = "GB/s"
+
+    line = {"metric": metric, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
+            "config": dict(runner.config(), l2="flushed between timed steps (512 MB write)",
+                           parallelism=f"replicas x{ws} (logical CP shards on each GPU)"),
+            "roofline": roof, "clocks": clk,
+            "gpu_launches": runner.launches_per_step * args.steps}
+    if e2e is not None:
+        line["e2e"] = e2e
+
+    if not args.no_secondary and w.kind != "decode":
+        dr = DecodeRunner(wl.WORKLOADS["decode"], dev, cpa)
+        ds, dd, _ = time_steps(dr, max(10, args.steps // 5), 3, flush, dev, stream)
+        d_s = statistics.mean(dd) / 1e3
+        hbm, hsrc = pk["hbm"]
+        line["secondary"] = {
+            "decode": {"value": dr.metric(statistics.mean(ds) / 1e3), "unit": "GB/s",
+                       "config": dr.config(),
+                       "roofline": {"bound": "hbm", "kernel": "cp_partial_attn_decode",
+                                    "achieved": dr.kv_bytes / d_s / 1e9, "peak": hbm,
+                                    "unit": "GB/s", "frac": dr.kv_bytes / d_s / 1e9 / hbm,
+                                    "peak_source": f"{hsrc} HBM copy", "launch_ms": d_s * 1e3}}}
+        del dr
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and w.kind == "pass_kv":
+        f, t, n = oracle_sample(w, args.cpu_rows, 777)
+        line["cpu_baseline"] = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"{n} stratified query rows x {w.num_q_heads} heads of the "
+                                          f"{w.name} workload, float64 NumPy oracle, {t:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,411 @@
+// Host side of the C ABI (include/cpattn.h): argument validation, error reporting and the
+// launches of the integer layout kernels and the LSE merge.  Attention kernels live in
+// prefill_tc.cu, prefill_simt.cu and decode.cu.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace {
+
+thread_local char g_detail[512] = "";
+thread_local int32_t g_status = CP_OK;
+
+cp_status fail(cp_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  g_status = st;
+  return st;
+}
+
+cp_status ok() {
+  g_status = CP_OK;
+  g_detail[0] = '\0';
+  return CP_OK;
+}
+
+cp_status launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(CP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQUIRE(cond, ...)                                   \
+  do {                                                       \
+    if (!(cond)) return fail(CP_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+#define REQUIRE_PTR(p) REQUIRE((p) != nullptr && aligned16(p), #p " must be a non-null 16-byte aligned pointer")
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+// ============================================================================ device kernels
+namespace cpattn {
+namespace {
+
+// ---- cp_partition: per-(rank, sequence) row offsets in shared memory, then one thread per
+// token.  Offsets: off[r][b] = rows of rank r that precede sequence b, base[r] = rows of the
+// ranks before r.
+__global__ void partition_kernel(const int32_t* __restrict__ cu, int B, int N, int cp,
+                                 int32_t* perm, int32_t* inv, int32_t* shard_offsets,
+                                 int32_t* chunk_bounds) {
+  extern __shared__ int32_t sm[];
+  int32_t* off = sm;                  // [cp][B + 1]
+  int32_t* base = sm + cp * (B + 1);  // [cp + 1]
+  for (int i = threadIdx.x; i < cp * B; i += blockDim.x) {
+    const int r = i / B, b = i % B;
+    const int T = cu[b + 1] - cu[b];
+    const int c2 = 2 * cp - 1 - r;
+    off[r * (B + 1) + b + 1] = (chunk_bound(r + 1, T, cp) - chunk_bound(r, T, cp)) +
+                               (chunk_bound(c2 + 1, T, cp) - chunk_bound(c2, T, cp));
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < cp; r += blockDim.x) {
+    int32_t* o = off + r * (B + 1);
+    o[0] = 0;
+    for (int b = 0; b < B; ++b) o[b + 1] += o[b];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    base[0] = 0;
+    for (int r = 0; r < cp; ++r) base[r + 1] = base[r] + off[r * (B + 1) + B];
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    if (shard_offsets)
+      for (int r = threadIdx.x; r <= cp; r += blockDim.x) shard_offsets[r] = base[r];
+    if (chunk_bounds)
+      for (int i = threadIdx.x; i < B * (2 * cp + 1); i += blockDim.x) {
+        const int b = i / (2 * cp + 1), k = i % (2 * cp + 1);
+        chunk_bounds[i] = chunk_bound(k, cu[b + 1] - cu[b], cp);
+      }
+  }
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < N; t += gridDim.x * blockDim.x) {
+    const int b = seq_of_row(cu, B, t);
+    const int T = cu[b + 1] - cu[b];
+    const int o = t - cu[b];
+    const int c = chunk_of(o, T, cp);
+    const int r = shard_of_chunk(c, cp);
+    const int within = (c == r) ? o - chunk_bound(r, T, cp)
+                                : (chunk_bound(r + 1, T, cp) - chunk_bound(r, T, cp)) +
+                                      (o - chunk_bound(c, T, cp));
+    const int row = base[r] + off[r * (B + 1) + b] + within;
+    if (row >= N) continue;  // total_tokens smaller than cu_seqlens[B]: caller error, no write
+    if (perm) perm[row] = t;
+    if (inv) inv[t] = row;
+  }
+}
+
+// ---- cp_kv_interleave_layout: closed forms of the round-robin deal, one thread per item.
+__global__ void interleave_kernel(const int32_t* __restrict__ cu, int B, int N, int cp, int I,
+                                  int bs, const int32_t* __restrict__ tables, int max_blocks,
+                                  int32_t* local_lens, int32_t* rank_of, int32_t* local_of,
+                                  int64_t* slot_of, int32_t* err) {
+  const long long items = max((long long)N, (long long)cp * B);
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < items;
+       i += (long long)gridDim.x * blockDim.x) {
+    if (local_lens && i < (long long)cp * B) {
+      const int r = (int)(i / B), b = (int)(i % B);
+      local_lens[i] = rank_local_len(cu[b + 1] - cu[b], r, cp, I);
+    }
+    if (i < N) {
+      const int t = (int)i;
+      const int b = seq_of_row(cu, B, t);
+      const long long p = t - cu[b];
+      const int r = (int)((p / I) % cp);
+      const long long l = (p / ((long long)I * cp)) * I + p % I;
+      if (rank_of) rank_of[t] = r;
+      if (local_of) local_of[t] = (int32_t)l;
+      if (slot_of) {
+        const long long col = l / bs;
+        long long slot = -1;
+        if (col < max_blocks) {
+          const int page = tables[((long long)r * B + b) * max_blocks + col];
+          if (page >= 0) slot = (long long)page * bs + l % bs;
+        }
+        if (slot < 0) report(err, CP_ERR_DEVICE_BOUNDS);
+        slot_of[t] = slot;
+      }
+    }
+  }
+}
+
+// ---- cp_lse_merge: one warp per (row, head); lanes own D/32 consecutive floats.
+template <int D, bool BF16_OUT>
+__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ po,
+                                                    const float* __restrict__ pl, int P,
+                                                    long long units, void* out, float* out_lse) {
+  constexpr int E = D / 32;
+  const long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (u >= units) return;
+  // M = max_p lse_p (log2 domain)
+  float M = -INFINITY;
+  for (int p0 = 0; p0 < P; p0 += 32) {
+    const int p = p0 + lane;
+    if (p < P) M = fmaxf(M, __ldg(pl + (long long)p * units + u) * kLog2e);
+  }
+  M = warp_max(M);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (M > -INFINITY) {
+#pragma unroll 4
+    for (int p = 0; p < P; ++p) {
+      const float lp = __ldg(pl + (long long)p * units + u);
+      if (lp == -INFINITY) continue;  // an empty partial is never read
+      const float w = exp2f(lp * kLog2e - M);
+      wsum += w;
+      const float* src = po + ((long long)p * units + u) * D + lane * E;
+      if constexpr (E == 4) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+        acc[2] += w * x.z;
+        acc[3] += w * x.w;
+      } else {
+        const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  if constexpr (BF16_OUT) {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + u * D + lane * E;
+    if constexpr (E == 4) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&a);
+      pk.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(o) = pk;
+    } else {
+      *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    }
+  } else {
+    float* o = static_cast<float*>(out) + u * D + lane * E;
+    if constexpr (E == 4) {
+      *reinterpret_cast<float4*>(o) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    } else {
+      *reinterpret_cast<float2*>(o) = make_float2(acc[0] * inv, acc[1] * inv);
+    }
+  }
+  if (out_lse && lane == 0) out_lse[u] = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
+}
+
+}  // namespace
+}  // namespace cpattn
+
+// ============================================================================ C ABI
+extern "C" {
+
+const char* cp_status_string(int32_t st) {
+  switch (st) {
+    case CP_OK: return "CP_OK";
+    case CP_ERR_INVALID_ARG: return "CP_ERR_INVALID_ARG";
+    case CP_ERR_UNSUPPORTED: return "CP_ERR_UNSUPPORTED";
+    case CP_ERR_CUDA: return "CP_ERR_CUDA";
+    case CP_ERR_TIMEOUT: return "CP_ERR_TIMEOUT";
+    case CP_ERR_DEVICE_BOUNDS: return "CP_ERR_DEVICE_BOUNDS";
+    default: return "CP_ERR_UNKNOWN";
+  }
+}
+
+int32_t cp_last_error(char* buf, size_t n) {
+  if (buf && n) {
+    strncpy(buf, g_detail, n - 1);
+    buf[n - 1] = '\0';
+  }
+  return g_status;
+}
+
+int32_t cp_abi_version(void) { return CPATTN_ABI_VERSION; }
+size_t cp_prefill_args_size(void) { return sizeof(cp_prefill_args); }
+size_t cp_decode_args_size(void) { return sizeof(cp_decode_args); }
+
+cp_status cp_partition(const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                       int32_t cp, int32_t* perm, int32_t* inv_perm, int32_t* shard_offsets,
+                       int32_t* chunk_bounds, void* stream) {
+  REQUIRE(num_seqs >= 1, "num_seqs must be >= 1 (got %d)", num_seqs);
+  REQUIRE(total_tokens >= 0, "total_tokens must be >= 0");
+  REQUIRE(cp >= 1 && cp <= 64, "cp must be in [1, 64] (got %d)", cp);
+  REQUIRE((long long)num_seqs * cp <= 16384, "num_seqs * cp must be <= 16384");
+  REQUIRE(cu_seqlens != nullptr, "cu_seqlens is null");
+  REQUIRE(perm || inv_perm || shard_offsets || chunk_bounds, "no output requested");
+  const size_t smem = ((size_t)cp * (num_seqs + 1) + cp + 1) * sizeof(int32_t);
+  const int threads = 256;
+  int blocks = (total_tokens + threads - 1) / threads;
+  blocks = blocks < 1 ? 1 : (blocks > 1184 ? 1184 : blocks);
+  cudaError_t e = cudaSuccess;
+  if (smem > 48 * 1024)
+    e = cudaFuncSetAttribute(cpattn::partition_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  if (e != cudaSuccess) return launched(e, "cp_partition attribute");
+  cpattn::partition_kernel<<<blocks, threads, smem, as_stream(stream)>>>(
+      cu_seqlens, num_seqs, total_tokens, cp, perm, inv_perm, shard_offsets, chunk_bounds);
+  return launched(cudaGetLastError(), "cp_partition launch");
+}
+
+cp_status cp_kv_interleave_layout(const int32_t* cu_seq_lens, int32_t num_seqs,
+                                  int32_t total_tokens, int32_t cp, int32_t interleave,
+                                  int32_t block_size, const int32_t* block_tables,
+                                  int32_t max_blocks, int32_t* local_lens, int32_t* rank_of_token,
+                                  int32_t* local_of_token, int64_t* slot_of_token, int32_t* err,
+                                  void* stream) {
+  REQUIRE(num_seqs >= 1 && total_tokens >= 0, "bad num_seqs / total_tokens");
+  REQUIRE(cp >= 1 && cp <= 64, "cp must be in [1, 64] (got %d)", cp);
+  REQUIRE(interleave >= 1, "interleave must be >= 1");
+  REQUIRE(block_size >= 1, "block_size must be >= 1");
+  REQUIRE(cu_seq_lens != nullptr, "cu_seq_lens is null");
+  REQUIRE(!slot_of_token || (block_tables && max_blocks >= 1),
+          "slot_of_token needs block_tables and max_blocks >= 1");
+  REQUIRE(local_lens || rank_of_token || local_of_token || slot_of_token, "no output requested");
+  const long long items = total_tokens > (long long)cp * num_seqs ? total_tokens : (long long)cp * num_seqs;
+  int blocks = (int)((items + 255) / 256);
+  blocks = blocks < 1 ? 1 : (blocks > 4096 ? 4096 : blocks);
+  cpattn::interleave_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
+      cu_seq_lens, num_seqs, total_tokens, cp, interleave, block_size, block_tables, max_blocks,
+      local_lens, rank_of_token, local_of_token, slot_of_token, err);
+  return launched(cudaGetLastError(), "cp_kv_interleave_layout launch");
+}
+
+cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32_t num_partials,
+                       int64_t rows, int32_t num_heads, int32_t head_dim, void* out,
+                       int32_t out_dtype, float* out_lse, void* stream) {
+  REQUIRE(num_partials >= 1, "num_partials must be >= 1");
+  REQUIRE(rows >= 0 && num_heads >= 1, "bad rows / num_heads");
+  REQUIRE(head_dim == 64 || head_dim == 128, "head_dim must be 64 or 128 (got %d)", head_dim);
+  REQUIRE(out_dtype == CP_F32 || out_dtype == CP_BF16, "out_dtype must be CP_F32 or CP_BF16");
+  REQUIRE_PTR(partial_out);
+  REQUIRE(partial_lse != nullptr, "partial_lse is null");
+  REQUIRE_PTR(out);
+  const long long units = rows * (long long)num_heads;
+  if (units == 0) return ok();
+  const long long blocks = (units * 32 + 255) / 256;
+  REQUIRE(blocks < (1ll << 31), "too many rows");
+  cudaStream_t s = as_stream(stream);
+  if (head_dim == 128) {
+    if (out_dtype == CP_BF16)
+      cpattn::merge_kernel<128, true><<<(unsigned)blocks, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse);
+    else
+      cpattn::merge_kernel<128, false><<<(unsigned)blocks, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse);
+  } else {
+    if (out_dtype == CP_BF16)
+      cpattn::merge_kernel<64, true><<<(unsigned)blocks, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse);
+    else
+      cpattn::merge_kernel<64, false><<<(unsigned)blocks, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse);
+  }
+  return launched(cudaGetLastError(), "cp_lse_merge launch");
+}
+
+cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
+  REQUIRE(a != nullptr, "args is null");
+  REQUIRE(a->mode == CP_PASS_KV || a->mode == CP_PASS_Q, "mode must be CP_PASS_KV or CP_PASS_Q");
+  REQUIRE(a->dtype == CP_F32 || a->dtype == CP_BF16, "dtype must be CP_F32 or CP_BF16");
+  REQUIRE(a->impl >= CP_IMPL_AUTO && a->impl <= CP_IMPL_SIMT, "unknown impl %d", a->impl);
+  REQUIRE(a->num_seqs >= 1, "num_seqs must be >= 1");
+  REQUIRE(a->num_kv_heads >= 1 && a->num_q_heads >= a->num_kv_heads &&
+              a->num_q_heads % a->num_kv_heads == 0,
+          "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", a->num_q_heads,
+          a->num_kv_heads);
+  if (a->head_dim != 64 && a->head_dim != 128)
+    return fail(CP_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", a->head_dim);
+  REQUIRE(a->cp >= 1 && a->cp <= 64, "cp must be in [1, 64] (got %d)", a->cp);
+  REQUIRE(a->total_q >= 0 && a->max_seqlen_q >= 0, "total_q / max_seqlen_q must be >= 0");
+  REQUIRE(a->q_shard >= -1 && a->q_shard < a->cp, "q_shard out of range");
+  REQUIRE(a->kv_shard >= -1 && a->kv_shard < a->cp, "kv_shard out of range");
+  REQUIRE(a->cu_seqlens_q != nullptr, "cu_seqlens_q is null");
+  REQUIRE_PTR(a->q);
+  REQUIRE_PTR(a->out);
+  REQUIRE(a->lse != nullptr, "lse is null");
+  if (a->mode == CP_PASS_KV) {
+    REQUIRE_PTR(a->k);
+    REQUIRE_PTR(a->v);
+  } else {
+    REQUIRE_PTR(a->k_cache);
+    REQUIRE_PTR(a->v_cache);
+    REQUIRE(a->block_tables != nullptr && a->seq_lens_kv != nullptr,
+            "PASS_Q needs block_tables and seq_lens_kv");
+    REQUIRE(a->max_blocks >= 1 && a->pool_pages >= 1, "PASS_Q needs max_blocks, pool_pages >= 1");
+    REQUIRE(a->interleave >= 1, "interleave must be >= 1");
+    if (a->block_size != 16)
+      return fail(CP_ERR_UNSUPPORTED, "block_size must be 16 (got %d)", a->block_size);
+  }
+  if (a->total_q == 0) return ok();
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
+  int impl = a->impl;
+  if (impl == CP_IMPL_AUTO) impl = (a->dtype == CP_BF16 && cp_prefill_tc_supported(*a)) ? CP_IMPL_TCGEN05 : CP_IMPL_SIMT;
+  if (impl == CP_IMPL_TCGEN05) {
+    if (a->dtype != CP_BF16 || !cp_prefill_tc_supported(*a))
+      return fail(CP_ERR_UNSUPPORTED, "the tcgen05 kernel needs bf16 inputs and a supported shape");
+    return launched(cp_launch_prefill_tc(*a, scale, as_stream(stream)), "prefill (tcgen05) launch");
+  }
+  return launched(cp_launch_prefill_simt(*a, scale, as_stream(stream)), "prefill (simt) launch");
+}
+
+cp_status cp_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t cp, int32_t interleave,
+                         int32_t block_size, int32_t max_seq_len, int32_t* num_splits,
+                         int32_t* split_tokens) {
+  REQUIRE(num_seqs >= 1 && num_kv_heads >= 1 && cp >= 1 && interleave >= 1 && block_size >= 1 &&
+              max_seq_len >= 1,
+          "all sizes must be >= 1");
+  REQUIRE(num_splits && split_tokens, "outputs are null");
+  // largest rank share: rank 0 never holds fewer tokens than another rank
+  const long long group = (long long)interleave * cp;
+  long long rem = max_seq_len % group;
+  const long long share = (max_seq_len / group) * interleave + (rem < interleave ? rem : interleave);
+  // target ~1024 local tokens per CTA and at least ~8 CTAs per SM over 152 SMs in total
+  const long long base = (long long)num_seqs * num_kv_heads * cp;
+  long long S = (share + 1023) / 1024;
+  const long long want = (8ll * 152 + base - 1) / base;
+  if (S < want) S = want;
+  const long long max_S = (share + block_size - 1) / block_size;
+  if (S > max_S) S = max_S;
+  if (S < 1) S = 1;
+  long long st = (share + S - 1) / S;
+  st = (st + block_size - 1) / block_size * block_size;
+  S = (share + st - 1) / st;
+  REQUIRE(S <= 65535, "too many splits");
+  *num_splits = (int32_t)S;
+  *split_tokens = (int32_t)st;
+  return ok();
+}
+
+cp_status cp_partial_attn_decode(const cp_decode_args* a, void* stream) {
+  REQUIRE(a != nullptr, "args is null");
+  REQUIRE(a->dtype == CP_F32 || a->dtype == CP_BF16, "dtype must be CP_F32 or CP_BF16");
+  REQUIRE(a->num_seqs >= 1, "num_seqs must be >= 1");
+  REQUIRE(a->num_kv_heads >= 1 && a->num_q_heads % a->num_kv_heads == 0,
+          "num_q_heads must be a multiple of num_kv_heads");
+  const int G = a->num_q_heads / a->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(CP_ERR_UNSUPPORTED, "q heads per kv head must be 1, 2, 4 or 8 (got %d)", G);
+  if (a->head_dim != 64 && a->head_dim != 128)
+    return fail(CP_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", a->head_dim);
+  if (a->block_size != 16)
+    return fail(CP_ERR_UNSUPPORTED, "block_size must be 16 (got %d)", a->block_size);
+  REQUIRE(a->cp >= 1 && a->cp <= 64 && a->interleave >= 1, "bad cp / interleave");
+  REQUIRE(a->num_splits >= 1 && a->num_splits <= 65535, "num_splits must be in [1, 65535]");
+  REQUIRE(a->split_tokens >= a->block_size && a->split_tokens % a->block_size == 0,
+          "split_tokens must be a positive multiple of block_size");
+  REQUIRE(a->max_blocks >= 1 && a->pool_pages >= 1, "max_blocks and pool_pages must be >= 1");
+  REQUIRE((long long)a->cp * a->num_seqs <= 65535 && a->num_kv_heads <= 65535, "grid too large");
+  REQUIRE_PTR(a->q);
+  REQUIRE_PTR(a->k_cache);
+  REQUIRE_PTR(a->v_cache);
+  REQUIRE_PTR(a->out);
+  REQUIRE(a->block_tables && a->seq_lens && a->lse, "block_tables, seq_lens and lse are required");
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
+  return launched(cp_launch_decode(*a, scale, as_stream(stream)), "decode launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Shared device/host helpers of libcpattn (internal; not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/cpattn.h"
+
+#define CP_DEV __device__ __forceinline__
+
+namespace cpattn {
+
+// First device-side error wins; CP_OK is never written.
+CP_DEV void report(int32_t* err, int32_t code) {
+  if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static CP_DEV float to_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static CP_DEV float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+};
+
+// Chunk bounds of the load-balanced partition: b_k = floor(k*T/(2cp)).
+CP_DEV int chunk_bound(int k, int T, int cp) {
+  return (int)(((long long)k * T) / (2 * cp));
+}
+
+// Chunk index c (0..2cp-1) of within-sequence offset t (0 <= t < T).
+CP_DEV int chunk_of(int t, int T, int cp) {
+  int c = (int)(((long long)t * 2 * cp) / T);  // lower estimate
+  // b_c <= t < b_{c+1}; the estimate is within one of the answer.
+  while (c + 1 < 2 * cp && chunk_bound(c + 1, T, cp) <= t) ++c;
+  while (c > 0 && chunk_bound(c, T, cp) > t) --c;
+  return c;
+}
+
+CP_DEV int shard_of_chunk(int c, int cp) { return c < cp ? c : 2 * cp - 1 - c; }
+
+// Round-robin interleave: tokens of rank r among positions [0, L).
+CP_DEV int rank_local_len(long long L, int r, int cp, int I) {
+  long long group = (long long)I * cp;
+  long long full = (L / group) * I;
+  long long rem = L % group - (long long)r * I;
+  rem = rem < 0 ? 0 : (rem > I ? I : rem);
+  return (int)(full + rem);
+}
+
+// Global position of local index l on rank r.
+CP_DEV long long rank_local_pos(long long l, int r, int cp, int I) {
+  return (l / I) * (long long)I * cp + (long long)r * I + (l % I);
+}
+
+// Sequence of a row: largest b with cu[b] <= row (cu non-decreasing, cu[0] = 0).
+CP_DEV int seq_of_row(const int32_t* __restrict__ cu, int num_seqs, int row) {
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+CP_DEV float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+CP_DEV float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+}  // namespace cpattn
+
+// ---------------------------------------------------------------------------- launchers
+// Implemented in the kernel translation units; called by the host ABI in api.cu after
+// argument validation.  They return the launch status.
+cudaError_t cp_launch_prefill_simt(const cp_prefill_args& a, float scale, cudaStream_t s);
+cudaError_t cp_launch_prefill_tc(const cp_prefill_args& a, float scale, cudaStream_t s);
+bool cp_prefill_tc_supported(const cp_prefill_args& a);
+cudaError_t cp_launch_decode(const cp_decode_args& a, float scale, cudaStream_t s);

@@ -1,0 +1,271 @@
+// Decode partial attention over a round-robin paged kv cache ("allgather decode").
+//
+// "Add utility functions to enable pass-kv prefill and allgather decode" (vLLM PR 26059),
+// Purpose: decode KV stays on the CP ranks round-robin, each rank attends the new query over
+// its own tokens and the partials are combined (cp_lse_merge).  "[Feature] Prefill Context
+// Parallel (PCP) basic support" (PR 28718), Purpose: per-rank block tables.
+//
+// Work unit (one CTA of 4 warps): split s of rank r's local tokens of sequence b, kv head g,
+// all G query heads of that group.  The kernel is HBM-bound: every kv byte is read once with
+// 16-byte loads straight into registers, a page (16 tokens, head-major so one head's page is
+// contiguous) per warp per iteration, and all of a page's loads are issued before its math.
+#include "common.cuh"
+
+namespace cpattn {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kPage = 16;  // tokens per page (block_size)
+
+struct DecodeParams {
+  int B, Hq, Hkv, cp, I, S, ST, max_blocks;
+  long long pool;
+  float scale_log2;
+  const void* q;
+  const void* kc;
+  const void* vc;
+  const int32_t* tables;
+  const int32_t* seq_lens;
+  float* out;
+  float* lse;
+  int32_t* err;
+};
+
+template <typename T> struct Vec;
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static CP_DEV void unpack(const uint4& u, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(h[i]);
+      f[2 * i] = x.x;
+      f[2 * i + 1] = x.y;
+    }
+  }
+};
+template <> struct Vec<float> {
+  static constexpr int N = 4;
+  static CP_DEV void unpack(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+};
+
+CP_DEV uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams p) {
+  constexpr int EPV = Vec<T>::N;          // elements per 16-byte vector
+  constexpr int QKV = (D / 2) / EPV;      // K vectors per lane: token lane/2, vectors 2i+lane%2
+  constexpr int NCH = D / EPV;            // V chunks per token
+  constexpr int TG = 32 / NCH;            // token groups in a warp for P.V
+  constexpr int TPL = kPage / TG;         // V tokens per lane
+  static_assert(NCH <= 32 && 32 % NCH == 0, "head_dim / vector width");
+
+  __shared__ __align__(16) float q_s[G][D];             // scaled into the log2 domain
+  __shared__ __align__(16) float p_s[kWarps][kPage][G];
+  __shared__ float m_w[kWarps][G], l_w[kWarps][G];
+  __shared__ __align__(16) float o_w[kWarps][G][D];
+
+  const int split = blockIdx.x, g = blockIdx.y;
+  const int r = blockIdx.z / p.B, b = blockIdx.z % p.B;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = __ldg(p.seq_lens + b);
+  const int n = rank_local_len(L, r, p.cp, p.I);
+  const int l0 = split * p.ST;
+  const int l1 = min(n, l0 + p.ST);
+  const int part = r * p.S + split;
+  const long long obase = ((long long)part * p.B + b) * p.Hq + (long long)g * G;
+
+  if (l0 >= l1) {  // nothing of this rank falls in this split
+    if (threadIdx.x < G) p.lse[obase + threadIdx.x] = -INFINITY;
+    return;
+  }
+
+  const T* qg = static_cast<const T*>(p.q) + ((long long)b * p.Hq + (long long)g * G) * D;
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+    (&q_s[0][0])[i] = Elem<T>::to_f(qg[i]) * p.scale_log2;
+  __syncthreads();
+
+  float m[G], l[G], acc[G][EPV];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    m[hh] = -INFINITY;
+    l[hh] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) acc[hh][e] = 0.f;
+  }
+
+  const int qk_tok = lane >> 1, half = lane & 1;
+  const int v_ch = lane % NCH, v_tg = lane / NCH;
+  const int32_t* trow = p.tables + ((long long)r * p.B + b) * p.max_blocks;
+  const long long head_stride = (long long)kPage * D;  // elements of one head's page
+  const T* kbase = static_cast<const T*>(p.kc);
+  const T* vbase = static_cast<const T*>(p.vc);
+
+  const int pg0 = l0 / kPage, pg1 = (l1 + kPage - 1) / kPage;
+  for (int pg = pg0 + warp; pg < pg1; pg += kWarps) {
+    const int page = pg < p.max_blocks ? __ldg(trow + pg) : -1;
+    if (page < 0 || page >= p.pool) {
+      if (lane == 0) report(p.err, CP_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    const long long off = (((long long)r * p.pool + page) * p.Hkv + g) * head_stride;
+    const T* kp = kbase + off;
+    const T* vp = vbase + off;
+    uint4 kv[QKV], vv[TPL];
+#pragma unroll
+    for (int i = 0; i < QKV; ++i)
+      kv[i] = ldg_stream(kp + (long long)qk_tok * D + (2 * i + half) * EPV);
+#pragma unroll
+    for (int i = 0; i < TPL; ++i)
+      vv[i] = ldg_stream(vp + (long long)(v_tg + i * TG) * D + v_ch * EPV);
+
+    // scores of token qk_tok for the G heads (two lanes per token, one half of d each)
+    float s[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) s[hh] = 0.f;
+#pragma unroll
+    for (int i = 0; i < QKV; ++i) {
+      float kf[EPV];
+      Vec<T>::unpack(kv[i], kf);
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float4* qv = reinterpret_cast<const float4*>(&q_s[hh][(2 * i + half) * EPV]);
+#pragma unroll
+        for (int e4 = 0; e4 < EPV / 4; ++e4) {
+          const float4 qq = qv[e4];
+          s[hh] += qq.x * kf[4 * e4] + qq.y * kf[4 * e4 + 1] + qq.z * kf[4 * e4 + 2] +
+                   qq.w * kf[4 * e4 + 3];
+        }
+      }
+    }
+    const bool valid = pg * kPage + qk_tok < l1;
+    float corr[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      s[hh] += __shfl_xor_sync(0xffffffffu, s[hh], 1);
+      s[hh] = valid ? s[hh] : -INFINITY;
+      const float m_new = fmaxf(m[hh], warp_max(s[hh]));
+      corr[hh] = exp2f(m[hh] - m_new);
+      const float pv = exp2f(s[hh] - m_new);
+      l[hh] = l[hh] * corr[hh] + warp_sum(half == 0 ? pv : 0.f);
+      m[hh] = m_new;
+      if (half == 0) p_s[warp][qk_tok][hh] = pv;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) acc[hh][e] *= corr[hh];
+#pragma unroll
+    for (int i = 0; i < TPL; ++i) {
+      float vf[EPV];
+      Vec<T>::unpack(vv[i], vf);
+      const int t = v_tg + i * TG;
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float pw = p_s[warp][t][hh];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[hh][e] += pw * vf[e];
+      }
+    }
+    __syncwarp();
+  }
+
+  // token groups of the warp -> one partial per warp
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+    for (int e = 0; e < EPV; ++e)
+#pragma unroll
+      for (int o = NCH; o < 32; o <<= 1) acc[hh][e] += __shfl_xor_sync(0xffffffffu, acc[hh][e], o);
+  if (lane == 0) {
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      m_w[warp][hh] = m[hh];
+      l_w[warp][hh] = l[hh];
+    }
+  }
+  if (v_tg == 0) {
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) o_w[warp][hh][v_ch * EPV + e] = acc[hh][e];
+  }
+  __syncthreads();
+
+  // warps -> the CTA's partial (warps that saw no page carry m = -inf and weight 0)
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int hh = i / D, dd = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, m_w[w][hh]);
+    float Ls = 0.f, Os = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float e = exp2f(m_w[w][hh] - M);
+      Ls += e * l_w[w][hh];
+      Os += e * o_w[w][hh][dd];
+    }
+    if (Ls > 0.f) {
+      p.out[(obase + hh) * D + dd] = Os / Ls;
+      if (dd == 0) p.lse[obase + hh] = (M + log2f(Ls)) * kLn2;
+    } else if (dd == 0) {
+      p.lse[obase + hh] = -INFINITY;
+    }
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_g(const DecodeParams& p, int G, dim3 grid, cudaStream_t s) {
+  switch (G) {
+    case 1: decode_kernel<T, D, 1><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 2: decode_kernel<T, D, 2><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 4: decode_kernel<T, D, 4><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 8: decode_kernel<T, D, 8><<<grid, kWarps * 32, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace cpattn
+
+cudaError_t cp_launch_decode(const cp_decode_args& a, float scale, cudaStream_t s) {
+  using namespace cpattn;
+  DecodeParams p;
+  p.B = a.num_seqs;
+  p.Hq = a.num_q_heads;
+  p.Hkv = a.num_kv_heads;
+  p.cp = a.cp;
+  p.I = a.interleave;
+  p.S = a.num_splits;
+  p.ST = a.split_tokens;
+  p.max_blocks = a.max_blocks;
+  p.pool = a.pool_pages;
+  p.scale_log2 = scale * kLog2e;
+  p.q = a.q;
+  p.kc = a.k_cache;
+  p.vc = a.v_cache;
+  p.tables = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.err = a.err;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  dim3 grid(a.num_splits, a.num_kv_heads, a.cp * a.num_seqs);
+  if (a.dtype == CP_BF16) {
+    return a.head_dim == 64 ? launch_g<__nv_bfloat16, 64>(p, G, grid, s)
+                            : launch_g<__nv_bfloat16, 128>(p, G, grid, s);
+  }
+  return a.head_dim == 64 ? launch_g<float, 64>(p, G, grid, s) : launch_g<float, 128>(p, G, grid, s);
+}

@@ -1,0 +1,260 @@
+/*
+ * cpattn.h -- C ABI of libcpattn.so: causal GQA partial attention over logical
+ * context-parallel (CP) shards on one GB300 (sm_103a), with LSE merge.
+ *
+ * Sources (vLLM pull-request pages):
+ *   [PKV]  "Add utility functions to enable pass-kv prefill and allgather decode"
+ *          (PR 26059), Purpose: attention is the only op that couples tokens of a
+ *          sequence; in prefill both Q and KV are split over CP ranks and either the
+ *          KV shards (full prefill) or the Q shards (chunked prefill with a long
+ *          cached context) travel past the resident ones while partial attention
+ *          runs; in decode the KV stays round-robin on the ranks, the query is made
+ *          available to all of them and their partial results are combined.
+ *   [PCP]  "[Feature] Prefill Context Parallel (PCP) basic support" (PR 28718),
+ *          Purpose and code-review summary: block tables extended for decode and
+ *          prefill CP; one kv-cache interleave size shared by both.
+ *   [GQA]  "[Feature] Support Prefill Context Parallel (PCP) for GQA flashinfer"
+ *          (PR 28723), Purpose and Test Plan: token partitioning for prefill CP,
+ *          GQA attention backend, interleave size 8.
+ *
+ * All CP ranks are LOGICAL: every shard lives in this GPU's memory and no call
+ * communicates with another GPU.
+ *
+ * Conventions shared by every entry point:
+ *   - Ownership: the caller allocates and frees every buffer.  Pointers named
+ *     "device" must be device memory of the current CUDA device; "host" pointers
+ *     are read before the call returns.  The library never allocates, frees or
+ *     synchronises; work is enqueued on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream) and returns immediately.
+ *   - Errors: argument errors are detected on the host, nothing is launched and a
+ *     non-zero cp_status is returned; cp_last_error() then gives a one-line reason
+ *     (thread-local).  A failed launch returns CP_ERR_CUDA.  Conditions only the
+ *     device can see (a block-table entry outside the pool, a pipeline wait that
+ *     ran out of its iteration budget) are written to the optional device word
+ *     `err` (first error wins, CP_OK is never written) and the affected work is
+ *     skipped; read it after synchronising the stream.
+ *   - Layout: tensors are dense, row-major, in the index order written beside them,
+ *     16-byte aligned.  Heads: query head h reads kv head h / (Hq / Hkv).
+ *   - LSE values are natural-log log-sum-exp of the scaled scores; an empty key set
+ *     gives LSE = -inf and an output row that is never read (see cp_lse_merge).
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CPATTN_ABI_VERSION 1
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or shape          */
+  CP_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, dtype, block size     */
+  CP_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed                 */
+  CP_ERR_TIMEOUT = 4,       /* device: a pipeline wait exceeded its budget          */
+  CP_ERR_DEVICE_BOUNDS = 5  /* device: an index (page id, position) out of range    */
+} cp_status;
+
+typedef enum { CP_F32 = 0, CP_BF16 = 1 } cp_dtype;
+typedef enum { CP_PASS_KV = 0, CP_PASS_Q = 1 } cp_mode;
+typedef enum {
+  CP_IMPL_AUTO = 0,     /* tcgen05 tensor-core kernel for bf16, SIMT kernel for f32   */
+  CP_IMPL_TCGEN05 = 1,  /* bf16 only: TMA + tcgen05.mma + TMEM                        */
+  CP_IMPL_SIMT = 2      /* plain CUDA cores, any supported dtype (cross-check path)   */
+} cp_impl;
+
+/* Human-readable name of a cp_status value (static string). */
+const char* cp_status_string(int32_t status);
+
+/* Copies the reason for the calling thread's last failed call into buf (NUL-
+ * terminated, truncated to n bytes) and returns that call's status. */
+int32_t cp_last_error(char* buf, size_t n);
+
+/* CPATTN_ABI_VERSION of the loaded library. */
+int32_t cp_abi_version(void);
+
+/* ------------------------------------------------------------------------------
+ * cp_partition -- load-balanced token partition for prefill CP ([GQA] Purpose:
+ * token partitioning; [PKV] Purpose: Q and KV both sharded in prefill).
+ *
+ * Each sequence of T tokens is cut into 2*cp chunks with bounds
+ * b_k = floor(k*T/(2*cp)); logical rank r holds chunk r then chunk 2cp-1-r.
+ * Shard-major order lists rank 0's rows first (sequence by sequence, chunk r
+ * before chunk 2cp-1-r), then rank 1's, and so on.
+ *
+ *   cu_seqlens    device int32 [num_seqs+1], cu_seqlens[0] = 0, non-decreasing,
+ *                 cu_seqlens[num_seqs] = total_tokens (rows beyond total_tokens are
+ *                 not written).
+ *   perm          device int32 [total_tokens] or NULL: shard-major row -> token.
+ *   inv_perm      device int32 [total_tokens] or NULL: token -> shard-major row.
+ *   shard_offsets device int32 [cp+1] or NULL: first shard-major row of each rank.
+ *   chunk_bounds  device int32 [num_seqs][2cp+1] or NULL: b_k within each sequence.
+ * Requires 1 <= cp <= 64 and num_seqs*cp <= 16384.  Bit-exact integer output.
+ * ---------------------------------------------------------------------------- */
+cp_status cp_partition(const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                       int32_t cp, int32_t* perm, int32_t* inv_perm, int32_t* shard_offsets,
+                       int32_t* chunk_bounds, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * cp_kv_interleave_layout -- round-robin kv placement ([PKV] Purpose: decode KV
+ * stored round-robin on the CP ranks; [PCP] code-review summary: interleave size
+ * shared by prefill and decode CP; [PCP] Purpose: block tables per CP rank).
+ *
+ * Position p of a sequence goes to rank rho = floor(p/I) mod cp at local index
+ * l = floor(p/(I*cp))*I + p mod I (groups of I positions dealt in turn, each rank
+ * keeping arrival order).  Rank r holds
+ * L_r = floor(L/(I*cp))*I + clamp(L mod (I*cp) - r*I, 0, I) tokens of a length-L
+ * sequence.  The slot of a token in its rank's page pool is
+ * block_tables[rho][b][l / block_size] * block_size + l mod block_size.
+ *
+ *   cu_seq_lens    device int32 [num_seqs+1] prefix sums of sequence lengths.
+ *   block_tables   device int32 [cp][num_seqs][max_blocks] (needed for slots only).
+ *   local_lens     device int32 [cp][num_seqs] or NULL.
+ *   rank_of_token  device int32 [total_tokens] or NULL.
+ *   local_of_token device int32 [total_tokens] or NULL.
+ *   slot_of_token  device int64 [total_tokens] or NULL (needs block_tables).
+ *   err            device int32 or NULL: CP_ERR_DEVICE_BOUNDS if a slot needs a
+ *                  table column >= max_blocks or a negative page id (slot = -1).
+ * Bit-exact integer output.
+ * ---------------------------------------------------------------------------- */
+cp_status cp_kv_interleave_layout(const int32_t* cu_seq_lens, int32_t num_seqs,
+                                  int32_t total_tokens, int32_t cp, int32_t interleave,
+                                  int32_t block_size, const int32_t* block_tables,
+                                  int32_t max_blocks, int32_t* local_lens, int32_t* rank_of_token,
+                                  int32_t* local_of_token, int64_t* slot_of_token, int32_t* err,
+                                  void* stream);
+
+/* ------------------------------------------------------------------------------
+ * cp_partial_attn_prefill -- partial attention for every (Q shard, KV shard) pair
+ * ([PKV] Purpose: pass-KV for full prefill, pass-Q for chunked prefill; the
+ * exchange itself is logical here, so one launch covers every rotation step).
+ *
+ * PASS_KV (self-attention of each sequence, q = k = v tokens):
+ *   partial s of query token i (position i in its sequence) is attention of i
+ *   over the keys of kv shard s (chunks s and 2cp-1-s, see cp_partition) with
+ *   position <= i.  Q rows of shard r are the tokens of chunks r and 2cp-1-r.
+ * PASS_Q (chunked prefill over a paged, round-robin cache):
+ *   sequence b has q_len_b = cu_seqlens_q[b+1]-cu_seqlens_q[b] new queries at
+ *   positions C_b .. C_b+q_len_b-1, C_b = seq_lens_kv[b] - q_len_b, and
+ *   seq_lens_kv[b] kv tokens (cached + new, already written) placed as in
+ *   cp_kv_interleave_layout.  Partial r of a query is its attention over rank r's
+ *   resident tokens with position <= its own.  Q rows of shard r are chunks r and
+ *   2cp-1-r of the new tokens (the math does not depend on this split).
+ *
+ * Outputs: out[p][row][h][:] f32 (normalised over partial p's keys) and
+ * lse[p][row][h] f32, p = kv shard / kv rank, row = token-major query row.  Pairs
+ * with no visible key get lse = -inf and their out rows are left unwritten.
+ * q_shard / kv_shard >= 0 restrict the launch to that Q shard / KV shard (one
+ * logical rotation step); outputs of other pairs are left untouched.
+ * ---------------------------------------------------------------------------- */
+typedef struct cp_prefill_args {
+  int32_t mode;                 /* cp_mode                                              */
+  int32_t dtype;                /* cp_dtype of q, k, v, k_cache, v_cache                */
+  int32_t impl;                 /* cp_impl                                              */
+  int32_t num_seqs;             /* B >= 1                                               */
+  int32_t num_q_heads;          /* Hq, multiple of num_kv_heads                         */
+  int32_t num_kv_heads;         /* Hkv                                                  */
+  int32_t head_dim;             /* d in {64, 128}                                       */
+  int32_t cp;                   /* logical ranks, 1..64                                 */
+  int32_t max_seqlen_q;         /* host: max new-query tokens of a sequence            */
+  float softmax_scale;          /* <= 0 selects 1/sqrt(head_dim)                        */
+  const int32_t* cu_seqlens_q;  /* device [B+1] token-major query rows                  */
+  const int32_t* seq_lens_kv;   /* PASS_Q: device [B] cached + new kv tokens            */
+  const void* q;                /* device [Nq][Hq][d]                                   */
+  const void* k;                /* PASS_KV: device [Nq][Hkv][d]                         */
+  const void* v;                /* PASS_KV: device [Nq][Hkv][d]                         */
+  const void* k_cache;          /* PASS_Q: device [cp][pool_pages][Hkv][block_size][d]  */
+  const void* v_cache;          /* PASS_Q: same layout as k_cache                       */
+  int64_t pool_pages;           /* PASS_Q: pages in each rank's pool                    */
+  const int32_t* block_tables;  /* PASS_Q: device [cp][B][max_blocks] page ids          */
+  int32_t max_blocks;           /* PASS_Q                                               */
+  int32_t block_size;           /* PASS_Q: 16                                           */
+  int32_t interleave;           /* PASS_Q: I >= 1                                       */
+  int32_t q_shard;              /* -1 = all                                             */
+  int32_t kv_shard;             /* -1 = all                                             */
+  int32_t total_q;              /* host: Nq = cu_seqlens_q[B], rows of q/out/lse        */
+  float* out;                   /* device [cp][Nq][Hq][d] f32                           */
+  float* lse;                   /* device [cp][Nq][Hq] f32                              */
+  int32_t* err;                 /* device int32 or NULL                                 */
+} cp_prefill_args;
+
+cp_status cp_partial_attn_prefill(const cp_prefill_args* args, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * cp_partial_attn_decode -- per-rank partial attention of one new query token per
+ * sequence over a round-robin paged cache ([PKV] Purpose: allgather decode, KV
+ * round-robin on the ranks; [PCP] Purpose: per-rank block tables).
+ *
+ * The query of sequence b is at position seq_lens[b]-1 (its own kv entry is
+ * already cached) and attends every token of the sequence; rank r's share is its
+ * L_r resident tokens (local indices 0..L_r-1, see cp_kv_interleave_layout), cut
+ * into num_splits ranges of split_tokens local tokens.  Partial p = r*num_splits+s.
+ *
+ *   q       device [B][Hq][d];  k_cache/v_cache as in cp_prefill_args.
+ *   out     device f32 [cp*num_splits][B][Hq][d]; lse f32 [cp*num_splits][B][Hq].
+ * Every split range must be covered: num_splits*split_tokens >= max_r L_r, which
+ * cp_decode_plan guarantees; split_tokens is a multiple of block_size.
+ * ---------------------------------------------------------------------------- */
+typedef struct cp_decode_args {
+  int32_t dtype;                /* cp_dtype of q and caches                             */
+  int32_t num_seqs;             /* B                                                    */
+  int32_t num_q_heads;          /* Hq                                                   */
+  int32_t num_kv_heads;         /* Hkv                                                  */
+  int32_t head_dim;             /* d in {64, 128}                                       */
+  int32_t cp;                   /* logical ranks                                        */
+  int32_t interleave;           /* I                                                    */
+  int32_t block_size;           /* 16                                                   */
+  int32_t num_splits;           /* >= 1                                                 */
+  int32_t split_tokens;         /* rank-local tokens per split                          */
+  float softmax_scale;          /* <= 0 selects 1/sqrt(head_dim)                        */
+  int32_t max_blocks;           /* columns of block_tables                              */
+  int64_t pool_pages;           /* pages in each rank's pool                            */
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;  /* device [cp][B][max_blocks]                           */
+  const int32_t* seq_lens;      /* device [B], 1 <= seq_lens[b] <= max_seq_len          */
+  float* out;
+  float* lse;
+  int32_t* err;
+} cp_decode_args;
+
+/* Host-side split planning: picks split_tokens (multiple of block_size) and
+ * num_splits so that num_splits*split_tokens covers the largest rank share of a
+ * sequence of max_seq_len tokens and the grid fills the GPU. */
+cp_status cp_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t cp, int32_t interleave,
+                         int32_t block_size, int32_t max_seq_len, int32_t* num_splits,
+                         int32_t* split_tokens);
+
+cp_status cp_partial_attn_decode(const cp_decode_args* args, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * cp_lse_merge -- combine P partials into exact attention (the combine step after
+ * partial attention, [PKV] Purpose).
+ *
+ *   M = max_p lse_p;  w_p = exp(lse_p - M) (0 for lse_p = -inf);
+ *   out = sum_p w_p * out_p / sum_p w_p;  out_lse = M + log(sum_p w_p).
+ * A partial with lse = -inf is never read.  All partials empty gives out = 0 and
+ * out_lse = -inf.
+ *
+ *   partial_out  device f32 [P][rows][H][d];  partial_lse device f32 [P][rows][H].
+ *   out          device [rows][H][d] of out_dtype (bf16: round to nearest even).
+ *   out_lse      device f32 [rows][H] or NULL.
+ * ---------------------------------------------------------------------------- */
+cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32_t num_partials,
+                       int64_t rows, int32_t num_heads, int32_t head_dim, void* out,
+                       int32_t out_dtype, float* out_lse, void* stream);
+
+/* sizeof() of the argument structs, so bindings can check their mirror. */
+size_t cp_prefill_args_size(void);
+size_t cp_decode_args_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H */

@@ -1,0 +1,58 @@
+"""Shared helpers of the GPU parity tests: tolerance checks against the float64 oracle.
+
+Tolerances (bf16 inputs, fp32 accumulation):
+  * outputs: max |O_gpu - O_oracle| <= 1e-2 (also for bf16-rounded merged outputs: |O| is at
+    most a few units here and bf16 rounding adds <= 2^-9 |O|);
+  * LSE: |LSE_gpu - LSE_oracle| <= 1e-3 |LSE_oracle| + 1e-5.  The absolute floor covers rows
+    whose LSE is near 0: fp32 dot products of 128 bf16 products of unit scale carry ~1e-6
+    absolute error, far inside 1e-5;
+  * an empty partial must be empty (-inf) on both sides: that set is decided by integers
+    (positions, chunk bounds, round-robin ranks), so it is compared exactly.
+"""
+import numpy as np
+import torch
+
+ATOL_O = 1e-2
+RTOL_LSE = 1e-3
+ATOL_LSE = 1e-5
+
+
+def to_np(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def check_partials(out, lse, O_ref, L_ref, rows=None, what=""):
+    """out [P, R, H, d], lse [P, R, H] (GPU, full) vs oracle [P, R', H, d] on rows (or all)."""
+    if rows is not None:
+        idx = torch.as_tensor(rows, device=lse.device, dtype=torch.long)
+        out = out.index_select(1, idx)
+        lse = lse.index_select(1, idx)
+    lse = to_np(lse)
+    out = to_np(out)
+    fin_ref = np.isfinite(L_ref)
+    fin = np.isfinite(lse)
+    assert not np.isnan(lse).any(), f"{what}: NaN in lse"
+    assert np.array_equal(fin, fin_ref), f"{what}: empty-partial sets differ " \
+        f"({int((fin != fin_ref).sum())} entries)"
+    dl = np.abs(lse[fin] - L_ref[fin])
+    tol = RTOL_LSE * np.abs(L_ref[fin]) + ATOL_LSE
+    assert (dl <= tol).all(), f"{what}: lse max err {dl.max():.3e} (worst ratio {(dl / tol).max():.2f})"
+    do = np.abs(out[fin] - O_ref[fin])
+    assert np.isfinite(out[fin]).all(), f"{what}: non-finite output"
+    assert do.max(initial=0) <= ATOL_O, f"{what}: out max err {do.max():.3e}"
+    return float(do.max(initial=0)), float(dl.max(initial=0))
+
+
+def check_merged(out, lse, O_ref, L_ref, what=""):
+    out = to_np(out)
+    do = np.abs(out - O_ref)
+    assert np.isfinite(out).all(), f"{what}: non-finite output"
+    assert do.max(initial=0) <= ATOL_O, f"{what}: merged out max err {do.max():.3e}"
+    if lse is not None:
+        lse = to_np(lse)
+        fin = np.isfinite(L_ref)
+        assert np.array_equal(np.isfinite(lse), fin)
+        dl = np.abs(lse[fin] - L_ref[fin])
+        assert (dl <= RTOL_LSE * np.abs(L_ref[fin]) + ATOL_LSE).all(), \
+            f"{what}: merged lse max err {dl.max():.3e}"
+    return float(do.max(initial=0))

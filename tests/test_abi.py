@@ -1,0 +1,90 @@
+"""The C ABI library loads on a machine without a GPU and exports every function that
+include/*.h declares; host-side validation rejects bad arguments before any launch."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import context_gqa_attention_gb300 as cpa
+from context_gqa_attention_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(cp_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return cpa.load()
+
+
+def test_header_declares_the_boundary():
+    want = {"cp_partition", "cp_kv_interleave_layout", "cp_partial_attn_prefill",
+            "cp_partial_attn_decode", "cp_lse_merge", "cp_decode_plan"}
+    assert want <= _declared()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(_build.LIB)
+    for name in sorted(_declared()):
+        assert hasattr(raw, name), name
+    assert set(cpa.EXPORTED) <= _declared()
+
+
+def test_struct_mirrors_match(lib):
+    assert lib.cp_prefill_args_size() == ctypes.sizeof(cpa.PrefillArgs)
+    assert lib.cp_decode_args_size() == ctypes.sizeof(cpa.DecodeArgs)
+    assert lib.cp_abi_version() == 1
+    assert lib.cp_status_string(5) == b"CP_ERR_DEVICE_BOUNDS"
+
+
+def _last(lib):
+    buf = ctypes.create_string_buffer(256)
+    st = lib.cp_last_error(buf, 256)
+    return st, buf.value.decode()
+
+
+def test_invalid_arguments_are_rejected_on_the_host(lib):
+    # null / bad pointers and sizes return an error without touching the device
+    assert lib.cp_partition(None, 1, 10, 2, None, None, None, None, None) == 1
+    assert "cu_seqlens" in _last(lib)[1]
+    assert lib.cp_partition(ctypes.c_void_p(16), 1, 10, 0, ctypes.c_void_p(16), None, None, None,
+                            None) == 1
+    assert lib.cp_lse_merge(ctypes.c_void_p(16), ctypes.c_void_p(16), 2, 4, 2, 96,
+                            ctypes.c_void_p(16), 1, None, None) == 1
+    assert lib.cp_lse_merge(ctypes.c_void_p(18), ctypes.c_void_p(16), 2, 4, 2, 128,
+                            ctypes.c_void_p(16), 1, None, None) == 1   # misaligned
+    a = cpa.PrefillArgs()
+    a.mode, a.dtype, a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.cp = 0, 1, 1, 6, 4, 128, 2
+    assert lib.cp_partial_attn_prefill(ctypes.byref(a), None) == 1      # Hq % Hkv != 0
+    assert "multiple" in _last(lib)[1]
+    a.num_q_heads, a.head_dim = 8, 96
+    assert lib.cp_partial_attn_prefill(ctypes.byref(a), None) == 2      # unsupported head_dim
+    d = cpa.DecodeArgs()
+    d.dtype, d.num_seqs, d.num_q_heads, d.num_kv_heads, d.head_dim = 1, 1, 32, 8, 128
+    d.cp, d.interleave, d.block_size, d.num_splits, d.split_tokens = 2, 8, 32, 1, 64
+    assert lib.cp_partial_attn_decode(ctypes.byref(d), None) == 2       # block size 32
+    d.block_size, d.split_tokens = 16, 40
+    assert lib.cp_partial_attn_decode(ctypes.byref(d), None) == 1       # split not page multiple
+
+
+def test_decode_plan_covers_every_rank_share(lib):
+    for B, Hkv, cp, I, L in [(64, 8, 2, 8, 32768), (1, 1, 1, 1, 1), (3, 2, 4, 8, 1000),
+                             (64, 8, 2, 8, 1024), (2, 8, 8, 16, 5)]:
+        ns, st = ctypes.c_int32(), ctypes.c_int32()
+        assert lib.cp_decode_plan(B, Hkv, cp, I, 16, L, ctypes.byref(ns), ctypes.byref(st)) == 0
+        group = I * cp
+        share = (L // group) * I + min(L % group, I)
+        assert st.value % 16 == 0 and ns.value * st.value >= share
+        assert (ns.value - 1) * st.value < max(share, 1)

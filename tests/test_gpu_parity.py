@@ -1,0 +1,239 @@
+"""GPU parity: every C-ABI entry point against the float64 oracle on the same seeded inputs.
+
+Small cases span several tiles and ragged tails; index maps are compared bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import cp_oracle as orc
+import workloads as wl
+from tests.parity_util import check_merged, check_partials, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _cu(lens):
+    cu = [0]
+    for x in lens:
+        cu.append(cu[-1] + x)
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+# ------------------------------------------------------------------------------------ maps
+
+@pytest.mark.parametrize("lens,cp", [([256], 2), ([8192], 2), ([32768, 32768], 4), ([37, 5, 64, 1], 4),
+                                     ([3], 4), ([100, 200, 0, 7], 8), ([1, 2, 3, 17], 1),
+                                     ([2048] * 4, 4), ([1000] * 37, 3)])
+def test_partition_bitexact(lib, lens, cp):
+    cu = _cu(lens)
+    perm, inv, so, cb = lib.cp_partition(cu.to(DEV), cp, sum(lens))
+    ref = orc.partition(lens, cp)
+    assert perm.cpu().numpy().tolist() == ref["perm"].tolist()
+    assert inv.cpu().numpy().tolist() == ref["inv_perm"].tolist()
+    assert so.cpu().numpy().tolist() == ref["shard_offsets"].tolist()
+    assert cb.cpu().numpy().tolist() == ref["chunk_bounds"].tolist()
+
+
+@pytest.mark.parametrize("lens,cp,I", [([40], 2, 8), ([37, 100, 1, 64], 2, 8), ([32768] * 4, 4, 8),
+                                       ([1023, 5000, 16], 3, 4), ([77], 8, 1), ([9, 130], 1, 16)])
+def test_interleave_bitexact(lib, lens, cp, I):
+    bs = 16
+    caps = [wl.block_capacity(L, cp, I, bs) for L in lens]
+    tables, pool = wl.shuffled_block_tables(caps, cp, torch.Generator().manual_seed(7))
+    cu = _cu(lens)
+    ll, rk, lc, sl = lib.cp_kv_interleave_layout(cu.to(DEV), cp, I, sum(lens), bs,
+                                                 block_tables=tables.to(DEV))
+    rank, local, slot = orc.slot_mapping(lens, cp, I, bs, tables)
+    assert ll.cpu().numpy().tolist() == orc.local_lengths(lens, cp, I).tolist()
+    assert rk.cpu().numpy().tolist() == rank.tolist()
+    assert lc.cpu().numpy().tolist() == local.tolist()
+    assert sl.cpu().numpy().tolist() == slot.tolist()
+
+
+def test_interleave_reports_bad_table(lib):
+    lens, cp, I = [64], 2, 8
+    tables = torch.full((cp, 1, 1), 3, dtype=torch.int32)   # one column: too short for 32 tokens
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    _, _, _, sl = lib.cp_kv_interleave_layout(_cu(lens).to(DEV), cp, I, 64, 16,
+                                              block_tables=tables.to(DEV), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 5
+    assert (sl.cpu() == -1).sum().item() == 32
+
+
+# ------------------------------------------------------------------------------------ merge
+
+@pytest.mark.parametrize("P,rows,H,d,dt", [(2, 1000, 16, 128, torch.bfloat16), (5, 77, 3, 64, torch.float32),
+                                           (64, 33, 32, 128, torch.bfloat16), (1, 9, 2, 128, torch.float32)])
+def test_merge_parity(lib, P, rows, H, d, dt):
+    g = torch.Generator().manual_seed(P * 1000 + rows)
+    O = torch.randn(P, rows, H, d, generator=g)
+    L = torch.randn(P, rows, H, generator=g) * 4
+    L[torch.rand(P, rows, H, generator=g) < 0.3] = -math.inf   # empty partials
+    L[:, 0, 0] = -math.inf                                      # a fully empty unit
+    O[torch.isinf(L)] = float("nan")                            # never read when empty
+    out, lse = lib.cp_lse_merge(O.to(DEV), L.to(DEV), out_dtype=dt)
+    Or, Lr = orc.lse_merge(O.numpy(), L.numpy())
+    check_merged(out, lse, Or, Lr, what="merge")
+
+
+# ------------------------------------------------------------------------------------ prefill
+
+def _impl_code(lib, name):
+    return {"simt": lib.CP_IMPL_SIMT, "tc": lib.CP_IMPL_TCGEN05}[name]
+
+
+PASS_KV_CASES = [
+    # lens, Hq, Hkv, d, dtype, cp
+    ([256], 4, 1, 64, torch.float32, 2),          # the tiny workload
+    ([1000, 333, 1], 8, 2, 128, torch.bfloat16, 2),
+    ([700, 129], 16, 2, 128, torch.bfloat16, 4),
+    ([515], 4, 4, 64, torch.bfloat16, 3),
+    ([300, 5], 8, 1, 128, torch.bfloat16, 8),
+    ([640], 8, 2, 128, torch.float32, 1),
+]
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("case", range(len(PASS_KV_CASES)))
+def test_pass_kv_parity(lib, case, impl):
+    lens, Hq, Hkv, d, dt, cp = PASS_KV_CASES[case]
+    if impl == "tc" and dt != torch.bfloat16:
+        pytest.skip("the tensor-core kernel takes bf16")
+    x = wl.prefill_inputs(lens, Hq, Hkv, d, dt, seed=100 + case)
+    scale = 1.0 / math.sqrt(d)
+    out, lse = lib.cp_partial_attn_prefill(
+        x["q"].to(DEV), x["cu_seqlens"].to(DEV), cp, k=x["k"].to(DEV), v=x["v"].to(DEV),
+        max_seqlen_q=max(lens), impl=_impl_code(lib, impl))
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], cp, scale)
+    check_partials(out, lse, O, L, what=f"pass-KV {impl} partials")
+    mo, ml = lib.cp_lse_merge(out, lse, out_dtype=dt)
+    Om, Lm = orc.lse_merge(O, L)
+    check_merged(mo, ml, Om, Lm, what=f"pass-KV {impl} merged")
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+def test_pass_kv_single_pair(lib, impl):
+    """q_shard / kv_shard restrict the launch to one rotation step; other pairs untouched."""
+    lens, Hq, Hkv, d, cp = [900], 8, 2, 128, 4
+    x = wl.prefill_inputs(lens, Hq, Hkv, d, torch.bfloat16, seed=55)
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], cp, 1 / math.sqrt(d))
+    part = orc.partition(lens, cp)
+    out = torch.full((cp, 900, Hq, d), 7.0, device=DEV)
+    lse = torch.full((cp, 900, Hq), 7.0, device=DEV)
+    qs, ks = 1, 2
+    lib.cp_partial_attn_prefill(x["q"].to(DEV), x["cu_seqlens"].to(DEV), cp, k=x["k"].to(DEV),
+                                v=x["v"].to(DEV), q_shard=qs, kv_shard=ks, out=out, lse=lse,
+                                impl=_impl_code(lib, impl), max_seqlen_q=900)
+    rows = part["perm"][part["shard_offsets"][qs]:part["shard_offsets"][qs + 1]]
+    check_partials(out[ks:ks + 1], lse[ks:ks + 1], O[ks:ks + 1][:, rows], L[ks:ks + 1][:, rows],
+                   rows=rows.tolist(), what="single pair")
+    mask = torch.ones(cp, 900, dtype=torch.bool)
+    mask[ks, torch.as_tensor(rows)] = False
+    assert (lse.cpu()[mask] == 7.0).all()
+
+
+def _paged_case(B, q_lens, kv_lens, Hq, Hkv, d, dt, cp, I, seed):
+    g = torch.Generator().manual_seed(seed)
+    caps = [wl.block_capacity(L, cp, I, 16) for L in kv_lens]
+    tables, pool = wl.shuffled_block_tables(caps, cp, torch.Generator().manual_seed(seed + 1))
+    q = wl.normal((sum(q_lens), Hq, d), dt, g)
+    kc = wl.normal((cp, pool, Hkv, 16, d), dt, g)
+    vc = wl.normal((cp, pool, Hkv, 16, d), dt, g)
+    return dict(q=q, k_cache=kc, v_cache=vc, block_tables=tables, cu_seqlens_q=_cu(q_lens),
+                seq_lens=torch.tensor(kv_lens, dtype=torch.int32))
+
+
+PASS_Q_CASES = [
+    # q_lens, kv_lens, Hq, Hkv, d, dtype, cp, I
+    ([100, 37], [700, 300], 8, 2, 128, torch.bfloat16, 4, 8),
+    ([256], [256], 16, 2, 128, torch.bfloat16, 2, 8),          # no cached context
+    ([130, 1, 64], [1000, 1, 64], 4, 1, 64, torch.bfloat16, 3, 4),
+    ([50], [2000], 8, 8, 128, torch.float32, 2, 16),
+    ([200], [1500], 8, 2, 128, torch.bfloat16, 1, 8),
+]
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("case", range(len(PASS_Q_CASES)))
+def test_pass_q_parity(lib, case, impl):
+    q_lens, kv_lens, Hq, Hkv, d, dt, cp, I = PASS_Q_CASES[case]
+    if impl == "tc" and dt != torch.bfloat16:
+        pytest.skip("the tensor-core kernel takes bf16")
+    x = _paged_case(len(q_lens), q_lens, kv_lens, Hq, Hkv, d, dt, cp, I, 300 + case)
+    out, lse = lib.cp_partial_attn_prefill(
+        x["q"].to(DEV), x["cu_seqlens_q"].to(DEV), cp, mode=lib.CP_PASS_Q,
+        k_cache=x["k_cache"].to(DEV), v_cache=x["v_cache"].to(DEV),
+        block_tables=x["block_tables"].to(DEV), seq_lens_kv=x["seq_lens"].to(DEV), interleave=I,
+        max_seqlen_q=max(q_lens), impl=_impl_code(lib, impl))
+    O, L = orc.pass_q_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                               x["cu_seqlens_q"], x["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
+    check_partials(out, lse, O, L, what=f"pass-Q {impl} partials")
+    mo, ml = lib.cp_lse_merge(out, lse, out_dtype=dt)
+    Om, Lm = orc.lse_merge(O, L)
+    check_merged(mo, ml, Om, Lm, what=f"pass-Q {impl} merged")
+
+
+def test_pass_q_reports_bad_page(lib):
+    x = _paged_case(1, [20], [100], 4, 1, 64, torch.bfloat16, 2, 8, 9)
+    tables = x["block_tables"].clone()
+    tables[1, 0, 1] = 10 ** 6          # outside the pool: the kernel checks before reading
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lib.cp_partial_attn_prefill(x["q"].to(DEV), x["cu_seqlens_q"].to(DEV), 2, mode=lib.CP_PASS_Q,
+                                k_cache=x["k_cache"].to(DEV), v_cache=x["v_cache"].to(DEV),
+                                block_tables=tables.to(DEV), seq_lens_kv=x["seq_lens"].to(DEV),
+                                interleave=8, impl=lib.CP_IMPL_SIMT, err=err, max_seqlen_q=20)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 5
+
+
+# ------------------------------------------------------------------------------------ decode
+
+DECODE_CASES = [
+    # B, lens range, Hq, Hkv, d, dtype, cp, I
+    (5, (1, 3000), 32, 8, 128, torch.bfloat16, 2, 8),
+    (3, (1, 40), 16, 2, 64, torch.bfloat16, 4, 8),
+    (7, (500, 900), 8, 8, 128, torch.float32, 3, 4),
+    (2, (1000, 2000), 16, 16, 64, torch.bfloat16, 1, 8),
+]
+
+
+@pytest.mark.parametrize("case", range(len(DECODE_CASES)))
+def test_decode_parity(lib, case):
+    B, (lo, hi), Hq, Hkv, d, dt, cp, I = DECODE_CASES[case]
+    lens = wl.decode_lengths(B, lo, hi, seed=400 + case).tolist()
+    lens[0] = hi                                   # longest sequence present
+    x = wl.paged_inputs(B, 1, lens, Hq, Hkv, d, dt, cp, I, 16, 500 + case, 600 + case,
+                        q_is_decode=True)
+    out, lse = lib.cp_partial_attn_decode(
+        x["q"].to(DEV), x["k_cache"].to(DEV), x["v_cache"].to(DEV), x["block_tables"].to(DEV),
+        x["seq_lens"].to(DEV), cp, I, max_seq_len=max(lens))
+    O, L = orc.decode_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"], x["seq_lens"],
+                               cp, I, 16, 1 / math.sqrt(d))
+    mo, ml = lib.cp_lse_merge(out, lse, out_dtype=dt)
+    Om, Lm = orc.lse_merge(O, L)
+    check_merged(mo, ml, Om, Lm, what="decode merged")
+    # per-rank partials: merge the GPU's splits of each rank and compare with the oracle's rank
+    S = out.shape[0] // cp
+    for r in range(cp):
+        ro, rl = lib.cp_lse_merge(out[r * S:(r + 1) * S].contiguous(),
+                                  lse[r * S:(r + 1) * S].contiguous(), out_dtype=torch.float32)
+        check_partials(ro[None], rl[None], O[r:r + 1], L[r:r + 1], what=f"decode rank {r}")
+
+
+def test_decode_explicit_single_split(lib):
+    """One split per rank: the decode partials are exactly the per-rank partials."""
+    B, Hq, Hkv, d, cp, I = 3, 16, 4, 128, 2, 8
+    lens = [33, 1, 250]
+    x = wl.paged_inputs(B, 1, lens, Hq, Hkv, d, torch.bfloat16, cp, I, 16, 11, 12, q_is_decode=True)
+    out, lse = lib.cp_partial_attn_decode(
+        x["q"].to(DEV), x["k_cache"].to(DEV), x["v_cache"].to(DEV), x["block_tables"].to(DEV),
+        x["seq_lens"].to(DEV), cp, I, num_splits=1, split_tokens=128)
+    O, L = orc.decode_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"], x["seq_lens"],
+                               cp, I, 16, 1 / math.sqrt(d))
+    check_partials(out, lse, O, L, what="decode single split")
