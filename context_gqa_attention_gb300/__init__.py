@@ -53,7 +53,8 @@ class PrefillArgs(ctypes.Structure):
         ("k_cache", _vp), ("v_cache", _vp), ("pool_pages", ctypes.c_int64),
         ("block_tables", _vp), ("max_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("interleave", ctypes.c_int32), ("q_shard", ctypes.c_int32), ("kv_shard", ctypes.c_int32),
-        ("total_q", ctypes.c_int32), ("out", _vp), ("lse", _vp), ("err", _vp),
+        ("total_q", ctypes.c_int32), ("debug", ctypes.c_int32), ("out", _vp), ("lse", _vp),
+        ("err", _vp),
     ]
 
 
@@ -210,7 +211,7 @@ def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=N
                             k_cache=None, v_cache=None, block_tables=None, seq_lens_kv=None,
                             interleave=8, max_seqlen_q=None, softmax_scale=0.0,
                             impl=CP_IMPL_AUTO, q_shard=-1, kv_shard=-1, out=None, lse=None,
-                            err=None, stream=None):
+                            err=None, debug=0, stream=None):
     """Partial attention of every (Q shard, KV shard) pair (see cpattn.h).
 
     q: [Nq, Hq, d].  PASS_KV: k, v [Nq, Hkv, d].  PASS_Q: k_cache/v_cache
@@ -231,6 +232,7 @@ def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=N
     a.softmax_scale = softmax_scale
     a.total_q = Nq
     a.q_shard, a.kv_shard = q_shard, kv_shard
+    a.debug = debug
     _dev(q, "q")
     _dev(cu_seqlens_q, "cu_seqlens_q", torch.int32)
     _dev(out, "out", torch.float32)

@@ -323,6 +323,7 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   REQUIRE(a->total_q >= 0 && a->max_seqlen_q >= 0, "total_q / max_seqlen_q must be >= 0");
   REQUIRE(a->q_shard >= -1 && a->q_shard < a->cp, "q_shard out of range");
   REQUIRE(a->kv_shard >= -1 && a->kv_shard < a->cp, "kv_shard out of range");
+  REQUIRE(a->debug == 0 || a->debug == 1, "debug must be 0 or 1");
   REQUIRE(a->cu_seqlens_q != nullptr, "cu_seqlens_q is null");
   REQUIRE_PTR(a->q);
   REQUIRE_PTR(a->out);

@@ -1,7 +1,589 @@
-// Tensor-core (tcgen05) partial attention -- filled in by the sm_103a kernel.
-#include "common.cuh"
+// Partial attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), bf16 in,
+// f32 accumulate.
+//
+// Pairs: "Add utility functions to enable pass-kv prefill and allgather decode" (vLLM PR
+// 26059), Purpose -- pass-KV (Q tile of chunk c against kv shard s = chunks s, 2cp-1-s) and
+// pass-Q (Q tile against kv rank r's round-robin resident tokens in paged storage, "[Feature]
+// Prefill Context Parallel (PCP) basic support" (PR 28718), Purpose: per-rank block tables).
+//
+// One CTA = one work item (128 query rows of one head) x (one kv shard / rank):
+//   warp 0      TMA producer: Q once, then K and V tiles (128 keys) into a 2-stage ring;
+//               paged kv arrives page by page (16 rows per copy).
+//   warp 1      TMEM owner and MMA issuer (one thread): S = Q K^T into one of two TMEM S
+//               buffers, then O += P V into the TMEM O accumulator.
+//   warps 2-5   softmax warpgroup: thread i owns query row i (TMEM lane i): reads its S row
+//               with tcgen05.ld, masks by position, keeps the running max / sum, rescales
+//               O in TMEM only when the max grows by more than 2^8, writes P (bf16) to shared
+//               memory in the 128-byte-swizzled K-major layout the MMA reads, and finally
+//               normalises O and writes the partial output and its LSE.
+// QK^T of tile t+1 runs on the tensor cores while the softmax of tile t runs.
+// Every wait is bounded; on expiry the CTA raises CP_ERR_TIMEOUT, drains its own copies and
+// MMAs, frees TMEM and returns.
+#include <cuda.h>
 
-bool cp_prefill_tc_supported(const cp_prefill_args&) { return false; }
-cudaError_t cp_launch_prefill_tc(const cp_prefill_args&, float, cudaStream_t) {
-  return cudaErrorNotSupported;
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace cpattn {
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128;          // query rows per tile (TMEM lanes)
+constexpr int BN = 128;          // keys per tile
+constexpr int NS = 2;            // K/V pipeline stages (the drain below assumes 2)
+constexpr int kThreads = 192;
+constexpr long long kBudget = 4000000000ll;  // SM cycles per wait (~2 s)
+constexpr float kRescaleThreshold = 8.f;     // log2 units
+
+struct TcParams {
+  int mode, B, Hq, Hkv, cp, I, max_blocks, q_shard, kv_shard, TPC, Nq, debug;
+  long long pool, budget;
+  float scale_log2;
+  const int32_t* cu_q;
+  const int32_t* seq_lens_kv;
+  const int32_t* tables;
+  float* out;
+  float* lse;
+  int32_t* err;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kQ = BM * D * 2;
+  static constexpr int kKV = BN * D * 2;
+  static constexpr int kP = BM * BN * 2;
+  static constexpr int oQ = 0;
+  static constexpr int oK = oQ + kQ;
+  static constexpr int oV = oK + NS * kKV;
+  static constexpr int oP = oV + NS * kKV;
+  static constexpr int oBar = oP + kP;
+  static constexpr int bQ = 0, bKF = 1, bVF = bKF + NS, bKE = bVF + NS, bVE = bKE + NS,
+                       bS = bVE + NS, bP = bS + 2, bO = bP + 1, bDone = bO + 1, nBar = bDone + 1;
+  static constexpr int oMisc = oBar + nBar * 8;
+  static constexpr int kBytes = oMisc + 16;
+  // +1 KB so the base can be rounded up to the 1 KB swizzle-atom alignment; never below
+  // 120 KB so that a single CTA (and its 512 TMEM columns) occupies an SM.
+  static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+};
+
+struct Work {
+  int valid, b, h, g, p;
+  int q_row0, q_lo, q_hi;   // first token-major row; tile rows [q_lo, q_hi) of the sequence
+  long long qpos0;          // position of row q_lo
+  int kv_row0;              // pass-KV: first token-major kv row of the sequence
+  int ks[2], ke[2], nt[2];  // pass-KV key ranges (positions) and their tile counts
+  int n_local;              // pass-Q: resident tokens of rank p that any row can see
+  int ntiles;
+};
+
+CP_DEV Work decode_work(const TcParams& p) {
+  Work w;
+  w.valid = 0;
+  long long lin = blockIdx.x;
+  w.h = (int)(lin % p.Hq);
+  lin /= p.Hq;
+  if (p.kv_shard >= 0) {
+    w.p = p.kv_shard;
+  } else {
+    w.p = (int)(lin % p.cp);
+    lin /= p.cp;
+  }
+  w.b = (int)(lin % p.B);
+  lin /= p.B;
+  const int slot = (int)lin;  // heaviest tiles first: last chunk, last tile
+  const int c = 2 * p.cp - 1 - slot / p.TPC;
+  const int j = p.TPC - 1 - slot % p.TPC;
+  const int q0 = p.cu_q[w.b];
+  const int Tq = p.cu_q[w.b + 1] - q0;
+  if (Tq <= 0) return w;
+  const int cs = chunk_bound(c, Tq, p.cp), ce = chunk_bound(c + 1, Tq, p.cp);
+  w.q_lo = cs + j * BM;
+  if (w.q_lo >= ce) return w;
+  w.q_hi = min(w.q_lo + BM, ce);
+  if (p.q_shard >= 0 && shard_of_chunk(c, p.cp) != p.q_shard) return w;
+  w.valid = 1;
+  w.g = w.h / (p.Hq / p.Hkv);
+  w.q_row0 = q0 + w.q_lo;
+  w.ntiles = 0;
+  if (p.mode == CP_PASS_KV) {
+    w.qpos0 = w.q_lo;
+    w.kv_row0 = q0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int ch = i == 0 ? w.p : 2 * p.cp - 1 - w.p;
+      w.ks[i] = chunk_bound(ch, Tq, p.cp);
+      w.ke[i] = min(chunk_bound(ch + 1, Tq, p.cp), w.q_hi);  // positions < q_hi
+      if (w.ke[i] < w.ks[i]) w.ke[i] = w.ks[i];
+      w.nt[i] = (w.ke[i] - w.ks[i] + BN - 1) / BN;
+      w.ntiles += w.nt[i];
+    }
+  } else {
+    const long long C = (long long)p.seq_lens_kv[w.b] - Tq;
+    w.qpos0 = C + w.q_lo;
+    w.n_local = rank_local_len(C + w.q_hi, w.p, p.cp, p.I);
+    w.ntiles = (w.n_local + BN - 1) / BN;
+  }
+  return w;
+}
+
+CP_DEV uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+CP_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+CP_DEV void fail_timeout(volatile uint32_t* abort_flag, int32_t* err) {
+  *abort_flag = 1u;
+  report(err, CP_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------------- kernel
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q,
+                      const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_v, const TcParams p) {
+  using Ly = Layout<D>;
+  constexpr int KB = D / 64;  // 64-column (128-byte) blocks of a head row
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Work w = decode_work(p);
+  if (!w.valid) return;  // uniform over the CTA
+
+  if (w.ntiles == 0) {  // no visible key in this pair: an empty partial
+    if (warp >= 2) {
+      const int row = (warp & 3) * 32 + lane;
+      if (w.q_lo + row < w.q_hi)
+        p.lse[((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h] = -INFINITY;
+    }
+    return;
+  }
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + Ly::oQ, sK = base + Ly::oK, sV = base + Ly::oV, sP = base + Ly::oP;
+  const uint32_t bars = base + Ly::oBar;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Ly::oMisc);
+  volatile uint32_t* abort_flag = misc + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Ly::bQ), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar(Ly::bKF + s), 1);
+      mbar_init(bar(Ly::bVF + s), 1);
+      mbar_init(bar(Ly::bKE + s), 1);
+      mbar_init(bar(Ly::bVE + s), 1);
+    }
+    mbar_init(bar(Ly::bS), 1);
+    mbar_init(bar(Ly::bS + 1), 1);
+    mbar_init(bar(Ly::bP), 4);
+    mbar_init(bar(Ly::bO), 1);
+    mbar_init(bar(Ly::bDone), 1);
+    misc[1] = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(misc), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const uint32_t tO = tmem + 256;  // S buffers at columns [0,128) and [128,256)
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      mbar_expect_tx(bar(Ly::bQ), Ly::kQ);
+#pragma unroll
+      for (int kb = 0; kb < KB; ++kb)
+        tma_load_2d(sQ + kb * BM * 128, &map_q, w.h * D + kb * 64, w.q_row0, bar(Ly::bQ));
+      int lk0 = -1, lk1 = -1, lv0 = -1, lv1 = -1;  // phase of the last K / V fill per stage
+      const int32_t* trow =
+          p.mode == CP_PASS_Q ? p.tables + ((long long)w.p * p.B + w.b) * p.max_blocks : nullptr;
+      bool ok = true;
+      for (int t = 0; t < w.ntiles; ++t) {
+        const int s = t % NS;
+        const uint32_t ph = (uint32_t)(t / NS) & 1u;
+        if (!mbar_wait(bar(Ly::bKE + s), ph ^ 1u, abort_flag, p.budget)) { ok = false; break; }
+        const uint32_t dK = sK + s * Ly::kKV, dV = sV + s * Ly::kKV;
+        if (p.mode == CP_PASS_KV) {
+          const bool r0 = t < w.nt[0];
+          const int y = w.kv_row0 + (r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN);
+          mbar_expect_tx(bar(Ly::bKF + s), Ly::kKV);
+#pragma unroll
+          for (int kb = 0; kb < KB; ++kb)
+            tma_load_2d(dK + kb * BN * 128, &map_k, w.g * D + kb * 64, y, bar(Ly::bKF + s));
+          if (!mbar_wait(bar(Ly::bVE + s), ph ^ 1u, abort_flag, p.budget)) { ok = false; break; }
+          if (p.debug & 1) {  // testing: V never arrives, the consumer's wait expires
+            if (s == 0) lk0 = (int)ph; else lk1 = (int)ph;
+            continue;
+          }
+          mbar_expect_tx(bar(Ly::bVF + s), Ly::kKV);
+#pragma unroll
+          for (int kb = 0; kb < KB; ++kb)
+            tma_load_2d(dV + kb * BN * 128, &map_v, w.g * D + kb * 64, y, bar(Ly::bVF + s));
+        } else {
+          // 8 pages of 16 rank-local tokens; pages past the visible range reload the last
+          // valid page (finite data, masked by the softmax) so the byte count is constant
+          int rows[BN / 16];
+          int last_good = -1;
+#pragma unroll
+          for (int i = 0; i < BN / 16; ++i) {
+            const int l = t * BN + i * 16;
+            int pg = -1;
+            if (l < w.n_local) {
+              const int col = l / 16;
+              pg = col < p.max_blocks ? __ldg(trow + col) : -1;
+              if (pg < 0 || pg >= p.pool) {
+                report(p.err, CP_ERR_DEVICE_BOUNDS);
+                pg = -1;
+              }
+            }
+            if (pg >= 0) last_good = pg;
+            rows[i] = pg;
+          }
+          if (last_good < 0) last_good = 0;
+#pragma unroll
+          for (int i = 0; i < BN / 16; ++i) {
+            const int pg = rows[i] >= 0 ? rows[i] : last_good;
+            rows[i] = (int)((((long long)w.p * p.pool + pg) * p.Hkv + w.g) * 16);
+          }
+          mbar_expect_tx(bar(Ly::bKF + s), Ly::kKV);
+#pragma unroll
+          for (int i = 0; i < BN / 16; ++i)
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)
+              tma_load_2d(dK + kb * BN * 128 + i * 16 * 128, &map_k, kb * 64, rows[i],
+                          bar(Ly::bKF + s));
+          if (!mbar_wait(bar(Ly::bVE + s), ph ^ 1u, abort_flag, p.budget)) { ok = false; break; }
+          if (p.debug & 1) {
+            if (s == 0) lk0 = (int)ph; else lk1 = (int)ph;
+            continue;
+          }
+          mbar_expect_tx(bar(Ly::bVF + s), Ly::kKV);
+#pragma unroll
+          for (int i = 0; i < BN / 16; ++i)
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)
+              tma_load_2d(dV + kb * BN * 128 + i * 16 * 128, &map_v, kb * 64, rows[i],
+                          bar(Ly::bVF + s));
+        }
+        if (s == 0) lk0 = (int)ph; else lk1 = (int)ph;
+        if (s == 0) lv0 = (int)ph; else lv1 = (int)ph;
+      }
+      if (!ok) fail_timeout(abort_flag, p.err);
+      // drain: every copy issued into this CTA's shared memory has landed before it exits
+      mbar_wait(bar(Ly::bQ), 0u, nullptr, p.budget);
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        const int lk = s == 0 ? lk0 : lk1, lv = s == 0 ? lv0 : lv1;
+        if (lk >= 0) mbar_wait(bar(Ly::bKF + s), (uint32_t)lk, nullptr, p.budget);
+        if (lv >= 0) mbar_wait(bar(Ly::bVF + s), (uint32_t)lv, nullptr, p.budget);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16_f32(BM, BN, false, false);
+      const uint32_t id_pv = idesc_bf16_f32(BM, D, false, true);
+      auto issue_qk = [&](int t) {
+        const uint32_t kst = sK + (t % NS) * Ly::kKV;
+        const uint32_t dS = tmem + (uint32_t)((t & 1) * BN);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * (BM * 128) + (k % 4) * 32;
+          const uint32_t offk = (k / 4) * (BN * 128) + (k % 4) * 32;
+          mma_ss(dS, desc_sw128(sQ + off, 16, 1024), desc_sw128(kst + offk, 16, 1024), id_qk,
+                 k > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar(Ly::bQ), 0u, abort_flag, p.budget);
+      if (ok) ok = mbar_wait(bar(Ly::bKF), 0u, abort_flag, p.budget);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0);
+        mma_commit(bar(Ly::bS));
+        mma_commit(bar(Ly::bKE));
+      }
+      for (int t = 0; ok && t < w.ntiles; ++t) {
+        if (t + 1 < w.ntiles) {
+          const int s1 = (t + 1) % NS;
+          ok = mbar_wait(bar(Ly::bKF + s1), (uint32_t)((t + 1) / NS) & 1u, abort_flag, p.budget);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(t + 1);
+          mma_commit(bar(Ly::bS + ((t + 1) & 1)));
+          mma_commit(bar(Ly::bKE + s1));
+        }
+        ok = mbar_wait(bar(Ly::bP), (uint32_t)t & 1u, abort_flag, p.budget);
+        if (!ok) break;
+        const int s = t % NS;
+        ok = mbar_wait(bar(Ly::bVF + s), (uint32_t)(t / NS) & 1u, abort_flag, p.budget);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vst = sV + s * Ly::kKV;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          const uint32_t offp = (k / 4) * (BM * 128) + (k % 4) * 32;
+          mma_ss(tO, desc_sw128(sP + offp, 16, 1024), desc_sw128(vst + k * 16 * 128, BN * 128, 1024),
+                 id_pv, (t > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(Ly::bO));
+        mma_commit(bar(Ly::bVE + s));
+      }
+      if (!ok) fail_timeout(abort_flag, p.err);
+      // every MMA issued by this thread has retired before TMEM is released
+      mma_commit(bar(Ly::bDone));
+      mbar_wait(bar(Ly::bDone), 0u, nullptr, p.budget);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroup
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const bool row_valid = w.q_lo + row < w.q_hi;
+    const long long qpos = w.qpos0 + row;
+    // keys visible to this row within the pass-Q range (local indices < nvis)
+    int nvis = 0;
+    if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < w.ntiles; ++t) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(bar(Ly::bS + (t & 1)), (uint32_t)(t >> 1) & 1u, abort_flag, p.budget));
+      if (!ok) break;
+      tc_fence_after();
+      float s0[32], s1[32], s2[32], s3[32];
+      const uint32_t tS = tmem + lane_off + (uint32_t)((t & 1) * BN);
+      tmem_ld32(tS, s0);
+      tmem_ld32(tS + 32, s1);
+      tmem_ld32(tS + 64, s2);
+      tmem_ld32(tS + 96, s3);
+      tmem_wait_ld(s0);
+      tmem_wait_ld(s1);
+      tmem_wait_ld(s2);
+      tmem_wait_ld(s3);
+      // last visible key column of this row in the tile (all keys <= lim are visible)
+      int lim;
+      if (p.mode == CP_PASS_KV) {
+        const bool r0 = t < w.nt[0];
+        const int k0 = r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN;
+        const int ke = r0 ? w.ke[0] : w.ke[1];
+        lim = (int)min((long long)ke - 1, qpos) - k0;
+      } else {
+        lim = nvis - 1 - t * BN;
+      }
+      if (lim < BN - 1) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          s0[k] = k <= lim ? s0[k] : -INFINITY;
+          s1[k] = k + 32 <= lim ? s1[k] : -INFINITY;
+          s2[k] = k + 64 <= lim ? s2[k] : -INFINITY;
+          s3[k] = k + 96 <= lim ? s3[k] : -INFINITY;
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        mx = fmaxf(mx, fmaxf(fmaxf(s0[k], s1[k]), fmaxf(s2[k], s3[k])));
+      const float m_tile = mx * p.scale_log2;
+      float alpha = 1.f;
+      if (m_tile > m + kRescaleThreshold) {  // first visible tile, or the max grew a lot
+        alpha = ex2(m - m_tile);
+        m = m_tile;
+      }
+      const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      const float sc = p.scale_log2;
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        s0[k] = ex2(fmaf(s0[k], sc, neg_m));
+        s1[k] = ex2(fmaf(s1[k], sc, neg_m));
+        s2[k] = ex2(fmaf(s2[k], sc, neg_m));
+        s3[k] = ex2(fmaf(s3[k], sc, neg_m));
+        sum += (s0[k] + s1[k]) + (s2[k] + s3[k]);
+      }
+      l = l * alpha + sum;
+      if (t > 0) {  // PV(t-1) has finished: the P buffer is free and O is stable
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO), (uint32_t)(t - 1) & 1u, abort_flag, p.budget));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tO + lane_off + c * 32, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= alpha;
+            tmem_st32(tO + lane_off + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P row (bf16) into the 128B-swizzled K-major tile: 16-byte chunk c of row r sits at
+      // chunk c ^ (r % 8) of its 128-byte row, 64 columns per block
+      const uint32_t prow = sP + row * 128;
+      const uint32_t sw = (uint32_t)(row & 7);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float* a = c == 0 ? s0 : c == 1 ? s1 : c == 2 ? s2 : s3;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {  // 8 columns per 16-byte chunk
+          const int col = c * 32 + h * 8;
+          const uint32_t blk = (uint32_t)(col / 64), ch = (uint32_t)((col % 64) / 8);
+          st_shared_v4(prow + blk * (BM * 128) + ((ch ^ sw) << 4), pack_bf16(a[h * 8], a[h * 8 + 1]),
+                       pack_bf16(a[h * 8 + 2], a[h * 8 + 3]), pack_bf16(a[h * 8 + 4], a[h * 8 + 5]),
+                       pack_bf16(a[h * 8 + 6], a[h * 8 + 7]));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::bP));
+    }
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO), (uint32_t)(w.ntiles - 1) & 1u,
+                                             abort_flag, p.budget));
+    if (ok) {
+      tc_fence_after();
+      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      float* dst = p.out + orow * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_wait_ld(o);
+        if (row_valid && l > 0.f) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(dst + c * 32 + k) =
+                make_float4(o[k] * inv_l, o[k + 1] * inv_l, o[k + 2] * inv_l, o[k + 3] * inv_l);
+        }
+      }
+      if (row_valid) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    } else {
+      fail_timeout(abort_flag, p.err);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------------- host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2D bf16 tensor map over `rows` rows of `cols` elements (row pitch `pitch_elems`), box of
+// 64 columns x box_rows rows, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* base, unsigned long long cols, unsigned long long rows,
+              unsigned long long pitch_elems, unsigned box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s) {
+  CUtensorMap mq, mk, mv;
+  const unsigned long long Nq = (unsigned long long)a.total_q;
+  if (!make_map(&mq, a.q, (unsigned long long)a.num_q_heads * D, Nq,
+                (unsigned long long)a.num_q_heads * D, BM))
+    return cudaErrorInvalidValue;
+  if (a.mode == CP_PASS_KV) {
+    const unsigned long long hd = (unsigned long long)a.num_kv_heads * D;
+    if (!make_map(&mk, a.k, hd, Nq, hd, BN) || !make_map(&mv, a.v, hd, Nq, hd, BN))
+      return cudaErrorInvalidValue;
+  } else {
+    const unsigned long long rows = (unsigned long long)a.cp * a.pool_pages * a.num_kv_heads * 16;
+    if (!make_map(&mk, a.k_cache, D, rows, D, 16) || !make_map(&mv, a.v_cache, D, rows, D, 16))
+      return cudaErrorInvalidValue;
+  }
+  TcParams p;
+  p.mode = a.mode;
+  p.B = a.num_seqs;
+  p.Hq = a.num_q_heads;
+  p.Hkv = a.num_kv_heads;
+  p.cp = a.cp;
+  p.I = a.interleave;
+  p.max_blocks = a.max_blocks;
+  p.q_shard = a.q_shard;
+  p.kv_shard = a.kv_shard;
+  p.debug = a.debug;
+  p.budget = (a.debug & 1) ? (1ll << 21) : kBudget;
+  const int chunk_max = (a.max_seqlen_q + 2 * a.cp - 1) / (2 * a.cp);
+  p.TPC = (chunk_max + BM - 1) / BM;
+  p.Nq = a.total_q;
+  p.pool = a.pool_pages;
+  p.scale_log2 = scale * kLog2e;
+  p.cu_q = a.cu_seqlens_q;
+  p.seq_lens_kv = a.seq_lens_kv;
+  p.tables = a.block_tables;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.err = a.err;
+  const long long grid = (long long)2 * a.cp * p.TPC * a.num_seqs *
+                         (a.kv_shard >= 0 ? 1 : a.cp) * a.num_q_heads;
+  if (grid == 0) return cudaSuccess;
+  if (grid >= (1ll << 31)) return cudaErrorInvalidConfiguration;
+  const int smem = Layout<D>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  prefill_tc_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace cpattn
+
+bool cp_prefill_tc_supported(const cp_prefill_args& a) {
+  if (a.dtype != CP_BF16) return false;
+  if (a.head_dim != 64 && a.head_dim != 128) return false;
+  if (a.mode == CP_PASS_Q && a.block_size != 16) return false;
+  return true;
+}
+
+cudaError_t cp_launch_prefill_tc(const cp_prefill_args& a, float scale, cudaStream_t s) {
+  return a.head_dim == 64 ? cpattn::launch<64>(a, scale, s) : cpattn::launch<128>(a, scale, s);
 }

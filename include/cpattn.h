@@ -177,6 +177,9 @@ typedef struct cp_prefill_args {
   int32_t q_shard;              /* -1 = all                                             */
   int32_t kv_shard;             /* -1 = all                                             */
   int32_t total_q;              /* host: Nq = cu_seqlens_q[B], rows of q/out/lse        */
+  int32_t debug;                /* 0.  Testing only (tcgen05 kernel): 1 withholds the V */
+                                /* tiles and shortens the wait budget so the pipeline's */
+                                /* bounded waits expire -> CP_ERR_TIMEOUT in err        */
   float* out;                   /* device [cp][Nq][Hq][d] f32                           */
   float* lse;                   /* device [cp][Nq][Hq] f32                              */
   int32_t* err;                 /* device int32 or NULL                                 */
