@@ -153,6 +153,7 @@ class PrefillRunner:
         self.cb = torch.empty(len(lens), 2 * cp + 1, dtype=torch.int32, device=dev)
         self.flops = 4.0 * d * Hq * causal_pairs_pass_kv(lens)
         self.launches_per_step = 3
+        self.impl = cpa.CP_IMPL_AUTO
         self.out_host = torch.empty(self.out.shape, dtype=w.dtype).pin_memory()
 
     def step(self, ev=None):
@@ -161,7 +162,8 @@ class PrefillRunner:
         if ev is not None:
             ev[0].record()
         cpa.cp_partial_attn_prefill(self.q, self.cu, w.cp, k=self.k, v=self.v,
-                                    max_seqlen_q=max(self.lens), out=self.part, lse=self.plse)
+                                    max_seqlen_q=max(self.lens), out=self.part, lse=self.plse,
+                                    impl=self.impl)
         if ev is not None:
             ev[1].record()
         cpa.cp_lse_merge(self.part, self.plse, out=self.out, out_lse=self.olse)
@@ -393,6 +395,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--prefill-impl", default="auto", choices=["auto", "tcgen05", "simt"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -408,6 +411,8 @@ def main():
     pk = peaks()
     w = wl.WORKLOADS[args.workload]
     runner = DecodeRunner(w, dev, cpa) if w.kind == "decode" else PrefillRunner(w, dev, cpa)
+    runner.impl = {"auto": cpa.CP_IMPL_AUTO, "tcgen05": cpa.CP_IMPL_TCGEN05,
+                   "simt": cpa.CP_IMPL_SIMT}[args.prefill_impl]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     clocks = ClockSampler(local)

@@ -79,7 +79,15 @@ def test_merge_parity(lib, P, rows, H, d, dt):
     O[torch.isinf(L)] = float("nan")                            # never read when empty
     out, lse = lib.cp_lse_merge(O.to(DEV), L.to(DEV), out_dtype=dt)
     Or, Lr = orc.lse_merge(O.numpy(), L.numpy())
-    check_merged(out, lse, Or, Lr, what="merge")
+    # the merge alone is exact up to f32 rounding; a bf16 output adds at most half an ulp
+    # (2^-9 |O|).  Random partials here reach |O| ~ 4, so the bound is relative.
+    ref = torch.from_numpy(Or)
+    tol = (2.0 ** -8 if dt == torch.bfloat16 else 1e-5) * ref.abs() + 1e-5
+    assert ((out.double().cpu() - ref).abs() <= tol).all(), "merge output"
+    fin = torch.isfinite(torch.from_numpy(Lr))
+    assert torch.equal(torch.isfinite(lse.cpu()), fin)
+    assert ((lse.double().cpu()[fin] - torch.from_numpy(Lr)[fin]).abs()
+            <= 1e-5 * torch.from_numpy(Lr)[fin].abs() + 1e-5).all(), "merge lse"
 
 
 # ------------------------------------------------------------------------------------ prefill
