@@ -138,46 +138,31 @@ __global__ void interleave_kernel(const int32_t* __restrict__ cu, int B, int N, 
 }
 
 // ---- cp_lse_merge: one warp per (row, head); lanes own D/32 consecutive floats.
+template <int D>
+struct MergeVec;
+template <>
+struct MergeVec<128> {
+  using T = float4;
+  static CP_DEV void fma(float (&acc)[4], float w, const T& x) {
+    acc[0] += w * x.x;
+    acc[1] += w * x.y;
+    acc[2] += w * x.z;
+    acc[3] += w * x.w;
+  }
+};
+template <>
+struct MergeVec<64> {
+  using T = float2;
+  static CP_DEV void fma(float (&acc)[2], float w, const T& x) {
+    acc[0] += w * x.x;
+    acc[1] += w * x.y;
+  }
+};
+
 template <int D, bool BF16_OUT>
-__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ po,
-                                                    const float* __restrict__ pl, int P,
-                                                    long long units, void* out, float* out_lse) {
+CP_DEV void merge_store(void* out, float* out_lse, long long u, int lane, const float (&acc)[D / 32],
+                        float wsum, float M) {
   constexpr int E = D / 32;
-  const long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (u >= units) return;
-  // M = max_p lse_p (log2 domain)
-  float M = -INFINITY;
-  for (int p0 = 0; p0 < P; p0 += 32) {
-    const int p = p0 + lane;
-    if (p < P) M = fmaxf(M, __ldg(pl + (long long)p * units + u) * kLog2e);
-  }
-  M = warp_max(M);
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M > -INFINITY) {
-#pragma unroll 4
-    for (int p = 0; p < P; ++p) {
-      const float lp = __ldg(pl + (long long)p * units + u);
-      if (lp == -INFINITY) continue;  // an empty partial is never read
-      const float w = exp2f(lp * kLog2e - M);
-      wsum += w;
-      const float* src = po + ((long long)p * units + u) * D + lane * E;
-      if constexpr (E == 4) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(src));
-        acc[0] += w * x.x;
-        acc[1] += w * x.y;
-        acc[2] += w * x.z;
-        acc[3] += w * x.w;
-      } else {
-        const float2 x = __ldg(reinterpret_cast<const float2*>(src));
-        acc[0] += w * x.x;
-        acc[1] += w * x.y;
-      }
-    }
-  }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   if constexpr (BF16_OUT) {
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + u * D + lane * E;
@@ -200,6 +185,98 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ po
     }
   }
   if (out_lse && lane == 0) out_lse[u] = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
+}
+
+// Few partials (the prefill case): every LSE and output load is issued before any arithmetic,
+// one memory round trip per unit.  An empty partial's row is loaded but given weight 0 by a
+// select, so whatever its unwritten memory holds never reaches the result.
+template <int D, bool BF16_OUT, int P>
+__global__ void __launch_bounds__(256) merge_small_kernel(const float* __restrict__ po,
+                                                          const float* __restrict__ pl,
+                                                          long long units, void* out,
+                                                          float* out_lse) {
+  constexpr int E = D / 32;
+  using V = typename MergeVec<D>::T;
+  const long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (u >= units) return;
+  float lp[P];
+  V x[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    lp[p] = __ldg(pl + (long long)p * units + u) * kLog2e;
+    x[p] = __ldg(reinterpret_cast<const V*>(po + ((long long)p * units + u) * D + lane * E));
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int p = 0; p < P; ++p) M = fmaxf(M, lp[p]);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (M > -INFINITY) {
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const bool live = lp[p] > -INFINITY;
+      const float w = live ? exp2f(lp[p] - M) : 0.f;
+      wsum += w;
+      if (live) MergeVec<D>::fma(acc, w, x[p]);
+    }
+  }
+  merge_store<D, BF16_OUT>(out, out_lse, u, lane, acc, wsum, M);
+}
+
+// Any number of partials (the decode case, cp x splits): LSEs read 32 at a time across the
+// lanes; only non-empty partials' rows are read.
+template <int D, bool BF16_OUT>
+__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ po,
+                                                    const float* __restrict__ pl, int P,
+                                                    long long units, void* out, float* out_lse) {
+  constexpr int E = D / 32;
+  using V = typename MergeVec<D>::T;
+  const long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (u >= units) return;
+  float M = -INFINITY;
+  for (int p0 = 0; p0 < P; p0 += 32) {
+    const int p = p0 + lane;
+    if (p < P) M = fmaxf(M, __ldg(pl + (long long)p * units + u) * kLog2e);
+  }
+  M = warp_max(M);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (M > -INFINITY) {
+    for (int p0 = 0; p0 < P; p0 += 32) {
+      const int p = p0 + lane;
+      const float lp = p < P ? __ldg(pl + (long long)p * units + u) * kLog2e : -INFINITY;
+      unsigned live = __ballot_sync(0xffffffffu, lp > -INFINITY);
+      while (live) {  // non-empty partials of this group, four loads in flight at a time
+        float w[4];
+        V x[4];
+        int n = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          w[q] = 0.f;
+          if (live) {
+            const int j = __ffs(live) - 1;
+            live &= live - 1;
+            w[q] = exp2f(__shfl_sync(0xffffffffu, lp, j) - M);
+            x[q] = __ldg(reinterpret_cast<const V*>(po + ((long long)(p0 + j) * units + u) * D + lane * E));
+            n = q + 1;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < n) {
+            wsum += w[q];
+            MergeVec<D>::fma(acc, w[q], x[q]);
+          }
+      }
+    }
+  }
+  merge_store<D, BF16_OUT>(out, out_lse, u, lane, acc, wsum, M);
 }
 
 }  // namespace
@@ -293,17 +370,22 @@ cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32
   const long long blocks = (units * 32 + 255) / 256;
   REQUIRE(blocks < (1ll << 31), "too many rows");
   cudaStream_t s = as_stream(stream);
-  if (head_dim == 128) {
-    if (out_dtype == CP_BF16)
-      cpattn::merge_kernel<128, true><<<(unsigned)blocks, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse);
-    else
-      cpattn::merge_kernel<128, false><<<(unsigned)blocks, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse);
-  } else {
-    if (out_dtype == CP_BF16)
-      cpattn::merge_kernel<64, true><<<(unsigned)blocks, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse);
-    else
-      cpattn::merge_kernel<64, false><<<(unsigned)blocks, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse);
+  const unsigned nb = (unsigned)blocks;
+#define CP_MERGE_SMALL(D, BF)                                                                 \
+  switch (num_partials) {                                                                   \
+    case 1: cpattn::merge_small_kernel<D, BF, 1><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    case 2: cpattn::merge_small_kernel<D, BF, 2><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    case 3: cpattn::merge_small_kernel<D, BF, 3><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    case 4: cpattn::merge_small_kernel<D, BF, 4><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    case 8: cpattn::merge_small_kernel<D, BF, 8><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    default: cpattn::merge_kernel<D, BF><<<nb, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse); \
   }
+  if (head_dim == 128) {
+    if (out_dtype == CP_BF16) { CP_MERGE_SMALL(128, true) } else { CP_MERGE_SMALL(128, false) }
+  } else {
+    if (out_dtype == CP_BF16) { CP_MERGE_SMALL(64, true) } else { CP_MERGE_SMALL(64, false) }
+  }
+#undef CP_MERGE_SMALL
   return launched(cudaGetLastError(), "cp_lse_merge launch");
 }
 
@@ -311,7 +393,7 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   REQUIRE(a != nullptr, "args is null");
   REQUIRE(a->mode == CP_PASS_KV || a->mode == CP_PASS_Q, "mode must be CP_PASS_KV or CP_PASS_Q");
   REQUIRE(a->dtype == CP_F32 || a->dtype == CP_BF16, "dtype must be CP_F32 or CP_BF16");
-  REQUIRE(a->impl >= CP_IMPL_AUTO && a->impl <= CP_IMPL_SIMT, "unknown impl %d", a->impl);
+  REQUIRE(a->impl >= CP_IMPL_AUTO && a->impl <= CP_IMPL_TCGEN05_SINGLE, "unknown impl %d", a->impl);
   REQUIRE(a->num_seqs >= 1, "num_seqs must be >= 1");
   REQUIRE(a->num_kv_heads >= 1 && a->num_q_heads >= a->num_kv_heads &&
               a->num_q_heads % a->num_kv_heads == 0,
@@ -345,7 +427,7 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
   int impl = a->impl;
   if (impl == CP_IMPL_AUTO) impl = (a->dtype == CP_BF16 && cp_prefill_tc_supported(*a)) ? CP_IMPL_TCGEN05 : CP_IMPL_SIMT;
-  if (impl == CP_IMPL_TCGEN05) {
+  if (impl == CP_IMPL_TCGEN05 || impl == CP_IMPL_TCGEN05_SINGLE) {
     if (a->dtype != CP_BF16 || !cp_prefill_tc_supported(*a))
       return fail(CP_ERR_UNSUPPORTED, "the tcgen05 kernel needs bf16 inputs and a supported shape");
     return launched(cp_launch_prefill_tc(*a, scale, as_stream(stream)), "prefill (tcgen05) launch");

@@ -111,24 +111,35 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
   const T* kbase = static_cast<const T*>(p.kc);
   const T* vbase = static_cast<const T*>(p.vc);
 
+  // This warp's pages: pg0 + warp, pg0 + warp + 4, ...  Their ids are fetched 32 at a time
+  // (lane j holds the j-th), so no page waits on its table entry.
   const int pg0 = l0 / kPage, pg1 = (l1 + kPage - 1) / kPage;
-  for (int pg = pg0 + warp; pg < pg1; pg += kWarps) {
-    const int page = pg < p.max_blocks ? __ldg(trow + pg) : -1;
-    if (page < 0 || page >= p.pool) {
-      if (lane == 0) report(p.err, CP_ERR_DEVICE_BOUNDS);
-      continue;
-    }
-    const long long off = (((long long)r * p.pool + page) * p.Hkv + g) * head_stride;
+  const int nmine = pg1 - pg0 > warp ? (pg1 - pg0 - warp + kWarps - 1) / kWarps : 0;
+
+  auto page_id = [&](int j) -> int {  // j-th page of this warp (all lanes)
+    const int pg = pg0 + warp + j * kWarps;
+    int id = pg < p.max_blocks ? __ldg(trow + pg) : -1;
+    if (id >= p.pool) id = -1;
+    return id;
+  };
+  auto issue = [&](int id, uint4 (&kv)[QKV], uint4 (&vv)[TPL]) {
+    if (id < 0) return;
+    const long long off = (((long long)r * p.pool + id) * p.Hkv + g) * head_stride;
     const T* kp = kbase + off;
     const T* vp = vbase + off;
-    uint4 kv[QKV], vv[TPL];
 #pragma unroll
     for (int i = 0; i < QKV; ++i)
       kv[i] = ldg_stream(kp + (long long)qk_tok * D + (2 * i + half) * EPV);
 #pragma unroll
     for (int i = 0; i < TPL; ++i)
       vv[i] = ldg_stream(vp + (long long)(v_tg + i * TG) * D + v_ch * EPV);
-
+  };
+  auto consume = [&](int j, int id, const uint4 (&kv)[QKV], const uint4 (&vv)[TPL]) {
+    if (id < 0) {  // a table entry outside the pool: the page is skipped and reported
+      if (lane == 0) report(p.err, CP_ERR_DEVICE_BOUNDS);
+      return;
+    }
+    const int pg = pg0 + warp + j * kWarps;
     // scores of token qk_tok for the G heads (two lanes per token, one half of d each)
     float s[G];
 #pragma unroll
@@ -179,6 +190,17 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
       }
     }
     __syncwarp();
+  };
+
+  for (int j0 = 0; j0 < nmine; j0 += 32) {
+    const int cnt = min(32, nmine - j0);
+    const int my_id = lane < cnt ? page_id(j0 + lane) : -1;
+    for (int j = 0; j < cnt; ++j) {
+      const int id = __shfl_sync(0xffffffffu, my_id, j);
+      uint4 kv[QKV], vv[TPL];
+      issue(id, kv, vv);
+      consume(j0 + j, id, kv, vv);
+    }
   }
 
   // token groups of the warp -> one partial per warp

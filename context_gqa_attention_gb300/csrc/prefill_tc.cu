@@ -77,12 +77,15 @@ struct Work {
   int ntiles;
 };
 
-CP_DEV Work decode_work(const TcParams& p) {
+// blockIdx.x -> (q tile slot, sequence, kv shard, head group of `hpc` consecutive q heads).
+// Slots run heaviest first (last chunk, last tile) so long items start early.
+CP_DEV Work decode_work(const TcParams& p, int hpc) {
   Work w;
   w.valid = 0;
   long long lin = blockIdx.x;
-  w.h = (int)(lin % p.Hq);
-  lin /= p.Hq;
+  const int groups = p.Hq / hpc;
+  w.h = (int)(lin % groups) * hpc;
+  lin /= groups;
   if (p.kv_shard >= 0) {
     w.p = p.kv_shard;
   } else {
@@ -143,17 +146,219 @@ CP_DEV void fail_timeout(volatile uint32_t* abort_flag, int32_t* err) {
   report(err, CP_ERR_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------------- row softmax
+// Packed two-lane fp32 arithmetic (f32x2 instructions of the sm_100 family) and 3-input max.
+CP_DEV uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+CP_DEV void f2u(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+CP_DEV uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+CP_DEV uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+CP_DEV float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// The 128 scores of this thread's row (its TMEM lane), one TMEM round trip.
+CP_DEV void load_row(uint32_t tS, float (&v0)[32], float (&v1)[32], float (&v2)[32],
+                     float (&v3)[32]) {
+  tmem_ld32(tS, v0);
+  tmem_ld32(tS + 32, v1);
+  tmem_ld32(tS + 64, v2);
+  tmem_ld32(tS + 96, v3);
+  tmem_wait_ld(v0);
+  tmem_wait_ld(v1);
+  tmem_wait_ld(v2);
+  tmem_wait_ld(v3);
+}
+
+CP_DEV void exp_chunk(float (&a)[32], uint64_t sc2, uint64_t n2, uint64_t& sum2) {
+#pragma unroll
+  for (int k = 0; k < 32; k += 2) {
+    float x0, x1;
+    f2u(ffma2(f2(a[k], a[k + 1]), sc2, n2), x0, x1);
+    a[k] = ex2(x0);
+    a[k + 1] = ex2(x1);
+    sum2 = fadd2(sum2, f2(a[k], a[k + 1]));
+  }
+}
+
+// Online-softmax step of one row over a 128-key tile: columns > lim are masked (skipped when
+// every row of the warp sees the whole tile), the running max m (log2 units) moves only when
+// the tile max exceeds it by more than 2^8, and the scores become p = 2^(s*sc - m) in place.
+// Returns alpha, the factor the row's O accumulator must be scaled by (l is updated here).
+CP_DEV float row_softmax(float (&v0)[32], float (&v1)[32], float (&v2)[32], float (&v3)[32],
+                         int lim, float sc, float& m, float& l) {
+  if (!__all_sync(0xffffffffu, lim >= BN - 1)) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      v0[k] = k <= lim ? v0[k] : -INFINITY;
+      v1[k] = k + 32 <= lim ? v1[k] : -INFINITY;
+      v2[k] = k + 64 <= lim ? v2[k] : -INFINITY;
+      v3[k] = k + 96 <= lim ? v3[k] : -INFINITY;
+    }
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    mx = fmax3(mx, v0[k], v1[k]);
+    mx = fmax3(mx, v2[k], v3[k]);
+  }
+  const float m_tile = mx * sc;
+  float alpha = 1.f;
+  if (m_tile > m + kRescaleThreshold) {  // first visible tile, or the max grew a lot
+    alpha = ex2(m - m_tile);
+    m = m_tile;
+  }
+  const float neg = (m == -INFINITY) ? 0.f : -m;
+  const uint64_t sc2 = f2(sc, sc), n2 = f2(neg, neg);
+  uint64_t sum2 = f2(0.f, 0.f);
+  exp_chunk(v0, sc2, n2, sum2);
+  exp_chunk(v1, sc2, n2, sum2);
+  exp_chunk(v2, sc2, n2, sum2);
+  exp_chunk(v3, sc2, n2, sum2);
+  float s_lo, s_hi;
+  f2u(sum2, s_lo, s_hi);
+  l = l * alpha + (s_lo + s_hi);
+  return alpha;
+}
+
+// Split form of row_softmax for kernels whose P buffer is already free when the scores
+// arrive: mask + max + running-max update first (returns alpha) ...
+CP_DEV float row_max_update(float (&v0)[32], float (&v1)[32], float (&v2)[32], float (&v3)[32],
+                            int lim, float sc, float& m) {
+  if (!__all_sync(0xffffffffu, lim >= BN - 1)) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      v0[k] = k <= lim ? v0[k] : -INFINITY;
+      v1[k] = k + 32 <= lim ? v1[k] : -INFINITY;
+      v2[k] = k + 64 <= lim ? v2[k] : -INFINITY;
+      v3[k] = k + 96 <= lim ? v3[k] : -INFINITY;
+    }
+  }
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    mx = fmax3(mx, v0[k], v1[k]);
+    mx = fmax3(mx, v2[k], v3[k]);
+  }
+  const float m_tile = mx * sc;
+  float alpha = 1.f;
+  if (m_tile > m + kRescaleThreshold) {
+    alpha = ex2(m - m_tile);
+    m = m_tile;
+  }
+  return alpha;
+}
+
+// ... then exponentials streamed 32 columns at a time straight into the swizzled P tile
+// (returns the row sum of p).
+CP_DEV void exp_store_chunk(float (&a)[32], int c, uint64_t sc2, uint64_t n2, uint64_t& sum2,
+                            uint32_t prow, uint32_t sw) {
+  exp_chunk(a, sc2, n2, sum2);
+  const uint32_t blk = prow + (uint32_t)(c >> 1) * (BM * 128);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint32_t ch = (uint32_t)((c & 1) * 4 + h);
+    st_shared_v4(blk + ((ch ^ sw) << 4), pack_bf16(a[h * 8], a[h * 8 + 1]),
+                 pack_bf16(a[h * 8 + 2], a[h * 8 + 3]), pack_bf16(a[h * 8 + 4], a[h * 8 + 5]),
+                 pack_bf16(a[h * 8 + 6], a[h * 8 + 7]));
+  }
+}
+CP_DEV float row_exp_store(float (&v0)[32], float (&v1)[32], float (&v2)[32], float (&v3)[32],
+                           float sc, float m, uint32_t sP, int row) {
+  const float neg = (m == -INFINITY) ? 0.f : -m;
+  const uint64_t sc2 = f2(sc, sc), n2 = f2(neg, neg);
+  uint64_t sum2 = f2(0.f, 0.f);
+  const uint32_t prow = sP + row * 128, sw = (uint32_t)(row & 7);
+  exp_store_chunk(v0, 0, sc2, n2, sum2, prow, sw);
+  exp_store_chunk(v1, 1, sc2, n2, sum2, prow, sw);
+  exp_store_chunk(v2, 2, sc2, n2, sum2, prow, sw);
+  exp_store_chunk(v3, 3, sc2, n2, sum2, prow, sw);
+  float lo, hi;
+  f2u(sum2, lo, hi);
+  return lo + hi;
+}
+
+// P row (bf16) into a 128x128 P tile stored as two 64-column blocks in the 128-byte-swizzled
+// K-major layout the MMA reads: 16-byte chunk c of row r sits at chunk c ^ (r % 8).
+CP_DEV void store_p_row(uint32_t sP, int row, const float (&v0)[32], const float (&v1)[32],
+                        const float (&v2)[32], const float (&v3)[32]) {
+  const uint32_t prow = sP + row * 128;
+  const uint32_t sw = (uint32_t)(row & 7);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float* a = c == 0 ? v0 : c == 1 ? v1 : c == 2 ? v2 : v3;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int col = c * 32 + h * 8;
+      const uint32_t blk = (uint32_t)(col / 64), ch = (uint32_t)((col % 64) / 8);
+      st_shared_v4(prow + blk * (BM * 128) + ((ch ^ sw) << 4), pack_bf16(a[h * 8], a[h * 8 + 1]),
+                   pack_bf16(a[h * 8 + 2], a[h * 8 + 3]), pack_bf16(a[h * 8 + 4], a[h * 8 + 5]),
+                   pack_bf16(a[h * 8 + 6], a[h * 8 + 7]));
+    }
+  }
+}
+
+// O row *= alpha in TMEM (warp-collective; nothing to do when no lane of the warp needs it).
+template <int D>
+CP_DEV void rescale_o(uint32_t tO, float alpha) {
+  if (!__any_sync(0xffffffffu, alpha != 1.f)) return;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    float o[32];
+    tmem_ld32(tO + c * 32, o);
+    tmem_wait_ld(o);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] *= alpha;
+    tmem_st32(tO + c * 32, o);
+  }
+  tmem_wait_st();
+}
+
+// Final O row / l -> the partial output (f32) and its natural-log LSE (warp-collective).
+template <int D>
+CP_DEV void write_row(uint32_t tO, float m, float l, bool row_valid, float* dst, float* lse_dst) {
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    float o[32];
+    tmem_ld32(tO + c * 32, o);
+    tmem_wait_ld(o);
+    if (row_valid && l > 0.f) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 4)
+        *reinterpret_cast<float4*>(dst + c * 32 + k) =
+            make_float4(o[k] * inv_l, o[k + 1] * inv_l, o[k + 2] * inv_l, o[k + 3] * inv_l);
+    }
+  }
+  if (row_valid) *lse_dst = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
 // ---------------------------------------------------------------------------------- kernel
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap map_q,
+    prefill_tc1_kernel(const __grid_constant__ CUtensorMap map_q,
                       const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const TcParams p) {
   using Ly = Layout<D>;
   constexpr int KB = D / 64;  // 64-column (128-byte) blocks of a head row
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Work w = decode_work(p);
+  const Work w = decode_work(p, 1);
   if (!w.valid) return;  // uniform over the CTA
 
   if (w.ntiles == 0) {  // no visible key in this pair: an empty partial
@@ -367,15 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       float s0[32], s1[32], s2[32], s3[32];
-      const uint32_t tS = tmem + lane_off + (uint32_t)((t & 1) * BN);
-      tmem_ld32(tS, s0);
-      tmem_ld32(tS + 32, s1);
-      tmem_ld32(tS + 64, s2);
-      tmem_ld32(tS + 96, s3);
-      tmem_wait_ld(s0);
-      tmem_wait_ld(s1);
-      tmem_wait_ld(s2);
-      tmem_wait_ld(s3);
+      load_row(tmem + lane_off + (uint32_t)((t & 1) * BN), s0, s1, s2, s3);
       // last visible key column of this row in the tile (all keys <= lim are visible)
       int lim;
       if (p.mode == CP_PASS_KV) {
@@ -386,70 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         lim = nvis - 1 - t * BN;
       }
-      if (lim < BN - 1) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          s0[k] = k <= lim ? s0[k] : -INFINITY;
-          s1[k] = k + 32 <= lim ? s1[k] : -INFINITY;
-          s2[k] = k + 64 <= lim ? s2[k] : -INFINITY;
-          s3[k] = k + 96 <= lim ? s3[k] : -INFINITY;
-        }
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 32; ++k)
-        mx = fmaxf(mx, fmaxf(fmaxf(s0[k], s1[k]), fmaxf(s2[k], s3[k])));
-      const float m_tile = mx * p.scale_log2;
-      float alpha = 1.f;
-      if (m_tile > m + kRescaleThreshold) {  // first visible tile, or the max grew a lot
-        alpha = ex2(m - m_tile);
-        m = m_tile;
-      }
-      const float neg_m = (m == -INFINITY) ? 0.f : -m;
-      const float sc = p.scale_log2;
-      float sum = 0.f;
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        s0[k] = ex2(fmaf(s0[k], sc, neg_m));
-        s1[k] = ex2(fmaf(s1[k], sc, neg_m));
-        s2[k] = ex2(fmaf(s2[k], sc, neg_m));
-        s3[k] = ex2(fmaf(s3[k], sc, neg_m));
-        sum += (s0[k] + s1[k]) + (s2[k] + s3[k]);
-      }
-      l = l * alpha + sum;
+      const float alpha = row_softmax(s0, s1, s2, s3, lim, p.scale_log2, m, l);
       if (t > 0) {  // PV(t-1) has finished: the P buffer is free and O is stable
         ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO), (uint32_t)(t - 1) & 1u, abort_flag, p.budget));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32(tO + lane_off + c * 32, o);
-            tmem_wait_ld(o);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] *= alpha;
-            tmem_st32(tO + lane_off + c * 32, o);
-          }
-          tmem_wait_st();
-        }
+        rescale_o<D>(tO + lane_off, alpha);
       }
-      // P row (bf16) into the 128B-swizzled K-major tile: 16-byte chunk c of row r sits at
-      // chunk c ^ (r % 8) of its 128-byte row, 64 columns per block
-      const uint32_t prow = sP + row * 128;
-      const uint32_t sw = (uint32_t)(row & 7);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float* a = c == 0 ? s0 : c == 1 ? s1 : c == 2 ? s2 : s3;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {  // 8 columns per 16-byte chunk
-          const int col = c * 32 + h * 8;
-          const uint32_t blk = (uint32_t)(col / 64), ch = (uint32_t)((col % 64) / 8);
-          st_shared_v4(prow + blk * (BM * 128) + ((ch ^ sw) << 4), pack_bf16(a[h * 8], a[h * 8 + 1]),
-                       pack_bf16(a[h * 8 + 2], a[h * 8 + 3]), pack_bf16(a[h * 8 + 4], a[h * 8 + 5]),
-                       pack_bf16(a[h * 8 + 6], a[h * 8 + 7]));
-        }
-      }
+      store_p_row(sP, row, s0, s1, s2, s3);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -461,21 +602,294 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      float* dst = p.out + orow * D;
+      write_row<D>(tO + lane_off, m, l, row_valid, p.out + orow * D, p.lse + orow);
+    } else {
+      fail_timeout(abort_flag, p.err);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------------- kernel 2
+// Two query heads of the same kv group per CTA (tiles 0 and 1: heads h, h+1, same 128 rows),
+// sharing every K/V tile.  Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2-5 softmax of
+// tile 0, 6-9 softmax of tile 1 (warp w reads TMEM lanes 32 (w % 4) ..).  TMEM: S0 [0,128), S1 [128,256),
+// O0 [256, 256+D), O1 [256+D, 256+2D).  K and V tiles stream through a 3-slot ring (load i:
+// K(t) for i = 2t, V(t) for i = 2t+1).  Tensor-core order per key tile t:
+//   PV0(t) | QK0(t+1) | PV1(t) | QK1(t+1)
+// so the softmax of each tile overlaps the other tile's two MMAs.
+constexpr int kThreads2 = 320;
+constexpr int NSLOT = 3;
+
+template <int D>
+struct Layout2 {
+  static constexpr int kQ = BM * D * 2;
+  static constexpr int kKV = BN * D * 2;
+  static constexpr int kP = BM * BN * 2;
+  static constexpr int oQ = 0;
+  static constexpr int oKV = 2 * kQ;
+  static constexpr int oP = oKV + NSLOT * kKV;
+  static constexpr int oBar = oP + 2 * kP;
+  static constexpr int bQ = 0, bFull = 1, bEmpty = bFull + NSLOT, bS = bEmpty + NSLOT, bP = bS + 2,
+                       bO = bP + 2, bDone = bO + 2, nBar = bDone + 1;
+  static constexpr int oMisc = oBar + nBar * 8;
+  static constexpr int kBytes = oMisc + 16;
+  static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads2, 1)
+    prefill_tc2_kernel(const __grid_constant__ CUtensorMap map_q,
+                       const __grid_constant__ CUtensorMap map_k,
+                       const __grid_constant__ CUtensorMap map_v, const TcParams p) {
+  using Ly = Layout2<D>;
+  constexpr int KB = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Work w = decode_work(p, 2);
+  if (!w.valid) return;
+
+  if (w.ntiles == 0) {  // empty pair
+    if (warp >= 2) {
+      const int tile = (warp - 2) >> 2;
+      const int row = (warp & 3) * 32 + lane;
+      if (w.q_lo + row < w.q_hi)
+        p.lse[((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile] = -INFINITY;
+    }
+    return;
+  }
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + Ly::oQ, sKV = base + Ly::oKV, sP = base + Ly::oP;
+  const uint32_t bars = base + Ly::oBar;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Ly::oMisc);
+  volatile uint32_t* abort_flag = misc + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Ly::bQ), 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(bar(Ly::bFull + s), 1);
+      mbar_init(bar(Ly::bEmpty + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(Ly::bS + i), 1);
+      mbar_init(bar(Ly::bP + i), 4);
+      mbar_init(bar(Ly::bO + i), 1);
+    }
+    mbar_init(bar(Ly::bDone), 1);
+    misc[1] = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(misc), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      mbar_expect_tx(bar(Ly::bQ), 2 * Ly::kQ);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
-        tmem_wait_ld(o);
-        if (row_valid && l > 0.f) {
+      for (int i = 0; i < 2; ++i)
 #pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + k) =
-                make_float4(o[k] * inv_l, o[k + 1] * inv_l, o[k + 2] * inv_l, o[k + 3] * inv_l);
+        for (int kb = 0; kb < KB; ++kb)
+          tma_load_2d(sQ + i * Ly::kQ + kb * BM * 128, &map_q, (w.h + i) * D + kb * 64, w.q_row0,
+                      bar(Ly::bQ));
+      int last0 = -1, last1 = -1, last2 = -1;  // phase of the last fill of each slot
+      const int32_t* trow =
+          p.mode == CP_PASS_Q ? p.tables + ((long long)w.p * p.B + w.b) * p.max_blocks : nullptr;
+      int prow[BN / 16];  // pass-Q: element rows of the current tile's pages (K and V alike)
+      bool ok = true;
+      for (int i = 0; i < 2 * w.ntiles; ++i) {
+        const int slot = i % NSLOT;
+        const uint32_t ph = (uint32_t)(i / NSLOT) & 1u;
+        const int t = i >> 1;
+        const bool isV = (i & 1) != 0;
+        if (!mbar_wait(bar(Ly::bEmpty + slot), ph ^ 1u, abort_flag, p.budget)) { ok = false; break; }
+        if (isV && (p.debug & 1)) continue;  // testing: V never arrives
+        const uint32_t dst = sKV + slot * Ly::kKV;
+        const CUtensorMap* map = isV ? &map_v : &map_k;
+        mbar_expect_tx(bar(Ly::bFull + slot), Ly::kKV);
+        if (p.mode == CP_PASS_KV) {
+          const bool r0 = t < w.nt[0];
+          const int y = w.kv_row0 + (r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN);
+#pragma unroll
+          for (int kb = 0; kb < KB; ++kb)
+            tma_load_2d(dst + kb * BN * 128, map, w.g * D + kb * 64, y, bar(Ly::bFull + slot));
+        } else {
+          if (!isV) {  // page rows of tile t (reused for its V load)
+            int last_good = -1;
+#pragma unroll
+            for (int j = 0; j < BN / 16; ++j) {
+              const int l = t * BN + j * 16;
+              int pg = -1;
+              if (l < w.n_local) {
+                const int col = l / 16;
+                pg = col < p.max_blocks ? __ldg(trow + col) : -1;
+                if (pg < 0 || pg >= p.pool) {
+                  report(p.err, CP_ERR_DEVICE_BOUNDS);
+                  pg = -1;
+                }
+              }
+              if (pg >= 0) last_good = pg;
+              prow[j] = pg;
+            }
+            if (last_good < 0) last_good = 0;
+#pragma unroll
+            for (int j = 0; j < BN / 16; ++j)
+              prow[j] = (int)((((long long)w.p * p.pool + (prow[j] >= 0 ? prow[j] : last_good)) *
+                                   p.Hkv + w.g) * 16);
+          }
+#pragma unroll
+          for (int j = 0; j < BN / 16; ++j)
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)
+              tma_load_2d(dst + kb * BN * 128 + j * 16 * 128, map, kb * 64, prow[j],
+                          bar(Ly::bFull + slot));
+        }
+        if (slot == 0) last0 = (int)ph; else if (slot == 1) last1 = (int)ph; else last2 = (int)ph;
+      }
+      if (!ok) fail_timeout(abort_flag, p.err);
+      mbar_wait(bar(Ly::bQ), 0u, nullptr, p.budget);
+      if (last0 >= 0) mbar_wait(bar(Ly::bFull + 0), (uint32_t)last0, nullptr, p.budget);
+      if (last1 >= 0) mbar_wait(bar(Ly::bFull + 1), (uint32_t)last1, nullptr, p.budget);
+      if (last2 >= 0) mbar_wait(bar(Ly::bFull + 2), (uint32_t)last2, nullptr, p.budget);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = idesc_bf16_f32(BM, BN, false, false);
+      const uint32_t id_pv = idesc_bf16_f32(BM, D, false, true);
+      auto issue_qk = [&](int tile, int slot) {
+        const uint32_t q = sQ + tile * Ly::kQ, k = sKV + slot * Ly::kKV;
+        const uint32_t dS = tmem + (uint32_t)(tile * BN);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offq = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+          const uint32_t offk = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+          mma_ss(dS, desc_sw128(q + offq, 16, 1024), desc_sw128(k + offk, 16, 1024), id_qk,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int tile, int slot, bool acc) {
+        const uint32_t pp = sP + tile * Ly::kP, v = sKV + slot * Ly::kKV;
+        const uint32_t dO = tmem + 256u + (uint32_t)(tile * D);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint32_t offp = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+          mma_ss(dO, desc_sw128(pp + offp, 16, 1024), desc_sw128(v + kk * 16 * 128, BN * 128, 1024),
+                 id_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(bar(Ly::bQ), 0u, abort_flag, p.budget);
+      if (ok) ok = mbar_wait(bar(Ly::bFull + 0), 0u, abort_flag, p.budget);  // K(0): load 0
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0, 0);
+        mma_commit(bar(Ly::bS + 0));
+        issue_qk(1, 0);
+        mma_commit(bar(Ly::bS + 1));
+        mma_commit(bar(Ly::bEmpty + 0));
+      }
+      for (int t = 0; ok && t < w.ntiles; ++t) {
+        const int iv = 2 * t + 1, ik = 2 * t + 2;
+        const int sv = iv % NSLOT, sk = ik % NSLOT;
+        ok = mbar_wait(bar(Ly::bFull + sv), (uint32_t)(iv / NSLOT) & 1u, abort_flag, p.budget);
+        if (!ok) break;
+        ok = mbar_wait(bar(Ly::bP + 0), (uint32_t)t & 1u, abort_flag, p.budget);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(0, sv, t > 0);
+        mma_commit(bar(Ly::bO + 0));
+        const bool more = t + 1 < w.ntiles;
+        if (more) {
+          ok = mbar_wait(bar(Ly::bFull + sk), (uint32_t)(ik / NSLOT) & 1u, abort_flag, p.budget);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(0, sk);
+          mma_commit(bar(Ly::bS + 0));
+        }
+        ok = mbar_wait(bar(Ly::bP + 1), (uint32_t)t & 1u, abort_flag, p.budget);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(1, sv, t > 0);
+        mma_commit(bar(Ly::bO + 1));
+        mma_commit(bar(Ly::bEmpty + sv));
+        if (more) {
+          issue_qk(1, sk);
+          mma_commit(bar(Ly::bS + 1));
+          mma_commit(bar(Ly::bEmpty + sk));
         }
       }
-      if (row_valid) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (!ok) fail_timeout(abort_flag, p.err);
+      mma_commit(bar(Ly::bDone));
+      mbar_wait(bar(Ly::bDone), 0u, nullptr, p.budget);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax, one WG per tile
+    const int tile = (warp - 2) >> 2;
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (uint32_t)(tile * BN);
+    const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(tile * D);
+    const bool row_valid = w.q_lo + row < w.q_hi;
+    const long long qpos = w.qpos0 + row;
+    int nvis = 0;
+    if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < w.ntiles; ++t) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bS + tile), (uint32_t)t & 1u, abort_flag, p.budget));
+      if (!ok) break;
+      tc_fence_after();
+      float s0[32], s1[32], s2[32], s3[32];
+      load_row(tS, s0, s1, s2, s3);
+      int lim;
+      if (p.mode == CP_PASS_KV) {
+        const bool r0 = t < w.nt[0];
+        const int k0 = r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN;
+        const int ke = r0 ? w.ke[0] : w.ke[1];
+        lim = (int)min((long long)ke - 1, qpos) - k0;
+      } else {
+        lim = nvis - 1 - t * BN;
+      }
+      const float alpha = row_max_update(s0, s1, s2, s3, lim, p.scale_log2, m);
+      if (t > 0) {  // PV(t-1) of this tile finished before QK(t) began: P free, O stable
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO + tile), (uint32_t)(t - 1) & 1u, abort_flag, p.budget));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      l = l * alpha + row_exp_store(s0, s1, s2, s3, p.scale_log2, m, sP + tile * Ly::kP, row);
+      if (t > 0) rescale_o<D>(tO, alpha);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::bP + tile));
+    }
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO + tile), (uint32_t)(w.ntiles - 1) & 1u,
+                                             abort_flag, p.budget));
+    if (ok) {
+      tc_fence_after();
+      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile;
+      write_row<D>(tO, m, l, row_valid, p.out + orow * D, p.lse + orow);
     } else {
       fail_timeout(abort_flag, p.err);
     }
@@ -562,15 +976,25 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s) {
   p.out = a.out;
   p.lse = a.lse;
   p.err = a.err;
-  const long long grid = (long long)2 * a.cp * p.TPC * a.num_seqs *
-                         (a.kv_shard >= 0 ? 1 : a.cp) * a.num_q_heads;
+  // two heads per CTA when the heads of a kv group pair up, unless one head per CTA is forced
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const bool pair = (G % 2 == 0) && a.impl != CP_IMPL_TCGEN05_SINGLE;
+  const long long grid = (long long)2 * a.cp * p.TPC * a.num_seqs * (a.kv_shard >= 0 ? 1 : a.cp) *
+                         (a.num_q_heads / (pair ? 2 : 1));
   if (grid == 0) return cudaSuccess;
   if (grid >= (1ll << 31)) return cudaErrorInvalidConfiguration;
-  const int smem = Layout<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  prefill_tc_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, p);
+  cudaError_t e;
+  if (pair) {
+    const int smem = Layout2<D>::kAlloc;
+    e = cudaFuncSetAttribute(prefill_tc2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    prefill_tc2_kernel<D><<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, p);
+  } else {
+    const int smem = Layout<D>::kAlloc;
+    e = cudaFuncSetAttribute(prefill_tc1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    prefill_tc1_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(mq, mk, mv, p);
+  }
   return cudaGetLastError();
 }
 

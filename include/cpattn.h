@@ -64,7 +64,9 @@ typedef enum { CP_PASS_KV = 0, CP_PASS_Q = 1 } cp_mode;
 typedef enum {
   CP_IMPL_AUTO = 0,     /* tcgen05 tensor-core kernel for bf16, SIMT kernel for f32   */
   CP_IMPL_TCGEN05 = 1,  /* bf16 only: TMA + tcgen05.mma + TMEM                        */
-  CP_IMPL_SIMT = 2      /* plain CUDA cores, any supported dtype (cross-check path)   */
+  CP_IMPL_SIMT = 2,     /* plain CUDA cores, any supported dtype (cross-check path)   */
+  CP_IMPL_TCGEN05_SINGLE = 3  /* bf16: tcgen05 kernel with one q head per CTA (the form */
+                              /* used when q heads per kv head is odd)                 */
 } cp_impl;
 
 /* Human-readable name of a cp_status value (static string). */
@@ -241,8 +243,9 @@ cp_status cp_partial_attn_decode(const cp_decode_args* args, void* stream);
  *
  *   M = max_p lse_p;  w_p = exp(lse_p - M) (0 for lse_p = -inf);
  *   out = sum_p w_p * out_p / sum_p w_p;  out_lse = M + log(sum_p w_p).
- * A partial with lse = -inf is never read.  All partials empty gives out = 0 and
- * out_lse = -inf.
+ * A partial with lse = -inf contributes nothing: its out rows may hold anything (they
+ * are never used; with few partials they may still be loaded).  All partials empty gives
+ * out = 0 and out_lse = -inf.
  *
  *   partial_out  device f32 [P][rows][H][d];  partial_lse device f32 [P][rows][H].
  *   out          device [rows][H][d] of out_dtype (bf16: round to nearest even).

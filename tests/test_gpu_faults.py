@@ -17,18 +17,20 @@ from tests.parity_util import check_partials
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_timeout_is_reported_and_context_survives(lib):
+@pytest.mark.parametrize("impl", ["tc", "tc1"])
+def test_wait_timeout_is_reported_and_context_survives(lib, impl):
     lens, Hq, Hkv, d, cp = [640], 8, 2, 128, 2
     x = wl.prefill_inputs(lens, Hq, Hkv, d, torch.bfloat16, seed=77)
     q, k, v, cu = (x[n].cuda() for n in ("q", "k", "v", "cu_seqlens"))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    lib.cp_partial_attn_prefill(q, cu, cp, k=k, v=v, max_seqlen_q=640, impl=lib.CP_IMPL_TCGEN05,
-                                err=err, debug=1)
+    code = lib.CP_IMPL_TCGEN05 if impl == "tc" else lib.CP_IMPL_TCGEN05_SINGLE
+    lib.cp_partial_attn_prefill(q, cu, cp, k=k, v=v, max_seqlen_q=640, impl=code, err=err,
+                                debug=1)
     torch.cuda.synchronize()
     assert int(err.item()) == 4          # CP_ERR_TIMEOUT
     err.zero_()
-    out, lse = lib.cp_partial_attn_prefill(q, cu, cp, k=k, v=v, max_seqlen_q=640,
-                                           impl=lib.CP_IMPL_TCGEN05, err=err)
+    out, lse = lib.cp_partial_attn_prefill(q, cu, cp, k=k, v=v, max_seqlen_q=640, impl=code,
+                                           err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], cp, 1 / math.sqrt(d))

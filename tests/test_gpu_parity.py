@@ -93,7 +93,8 @@ def test_merge_parity(lib, P, rows, H, d, dt):
 # ------------------------------------------------------------------------------------ prefill
 
 def _impl_code(lib, name):
-    return {"simt": lib.CP_IMPL_SIMT, "tc": lib.CP_IMPL_TCGEN05}[name]
+    return {"simt": lib.CP_IMPL_SIMT, "tc": lib.CP_IMPL_TCGEN05,
+            "tc1": lib.CP_IMPL_TCGEN05_SINGLE}[name]
 
 
 PASS_KV_CASES = [
@@ -107,11 +108,11 @@ PASS_KV_CASES = [
 ]
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 @pytest.mark.parametrize("case", range(len(PASS_KV_CASES)))
 def test_pass_kv_parity(lib, case, impl):
     lens, Hq, Hkv, d, dt, cp = PASS_KV_CASES[case]
-    if impl == "tc" and dt != torch.bfloat16:
+    if impl.startswith("tc") and dt != torch.bfloat16:
         pytest.skip("the tensor-core kernel takes bf16")
     x = wl.prefill_inputs(lens, Hq, Hkv, d, dt, seed=100 + case)
     scale = 1.0 / math.sqrt(d)
@@ -125,7 +126,7 @@ def test_pass_kv_parity(lib, case, impl):
     check_merged(mo, ml, Om, Lm, what=f"pass-KV {impl} merged")
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 def test_pass_kv_single_pair(lib, impl):
     """q_shard / kv_shard restrict the launch to one rotation step; other pairs untouched."""
     lens, Hq, Hkv, d, cp = [900], 8, 2, 128, 4
@@ -167,11 +168,11 @@ PASS_Q_CASES = [
 ]
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 @pytest.mark.parametrize("case", range(len(PASS_Q_CASES)))
 def test_pass_q_parity(lib, case, impl):
     q_lens, kv_lens, Hq, Hkv, d, dt, cp, I = PASS_Q_CASES[case]
-    if impl == "tc" and dt != torch.bfloat16:
+    if impl.startswith("tc") and dt != torch.bfloat16:
         pytest.skip("the tensor-core kernel takes bf16")
     x = _paged_case(len(q_lens), q_lens, kv_lens, Hq, Hkv, d, dt, cp, I, 300 + case)
     out, lse = lib.cp_partial_attn_prefill(
