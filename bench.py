@@ -17,6 +17,7 @@ on one GPU each) -- weak scaling, no collective on the data path.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -223,6 +224,9 @@ class DecodeRunner:
         self.part = torch.empty(P, w.num_seqs, Hq, d, dtype=torch.float32, device=dev)
         self.plse = torch.empty(P, w.num_seqs, Hq, dtype=torch.float32, device=dev)
         self.out = torch.empty(w.num_seqs, Hq, d, dtype=w.dtype, device=dev)
+        self.fused = True
+        self.ws = torch.zeros(cpa.cp_decode_workspace_size(w.num_seqs, Hq, Hkv, d, cp, self.ns),
+                              dtype=torch.uint8, device=dev)
         self.local_lens = torch.empty(cp, w.num_seqs, dtype=torch.int32, device=dev)
         el = torch.tensor([], dtype=w.dtype).element_size()
         pages = sum(-(-n // w.block_size) for L in lens
@@ -231,8 +235,11 @@ class DecodeRunner:
                               for r in range(cp)])
         self.bytes = (sum(lens) * Hkv * d * 2 * el + 2 * w.num_seqs * Hq * d * el + pages * 4)
         self.kv_bytes = sum(lens) * Hkv * d * 2 * el
-        self.launches_per_step = 3
         self.pool = pool
+
+    @property
+    def launches_per_step(self):
+        return 2 if self.fused else 3
 
     def step(self, ev=None):
         cpa, w = self.cpa, self.w
@@ -240,6 +247,13 @@ class DecodeRunner:
                                     local_lens=self.local_lens, want_slots=False)
         if ev is not None:
             ev[0].record()
+        if self.fused:  # partials + merge in one launch
+            cpa.cp_decode_attention(self.q, self.kc, self.vc, self.tables, self.seq_lens, w.cp,
+                                    w.interleave, num_splits=self.ns, split_tokens=self.st,
+                                    workspace=self.ws, out=self.out, want_lse=False)
+            if ev is not None:
+                ev[1].record()
+            return
         cpa.cp_partial_attn_decode(self.q, self.kc, self.vc, self.tables, self.seq_lens, w.cp,
                                    w.interleave, num_splits=self.ns, split_tokens=self.st,
                                    out=self.part, lse=self.plse)
@@ -396,6 +410,10 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--prefill-impl", default="auto", choices=["auto", "tcgen05", "simt"])
+    ap.add_argument("--decode-unfused", action="store_true",
+                    help="decode as two launches (partials, then cp_lse_merge)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's number of sequences (smaller profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -410,7 +428,11 @@ def main():
     stream = torch.cuda.current_stream(dev)
     pk = peaks()
     w = wl.WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = dataclasses.replace(w, num_seqs=args.batch)
     runner = DecodeRunner(w, dev, cpa) if w.kind == "decode" else PrefillRunner(w, dev, cpa)
+    if isinstance(runner, DecodeRunner):
+        runner.fused = not args.decode_unfused
     runner.impl = {"auto": cpa.CP_IMPL_AUTO, "tcgen05": cpa.CP_IMPL_TCGEN05,
                    "simt": cpa.CP_IMPL_SIMT}[args.prefill_impl]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -458,11 +480,13 @@ def main():
     else:
         e2e = None
         peak, src = pk["hbm"]
-        achieved = runner.kv_bytes / dom_s / 1e9
+        achieved = runner.bytes / dom_s / 1e9
         roof = {"bound": "hbm", "kernel": "cp_partial_attn_decode", "achieved": achieved,
                 "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": f"{src} HBM copy", "traffic": None, "launch_ms": dom_s * 1e3}
+                "peak_source": f"{src} HBM copy", "traffic": None, "launch_ms": dom_s * 1e3,
+                "algorithmic": f"{runner.bytes:.4e} B per launch (KV once + q + out + tables)"}
         metric = "decode KV-read GB/s (partial attention + LSE merge)"
+        roof["kernel"] = "cp_decode_attention (fused partials + merge)" if runner.fused else roof["kernel"]
         unit = "GB/s"
 
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
@@ -484,9 +508,9 @@ def main():
         line["secondary"] = {
             "decode": {"value": dr.metric(statistics.mean(ds) / 1e3), "unit": "GB/s",
                        "config": dr.config(),
-                       "roofline": {"bound": "hbm", "kernel": "cp_partial_attn_decode",
-                                    "achieved": dr.kv_bytes / d_s / 1e9, "peak": hbm,
-                                    "unit": "GB/s", "frac": dr.kv_bytes / d_s / 1e9 / hbm,
+                       "roofline": {"bound": "hbm", "kernel": "cp_decode_attention (fused)",
+                                    "achieved": dr.bytes / d_s / 1e9, "peak": hbm,
+                                    "unit": "GB/s", "frac": dr.bytes / d_s / 1e9 / hbm,
                                     "peak_source": f"{hsrc} HBM copy", "launch_ms": d_s * 1e3}}}
         del dr
 

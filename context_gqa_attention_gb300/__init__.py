@@ -23,7 +23,7 @@ __all__ = [
     "CPError", "load", "lib_path", "CP_F32", "CP_BF16", "CP_PASS_KV", "CP_PASS_Q",
     "CP_IMPL_AUTO", "CP_IMPL_TCGEN05", "CP_IMPL_SIMT", "CP_IMPL_TCGEN05_SINGLE", "cp_partition", "cp_kv_interleave_layout",
     "cp_partial_attn_prefill", "cp_decode_plan", "cp_partial_attn_decode", "cp_lse_merge",
-    "STATUS",
+    "cp_decode_workspace_size", "cp_decode_attention", "STATUS",
 ]
 
 CP_F32, CP_BF16 = 0, 1
@@ -90,6 +90,9 @@ _SIGS = [
     ("cp_partial_attn_decode", ctypes.c_int32, [ctypes.POINTER(DecodeArgs), _vp]),
     ("cp_lse_merge", ctypes.c_int32, [_vp, _vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                       ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp]),
+    ("cp_decode_workspace_size", ctypes.c_int32, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_size_t)]),
+    ("cp_decode_attention", ctypes.c_int32, [ctypes.POINTER(DecodeArgs), _vp, ctypes.c_size_t, _vp,
+                                             _vp, _vp]),
 ]
 
 EXPORTED = [s[0] for s in _SIGS]
@@ -301,6 +304,63 @@ def cp_partial_attn_decode(q, k_cache, v_cache, block_tables, seq_lens, cp, inte
                                                        _ptr(lse), _ptr(err))
     _check(_LIB.cp_partial_attn_decode(ctypes.byref(a), _stream(stream)))
     return out, lse
+
+
+def _decode_args(q, k_cache, v_cache, block_tables, seq_lens, cp, interleave, num_splits,
+                 split_tokens, softmax_scale, out, lse, err):
+    B, Hq, d = q.shape
+    for n, t, dt in (("q", q, None), ("k_cache", k_cache, q.dtype), ("v_cache", v_cache, q.dtype),
+                     ("block_tables", block_tables, torch.int32), ("seq_lens", seq_lens, torch.int32)):
+        _dev(t, n, dt)
+    a = DecodeArgs()
+    a.dtype, a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim = _cp_dtype(q), B, Hq, k_cache.shape[2], d
+    a.cp, a.interleave, a.block_size = cp, interleave, k_cache.shape[3]
+    a.num_splits, a.split_tokens, a.softmax_scale = num_splits, split_tokens, softmax_scale
+    a.max_blocks, a.pool_pages = block_tables.shape[-1], k_cache.shape[1]
+    a.q, a.k_cache, a.v_cache = _ptr(q), _ptr(k_cache), _ptr(v_cache)
+    a.block_tables, a.seq_lens, a.out, a.lse, a.err = (_ptr(block_tables), _ptr(seq_lens), _ptr(out),
+                                                       _ptr(lse), _ptr(err))
+    return a
+
+
+def cp_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, cp, num_splits):
+    """Bytes of scratch cp_decode_attention needs."""
+    load()
+    n = ctypes.c_size_t()
+    _check(_LIB.cp_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, cp,
+                                         num_splits, ctypes.byref(n)))
+    return n.value
+
+
+def cp_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, cp, interleave, *,
+                        max_seq_len=None, num_splits=None, split_tokens=None, softmax_scale=0.0,
+                        workspace=None, out=None, out_lse=None, want_lse=True, err=None,
+                        stream=None):
+    """Decode partials + merge in one launch (see cpattn.h).  `workspace` is a zero-filled
+    uint8 CUDA tensor of at least cp_decode_workspace_size() bytes; it is left reusable.
+    Returns (out [B, Hq, d] dtype of q, lse [B, Hq] f32 or None)."""
+    load()
+    B, Hq, d = q.shape
+    Hkv, bs = k_cache.shape[2], k_cache.shape[3]
+    if num_splits is None or split_tokens is None:
+        if max_seq_len is None:
+            max_seq_len = int(seq_lens.max().item())
+        num_splits, split_tokens = cp_decode_plan(B, Hkv, cp, interleave, bs, max_seq_len)
+    need = cp_decode_workspace_size(B, Hq, Hkv, d, cp, num_splits)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=q.dtype, device=q.device)
+    if out_lse is None and want_lse:
+        out_lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    _dev(workspace, "workspace")
+    _dev(out, "out", q.dtype)
+    _dev(out_lse, "out_lse", torch.float32)
+    a = _decode_args(q, k_cache, v_cache, block_tables, seq_lens, cp, interleave, num_splits,
+                     split_tokens, softmax_scale, None, None, err)
+    _check(_LIB.cp_decode_attention(ctypes.byref(a), _ptr(workspace), workspace.numel(), _ptr(out),
+                                    _ptr(out_lse), _stream(stream)))
+    return out, out_lse
 
 
 def cp_lse_merge(partial_out, partial_lse, out=None, out_dtype=torch.bfloat16, out_lse=None,

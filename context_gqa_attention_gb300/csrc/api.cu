@@ -463,7 +463,49 @@ cp_status cp_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t cp, int
   return ok();
 }
 
+static cp_status check_decode_args(const cp_decode_args* a, bool need_partials);
+
 cp_status cp_partial_attn_decode(const cp_decode_args* a, void* stream) {
+  const cp_status st = check_decode_args(a, true);
+  if (st != CP_OK) return st;
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
+  return launched(cp_launch_decode(*a, scale, as_stream(stream)), "decode launch");
+}
+
+cp_status cp_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t cp, int32_t num_splits,
+                                   size_t* bytes) {
+  REQUIRE(bytes != nullptr, "bytes is null");
+  REQUIRE(num_seqs >= 1 && num_q_heads >= 1 && num_kv_heads >= 1 && head_dim >= 1 && cp >= 1 &&
+              num_splits >= 1,
+          "all sizes must be >= 1");
+  size_t ol, oo;
+  *bytes = cp_decode_ws_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, cp * num_splits, &ol, &oo);
+  return ok();
+}
+
+cp_status cp_decode_attention(const cp_decode_args* a, void* workspace, size_t workspace_bytes,
+                              void* out, float* out_lse, void* stream) {
+  const cp_status st = check_decode_args(a, false);
+  if (st != CP_OK) return st;
+  REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
+          "workspace must be a non-null 256-byte aligned pointer");
+  REQUIRE_PTR(out);
+  size_t ol, oo;
+  const size_t need = cp_decode_ws_layout(a->num_seqs, a->num_q_heads, a->num_kv_heads, a->head_dim,
+                                          a->cp * a->num_splits, &ol, &oo);
+  REQUIRE(workspace_bytes >= need, "workspace too small: %zu bytes given, %zu needed",
+          workspace_bytes, need);
+  CpDecodeWorkspace ws;
+  ws.counters = static_cast<int32_t*>(workspace);
+  ws.partial_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ol);
+  ws.partial_out = reinterpret_cast<float*>(static_cast<char*>(workspace) + oo);
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
+  return launched(cp_launch_decode_fused(*a, scale, ws, out, out_lse, as_stream(stream)),
+                  "fused decode launch");
+}
+
+static cp_status check_decode_args(const cp_decode_args* a, bool need_partials) {
   REQUIRE(a != nullptr, "args is null");
   REQUIRE(a->dtype == CP_F32 || a->dtype == CP_BF16, "dtype must be CP_F32 or CP_BF16");
   REQUIRE(a->num_seqs >= 1, "num_seqs must be >= 1");
@@ -485,10 +527,12 @@ cp_status cp_partial_attn_decode(const cp_decode_args* a, void* stream) {
   REQUIRE_PTR(a->q);
   REQUIRE_PTR(a->k_cache);
   REQUIRE_PTR(a->v_cache);
-  REQUIRE_PTR(a->out);
-  REQUIRE(a->block_tables && a->seq_lens && a->lse, "block_tables, seq_lens and lse are required");
-  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
-  return launched(cp_launch_decode(*a, scale, as_stream(stream)), "decode launch");
+  REQUIRE(a->block_tables && a->seq_lens, "block_tables and seq_lens are required");
+  if (need_partials) {
+    REQUIRE_PTR(a->out);
+    REQUIRE(a->lse != nullptr, "lse is required");
+  }
+  return ok();
 }
 
 }  // extern "C"

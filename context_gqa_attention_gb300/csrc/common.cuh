@@ -87,3 +87,23 @@ cudaError_t cp_launch_prefill_simt(const cp_prefill_args& a, float scale, cudaSt
 cudaError_t cp_launch_prefill_tc(const cp_prefill_args& a, float scale, cudaStream_t s);
 bool cp_prefill_tc_supported(const cp_prefill_args& a);
 cudaError_t cp_launch_decode(const cp_decode_args& a, float scale, cudaStream_t s);
+
+// Scratch of the fused decode: arrival counters [B][Hkv] (zero between calls), partial LSEs
+// [cp*S][B][Hq] and partial outputs [cp*S][B][Hq][d], each region 256-byte aligned.
+struct CpDecodeWorkspace {
+  int32_t* counters;
+  float* partial_lse;
+  float* partial_out;
+};
+inline size_t cp_align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline size_t cp_decode_ws_layout(int B, int Hq, int Hkv, int d, int P, size_t* off_lse,
+                                  size_t* off_out) {
+  const size_t c = cp_align256((size_t)B * Hkv * sizeof(int32_t));
+  const size_t l = cp_align256((size_t)P * B * Hq * sizeof(float));
+  const size_t o = cp_align256((size_t)P * B * Hq * d * sizeof(float));
+  *off_lse = c;
+  *off_out = c + l;
+  return c + l + o;
+}
+cudaError_t cp_launch_decode_fused(const cp_decode_args& a, float scale, const CpDecodeWorkspace& ws,
+                                   void* out, float* out_lse, cudaStream_t s);

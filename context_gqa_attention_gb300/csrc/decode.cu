@@ -26,9 +26,13 @@ struct DecodeParams {
   const void* vc;
   const int32_t* tables;
   const int32_t* seq_lens;
-  float* out;
-  float* lse;
+  float* out;   // partials [cp*S][B][Hq][D] (the workspace when fused)
+  float* lse;   // partial LSEs [cp*S][B][Hq]
   int32_t* err;
+  // fused merge: per-(sequence, kv head) arrival counters, final output and LSE
+  int32_t* counters;
+  void* final_out;
+  float* final_lse;
 };
 
 template <typename T> struct Vec;
@@ -61,7 +65,54 @@ CP_DEV uint4 ldg_stream(const void* p) {
   return r;
 }
 
+// Fused merge (decode): after a CTA has written its partial it counts itself in for its
+// (sequence, kv head); the CTA that arrives last merges the cp * splits partials of the G heads
+// (the LSE merge: weights 2^(lse_p - M), empty partials skipped), writes the final output and
+// LSE and returns the counter to zero for the next call.  Publication follows the
+// fence-then-count pattern: each CTA fences its partial before the atomic increment, and the
+// last one fences again before reading the others' partials through L2.  No CTA waits on
+// another, so nothing can stall.
 template <typename T, int D, int G>
+CP_DEV void fused_tail(const DecodeParams& p, int b, int g) {
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int P = p.cp * p.S;
+    const int prev = atomicAdd(p.counters + (long long)b * p.Hkv + g, 1);
+    s_last = (prev == P - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int P = p.cp * p.S;
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int hh = i / D, dd = i % D;
+    const long long unit = (long long)b * p.Hq + (long long)g * G + hh;
+    const long long stride = (long long)p.B * p.Hq;
+    float M = -INFINITY;
+    for (int q = 0; q < P; ++q) M = fmaxf(M, __ldcg(p.lse + q * stride + unit) * kLog2e);
+    float Ls = 0.f, Os = 0.f;
+    if (M > -INFINITY) {
+      for (int q = 0; q < P; ++q) {
+        const float lq = __ldcg(p.lse + q * stride + unit) * kLog2e;
+        if (lq == -INFINITY) continue;
+        const float w = exp2f(lq - M);
+        Ls += w;
+        Os += w * __ldcg(p.out + (q * stride + unit) * D + dd);
+      }
+    }
+    const float o = Ls > 0.f ? Os / Ls : 0.f;
+    if constexpr (sizeof(T) == 2)
+      static_cast<__nv_bfloat16*>(p.final_out)[unit * D + dd] = __float2bfloat16_rn(o);
+    else
+      static_cast<float*>(p.final_out)[unit * D + dd] = o;
+    if (dd == 0 && p.final_lse) p.final_lse[unit] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+  }
+  if (threadIdx.x == 0) p.counters[(long long)b * p.Hkv + g] = 0;
+}
+
+template <typename T, int D, int G, bool FUSED>
 __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams p) {
   constexpr int EPV = Vec<T>::N;          // elements per 16-byte vector
   constexpr int QKV = (D / 2) / EPV;      // K vectors per lane: token lane/2, vectors 2i+lane%2
@@ -87,6 +138,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
 
   if (l0 >= l1) {  // nothing of this rank falls in this split
     if (threadIdx.x < G) p.lse[obase + threadIdx.x] = -INFINITY;
+    if constexpr (FUSED) fused_tail<T, D, G>(p, b, g);
     return;
   }
 
@@ -245,25 +297,32 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
       p.lse[obase + hh] = -INFINITY;
     }
   }
+  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g);
+
 }
 
-template <typename T, int D>
+template <typename T, int D, bool F>
 cudaError_t launch_g(const DecodeParams& p, int G, dim3 grid, cudaStream_t s) {
   switch (G) {
-    case 1: decode_kernel<T, D, 1><<<grid, kWarps * 32, 0, s>>>(p); break;
-    case 2: decode_kernel<T, D, 2><<<grid, kWarps * 32, 0, s>>>(p); break;
-    case 4: decode_kernel<T, D, 4><<<grid, kWarps * 32, 0, s>>>(p); break;
-    case 8: decode_kernel<T, D, 8><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 1: decode_kernel<T, D, 1, F><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 2: decode_kernel<T, D, 2, F><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 4: decode_kernel<T, D, 4, F><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 8: decode_kernel<T, D, 8, F><<<grid, kWarps * 32, 0, s>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }
 
-}  // namespace
-}  // namespace cpattn
+template <bool F>
+cudaError_t launch_all(const DecodeParams& p, const cp_decode_args& a, dim3 grid, cudaStream_t s) {
+  const int G = a.num_q_heads / a.num_kv_heads;
+  if (a.dtype == CP_BF16)
+    return a.head_dim == 64 ? launch_g<__nv_bfloat16, 64, F>(p, G, grid, s)
+                            : launch_g<__nv_bfloat16, 128, F>(p, G, grid, s);
+  return a.head_dim == 64 ? launch_g<float, 64, F>(p, G, grid, s) : launch_g<float, 128, F>(p, G, grid, s);
+}
 
-cudaError_t cp_launch_decode(const cp_decode_args& a, float scale, cudaStream_t s) {
-  using namespace cpattn;
+DecodeParams make_params(const cp_decode_args& a, float scale) {
   DecodeParams p;
   p.B = a.num_seqs;
   p.Hq = a.num_q_heads;
@@ -283,11 +342,31 @@ cudaError_t cp_launch_decode(const cp_decode_args& a, float scale, cudaStream_t 
   p.out = a.out;
   p.lse = a.lse;
   p.err = a.err;
-  const int G = a.num_q_heads / a.num_kv_heads;
+  p.counters = nullptr;
+  p.final_out = nullptr;
+  p.final_lse = nullptr;
+  return p;
+}
+
+}  // namespace
+}  // namespace cpattn
+
+cudaError_t cp_launch_decode(const cp_decode_args& a, float scale, cudaStream_t s) {
+  using namespace cpattn;
+  const DecodeParams p = make_params(a, scale);
   dim3 grid(a.num_splits, a.num_kv_heads, a.cp * a.num_seqs);
-  if (a.dtype == CP_BF16) {
-    return a.head_dim == 64 ? launch_g<__nv_bfloat16, 64>(p, G, grid, s)
-                            : launch_g<__nv_bfloat16, 128>(p, G, grid, s);
-  }
-  return a.head_dim == 64 ? launch_g<float, 64>(p, G, grid, s) : launch_g<float, 128>(p, G, grid, s);
+  return launch_all<false>(p, a, grid, s);
+}
+
+cudaError_t cp_launch_decode_fused(const cp_decode_args& a, float scale, const CpDecodeWorkspace& ws,
+                                   void* out, float* out_lse, cudaStream_t s) {
+  using namespace cpattn;
+  DecodeParams p = make_params(a, scale);
+  p.out = ws.partial_out;
+  p.lse = ws.partial_lse;
+  p.counters = ws.counters;
+  p.final_out = out;
+  p.final_lse = out_lse;
+  dim3 grid(a.num_splits, a.num_kv_heads, a.cp * a.num_seqs);
+  return launch_all<true>(p, a, grid, s);
 }

@@ -238,6 +238,25 @@ cp_status cp_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t cp, int
 cp_status cp_partial_attn_decode(const cp_decode_args* args, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * cp_decode_attention -- decode partial attention and its LSE merge in one launch
+ * ([PKV] Purpose: allgather decode -- every rank's partial, then their combination).
+ *
+ * Same inputs as cp_partial_attn_decode (args->out and args->lse are not used).  The
+ * cp * num_splits partials go to `workspace`; the last CTA to finish for a (sequence, kv
+ * head) merges them (as cp_lse_merge) and writes
+ *   out      device [B][Hq][d], dtype of q (bf16: round to nearest even)
+ *   out_lse  device f32 [B][Hq] or NULL.
+ * workspace: device scratch of at least cp_decode_workspace_size() bytes, 256-byte aligned,
+ * zero-filled before its first use (the call leaves it reusable: its counters return to
+ * zero).  Calls that use the same workspace must not overlap on the GPU.
+ * ---------------------------------------------------------------------------- */
+cp_status cp_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t cp, int32_t num_splits,
+                                   size_t* bytes);
+cp_status cp_decode_attention(const cp_decode_args* args, void* workspace, size_t workspace_bytes,
+                              void* out, float* out_lse, void* stream);
+
+/* ------------------------------------------------------------------------------
  * cp_lse_merge -- combine P partials into exact attention (the combine step after
  * partial attention, [PKV] Purpose).
  *

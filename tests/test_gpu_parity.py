@@ -105,6 +105,7 @@ PASS_KV_CASES = [
     ([515], 4, 4, 64, torch.bfloat16, 3),
     ([300, 5], 8, 1, 128, torch.bfloat16, 8),
     ([640], 8, 2, 128, torch.float32, 1),
+    ([4096], 16, 2, 128, torch.bfloat16, 2),      # ~512 work items: several per persistent CTA
 ]
 
 
@@ -165,6 +166,7 @@ PASS_Q_CASES = [
     ([130, 1, 64], [1000, 1, 64], 4, 1, 64, torch.bfloat16, 3, 4),
     ([50], [2000], 8, 8, 128, torch.float32, 2, 16),
     ([200], [1500], 8, 2, 128, torch.bfloat16, 1, 8),
+    ([512, 512], [4096, 3000], 16, 2, 128, torch.bfloat16, 4, 8),   # ~512 work items
 ]
 
 
@@ -246,3 +248,49 @@ def test_decode_explicit_single_split(lib):
     O, L = orc.decode_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"], x["seq_lens"],
                                cp, I, 16, 1 / math.sqrt(d))
     check_partials(out, lse, O, L, what="decode single split")
+
+
+@pytest.mark.parametrize("case", range(len(DECODE_CASES)))
+def test_decode_fused_parity(lib, case):
+    """cp_decode_attention (partials + merge in one launch) against the oracle, twice on the
+    same workspace (its arrival counters must come back to zero), and against the two-launch
+    path."""
+    B, (lo, hi), Hq, Hkv, d, dt, cp, I = DECODE_CASES[case]
+    lens = wl.decode_lengths(B, lo, hi, seed=400 + case).tolist()
+    lens[0] = hi
+    x = wl.paged_inputs(B, 1, lens, Hq, Hkv, d, dt, cp, I, 16, 500 + case, 600 + case,
+                        q_is_decode=True)
+    dev = {n: x[n].to(DEV) for n in ("q", "k_cache", "v_cache", "block_tables", "seq_lens")}
+    ns, st = lib.cp_decode_plan(B, Hkv, cp, I, 16, max(lens))
+    ws = torch.zeros(lib.cp_decode_workspace_size(B, Hq, Hkv, d, cp, ns), dtype=torch.uint8,
+                     device=DEV)
+    O, L = orc.decode_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"], x["seq_lens"],
+                               cp, I, 16, 1 / math.sqrt(d))
+    Om, Lm = orc.lse_merge(O, L)
+    outs = []
+    for _ in range(2):
+        out, lse = lib.cp_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"],
+                                           dev["block_tables"], dev["seq_lens"], cp, I,
+                                           num_splits=ns, split_tokens=st, workspace=ws)
+        check_merged(out, lse, Om, Lm, what="fused decode")
+        outs.append(out.clone())
+    assert torch.equal(outs[0], outs[1])
+    counters = ws[: B * Hkv * 4].view(torch.int32)
+    assert int(counters.abs().sum().item()) == 0
+    po, pl = lib.cp_partial_attn_decode(dev["q"], dev["k_cache"], dev["v_cache"],
+                                        dev["block_tables"], dev["seq_lens"], cp, I,
+                                        num_splits=ns, split_tokens=st)
+    mo, _ = lib.cp_lse_merge(po, pl, out_dtype=dt)
+    assert (mo.float() - outs[0].float()).abs().max().item() <= 1e-2
+
+
+def test_decode_fused_rejects_small_workspace(lib):
+    q = torch.zeros(2, 8, 128, dtype=torch.bfloat16, device=DEV)
+    kc = torch.zeros(1, 4, 2, 16, 128, dtype=torch.bfloat16, device=DEV)
+    tables = torch.zeros(1, 2, 2, dtype=torch.int32, device=DEV)
+    lens = torch.tensor([3, 5], dtype=torch.int32, device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(lib.CPError) as e:
+        lib.cp_decode_attention(q, kc, kc, tables, lens, 1, 8, num_splits=1, split_tokens=16,
+                                workspace=ws)
+    assert e.value.status == 1 and "workspace" in e.value.detail
