@@ -35,12 +35,35 @@ import torch  # noqa: E402
 
 import workloads as wl  # noqa: E402
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernels,
+# each from one ncu capture summarised under profiles/.  A figure is reported only while the
+# kernel's source file still has the SHA-1 the capture was taken on; otherwise traffic is null.
+NCU_TRAFFIC = {
+    # profiles/prefill_tc2_full_prefill.md: dram read 42.06 MB + write 65.12 MB
+    "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
+                "sha1": "0111a2b9414ea34c639d21667f38c1984de07853", "bytes": 107174912,
+                "workload": "full"},
+    "decode": None,
+}
+
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 * 1024 * 1024
 
 
 # ------------------------------------------------------------------------------------- utils
+
+def ncu_traffic(kind, workload):
+    import hashlib
+    rec = NCU_TRAFFIC.get(kind)
+    if not rec or rec.get("workload") != workload:
+        return None
+    path = os.path.join(ROOT, rec["file"])
+    with open(path, "rb") as f:
+        if hashlib.sha1(f.read()).hexdigest() != rec["sha1"]:
+            return None
+    return rec["bytes"]
+
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -472,7 +495,8 @@ def main():
         achieved = runner.flops / dom_s / 1e12
         roof = {"bound": "tensor", "kernel": "cp_partial_attn_prefill (pass-KV)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{src} bf16 dense (burst)", "traffic": None,
+                "peak_source": f"{src} bf16 dense (burst)",
+                "traffic": ncu_traffic("prefill", w.name),
                 "algorithmic": f"{runner.flops:.4e} causal FLOP per launch",
                 "launch_ms": dom_s * 1e3}
         metric = "causal GQA prefill TFLOP/s (pass-KV partial attention + LSE merge)"
@@ -483,7 +507,8 @@ def main():
         achieved = runner.bytes / dom_s / 1e9
         roof = {"bound": "hbm", "kernel": "cp_partial_attn_decode", "achieved": achieved,
                 "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": f"{src} HBM copy", "traffic": None, "launch_ms": dom_s * 1e3,
+                "peak_source": f"{src} HBM copy", "traffic": ncu_traffic("decode", w.name),
+                "launch_ms": dom_s * 1e3,
                 "algorithmic": f"{runner.bytes:.4e} B per launch (KV once + q + out + tables)"}
         metric = "decode KV-read GB/s (partial attention + LSE merge)"
         roof["kernel"] = "cp_decode_attention (fused partials + merge)" if runner.fused else roof["kernel"]

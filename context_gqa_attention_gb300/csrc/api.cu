@@ -491,6 +491,9 @@ cp_status cp_decode_attention(const cp_decode_args* a, void* workspace, size_t w
   REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
           "workspace must be a non-null 256-byte aligned pointer");
   REQUIRE_PTR(out);
+  if ((long long)a->cp * a->num_splits > 256)
+    return fail(CP_ERR_UNSUPPORTED, "cp * num_splits must be <= 256 for the fused decode (got %d)",
+                a->cp * a->num_splits);
   size_t ol, oo;
   const size_t need = cp_decode_ws_layout(a->num_seqs, a->num_q_heads, a->num_kv_heads, a->head_dim,
                                           a->cp * a->num_splits, &ol, &oo);
@@ -536,3 +539,4 @@ static cp_status check_decode_args(const cp_decode_args* a, bool need_partials) 
 }
 
 }  // extern "C"
+

@@ -16,6 +16,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kPage = 16;  // tokens per page (block_size)
+constexpr int kMaxFusedPartials = 256;  // cp * splits of one fused decode call
 
 struct DecodeParams {
   int B, Hq, Hkv, cp, I, S, ST, max_blocks;
@@ -67,53 +68,83 @@ CP_DEV uint4 ldg_stream(const void* p) {
 
 // Fused merge (decode): after a CTA has written its partial it counts itself in for its
 // (sequence, kv head); the CTA that arrives last merges the cp * splits partials of the G heads
-// (the LSE merge: weights 2^(lse_p - M), empty partials skipped), writes the final output and
-// LSE and returns the counter to zero for the next call.  Publication follows the
+// (the LSE merge: weights 2^(lse_p - M) staged once in shared memory, empty partials weigh 0),
+// writes the final output and LSE and returns the counter to zero for the next call.  Publication follows the
 // fence-then-count pattern: each CTA fences its partial before the atomic increment, and the
 // last one fences again before reading the others' partials through L2.  No CTA waits on
 // another, so nothing can stall.
 template <typename T, int D, int G>
 CP_DEV void fused_tail(const DecodeParams& p, int b, int g) {
   __shared__ int s_last;
+  __shared__ float s_w[kMaxFusedPartials * G];  // per (partial, head): log2 LSE, then weight
+  __shared__ float s_M[G], s_L[G];
   __syncthreads();
+  const int P = p.cp * p.S;
   if (threadIdx.x == 0) {
     __threadfence();
-    const int P = p.cp * p.S;
     const int prev = atomicAdd(p.counters + (long long)b * p.Hkv + g, 1);
     s_last = (prev == P - 1);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const int P = p.cp * p.S;
+  const long long stride = (long long)p.B * p.Hq;           // between partials
+  const long long unit0 = (long long)b * p.Hq + (long long)g * G;
+  for (int i = threadIdx.x; i < P * G; i += blockDim.x)
+    s_w[i] = __ldcg(p.lse + (i / G) * stride + unit0 + i % G) * kLog2e;
+  __syncthreads();
+  if (threadIdx.x < G) {
+    float M = -INFINITY;
+    for (int q = 0; q < P; ++q) M = fmaxf(M, s_w[q * G + threadIdx.x]);
+    s_M[threadIdx.x] = M;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < P * G; i += blockDim.x) {
+    const float M = s_M[i % G], lq = s_w[i];
+    s_w[i] = (M > -INFINITY && lq > -INFINITY) ? exp2f(lq - M) : 0.f;
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    float L = 0.f;
+    for (int q = 0; q < P; ++q) L += s_w[q * G + threadIdx.x];
+    s_L[threadIdx.x] = L;
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int hh = i / D, dd = i % D;
-    const long long unit = (long long)b * p.Hq + (long long)g * G + hh;
-    const long long stride = (long long)p.B * p.Hq;
-    float M = -INFINITY;
-    for (int q = 0; q < P; ++q) M = fmaxf(M, __ldcg(p.lse + q * stride + unit) * kLog2e);
-    float Ls = 0.f, Os = 0.f;
-    if (M > -INFINITY) {
-      for (int q = 0; q < P; ++q) {
-        const float lq = __ldcg(p.lse + q * stride + unit) * kLog2e;
-        if (lq == -INFINITY) continue;
-        const float w = exp2f(lq - M);
-        Ls += w;
-        Os += w * __ldcg(p.out + (q * stride + unit) * D + dd);
+    const float* src = p.out + (unit0 + hh) * D + dd;
+    const long long pstride = stride * D;
+    float acc = 0.f;
+    int q = 0;
+    for (; q + 8 <= P; q += 8) {  // eight partial rows in flight (empty ones weigh 0)
+      float x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = __ldcg(src + (q + u) * pstride);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float w = s_w[(q + u) * G + hh];
+        acc += w > 0.f ? w * x[u] : 0.f;
       }
     }
-    const float o = Ls > 0.f ? Os / Ls : 0.f;
+    for (; q < P; ++q) {
+      const float w = s_w[q * G + hh];
+      const float x = __ldcg(src + q * pstride);
+      acc += w > 0.f ? w * x : 0.f;
+    }
+    const float L = s_L[hh];
+    const float o = L > 0.f ? acc / L : 0.f;
     if constexpr (sizeof(T) == 2)
-      static_cast<__nv_bfloat16*>(p.final_out)[unit * D + dd] = __float2bfloat16_rn(o);
+      static_cast<__nv_bfloat16*>(p.final_out)[(unit0 + hh) * D + dd] = __float2bfloat16_rn(o);
     else
-      static_cast<float*>(p.final_out)[unit * D + dd] = o;
-    if (dd == 0 && p.final_lse) p.final_lse[unit] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+      static_cast<float*>(p.final_out)[(unit0 + hh) * D + dd] = o;
+    if (dd == 0 && p.final_lse)
+      p.final_lse[unit0 + hh] = L > 0.f ? (s_M[hh] + log2f(L)) * kLn2 : -INFINITY;
   }
   if (threadIdx.x == 0) p.counters[(long long)b * p.Hkv + g] = 0;
 }
 
 template <typename T, int D, int G, bool FUSED>
-__global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 4) decode_kernel(const DecodeParams p) {
   constexpr int EPV = Vec<T>::N;          // elements per 16-byte vector
   constexpr int QKV = (D / 2) / EPV;      // K vectors per lane: token lane/2, vectors 2i+lane%2
   constexpr int NCH = D / EPV;            // V chunks per token
@@ -127,7 +158,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
   __shared__ __align__(16) float o_w[kWarps][G][D];
 
   const int split = blockIdx.x, g = blockIdx.y;
-  const int r = blockIdx.z / p.B, b = blockIdx.z % p.B;
+  // the cp ranks of a sequence are adjacent in launch order, so a (sequence, kv head) group's
+  // CTAs run together and its fused merge is not deferred to the end of the grid
+  const int r = blockIdx.z % p.cp, b = blockIdx.z / p.cp;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = __ldg(p.seq_lens + b);
   const int n = rank_local_len(L, r, p.cp, p.I);
@@ -370,3 +403,4 @@ cudaError_t cp_launch_decode_fused(const cp_decode_args& a, float scale, const C
   dim3 grid(a.num_splits, a.num_kv_heads, a.cp * a.num_seqs);
   return launch_all<true>(p, a, grid, s);
 }
+

@@ -38,7 +38,6 @@ constexpr float kRescaleThreshold = 8.f;     // log2 units
 
 struct TcParams {
   int mode, B, Hq, Hkv, cp, I, max_blocks, q_shard, kv_shard, TPC, Nq, debug;
-  long long n_items;
   long long pool, budget;
   float scale_log2;
   const int32_t* cu_q;
@@ -78,12 +77,12 @@ struct Work {
   int ntiles;
 };
 
-// item -> (q tile slot, sequence, kv shard, head group of `hpc` consecutive q heads).
+// blockIdx.x -> (q tile slot, sequence, kv shard, head group of `hpc` consecutive q heads).
 // Slots run heaviest first (last chunk, last tile) so long items start early.
-CP_DEV Work decode_work(const TcParams& p, int hpc, long long item) {
+CP_DEV Work decode_work(const TcParams& p, int hpc) {
   Work w;
   w.valid = 0;
-  long long lin = item;
+  long long lin = blockIdx.x;
   const int groups = p.Hq / hpc;
   w.h = (int)(lin % groups) * hpc;
   lin /= groups;
@@ -294,6 +293,30 @@ CP_DEV float row_exp_store(float (&v0)[32], float (&v1)[32], float (&v2)[32], fl
   return lo + hi;
 }
 
+// Exponentials of a row packed as bf16 pairs into the first 64 columns of its S buffer in TMEM
+// (the A operand of a tensor-memory PV MMA), 16 columns per store; returns the row sum of p.
+CP_DEV void exp_pack_tmem(float (&a)[32], uint64_t sc2, uint64_t n2, uint64_t& sum2, uint32_t taddr) {
+  exp_chunk(a, sc2, n2, sum2);
+  uint32_t pk[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(a[2 * k], a[2 * k + 1]);
+  tmem_st16(taddr, pk);
+}
+CP_DEV float row_exp_tmem(float (&v0)[32], float (&v1)[32], float (&v2)[32], float (&v3)[32],
+                          float sc, float m, uint32_t tS) {
+  const float neg = (m == -INFINITY) ? 0.f : -m;
+  const uint64_t sc2 = f2(sc, sc), n2 = f2(neg, neg);
+  uint64_t sum2 = f2(0.f, 0.f);
+  exp_pack_tmem(v0, sc2, n2, sum2, tS);
+  exp_pack_tmem(v1, sc2, n2, sum2, tS + 16);
+  exp_pack_tmem(v2, sc2, n2, sum2, tS + 32);
+  exp_pack_tmem(v3, sc2, n2, sum2, tS + 48);
+  tmem_wait_st();
+  float lo, hi;
+  f2u(sum2, lo, hi);
+  return lo + hi;
+}
+
 // P row (bf16) into a 128x128 P tile stored as two 64-column blocks in the 128-byte-swizzled
 // K-major layout the MMA reads: 16-byte chunk c of row r sits at chunk c ^ (r % 8).
 CP_DEV void store_p_row(uint32_t sP, int row, const float (&v0)[32], const float (&v1)[32],
@@ -359,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int KB = D / 64;  // 64-column (128-byte) blocks of a head row
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Work w = decode_work(p, 1, blockIdx.x);
+  const Work w = decode_work(p, 1);
   if (!w.valid) return;  // uniform over the CTA
 
   if (w.ntiles == 0) {  // no visible key in this pair: an empty partial
@@ -618,54 +641,58 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------- kernel 2
-// Persistent, two query heads per work item.  One CTA per SM walks the work items in a
-// heavy-first "snake" order (round k visits its slot from the front on even rounds and from
-// the back on odd rounds), so every CTA gets a mix of long and short items.
-//
-// Item = two query heads of the same kv group (tiles 0 and 1: heads h, h+1, same 128 rows)
-// against one kv shard, sharing every K/V tile.  Warps: 0 TMA producer, 1 TMEM owner + MMA
-// issuer, 2-5 softmax of tile 0, 6-9 softmax of tile 1 (warp w reads TMEM lanes 32 (w % 4) ..).
-// TMEM: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D).  K and V tiles stream
-// through a 3-slot ring (K(t), V(t) alternate) that runs on across items.  Tensor-core order
-// per key tile t:   PV0(t) | QK0(t+1) | PV1(t) | QK1(t+1)
-// so the softmax of each tile overlaps the other tile's two MMAs.  Between items the MMA issuer
-// signals `q_empty` (the Q buffers may be refilled) and each softmax warpgroup signals
-// `o_free` once it has read its O accumulator, so the next item's loads, QK and first PV overlap
-// the previous item's epilogue.  Barrier phases are counted across items.
+// Two query heads of the same kv group per CTA (tiles 0 and 1: heads h, h+1, same 128 rows),
+// sharing every K/V tile.  Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2-5 softmax of
+// tile 0, 6-9 softmax of tile 1 (warp w reads TMEM lanes 32 (w % 4) ..).  TMEM: S0 [0,128), S1 [128,256),
+// O0 [256, 256+D), O1 [256+D, 256+2D).  K and V tiles stream through a 3-slot ring (load i:
+// K(t) for i = 2t, V(t) for i = 2t+1).  Tensor-core order per key tile t:
+//   PV0(t) | QK0(t+1) | PV1(t) | QK1(t+1)
+// so the softmax of each tile overlaps the other tile's two MMAs.
+// With PT (P in TMEM) the softmax writes P as packed bf16 pairs over the first 64 columns of
+// its own S buffer and the PV MMA reads A from tensor memory; the 64 KB of P tiles are given to
+// the K/V ring instead (5 slots).
 constexpr int kThreads2 = 320;
-constexpr int NSLOT = 3;
+constexpr bool kPInTmem = true;
 
-template <int D>
+template <int D, bool PT>
 struct Layout2 {
+  static constexpr int NSLOT = PT ? 5 : 3;
   static constexpr int kQ = BM * D * 2;
   static constexpr int kKV = BN * D * 2;
   static constexpr int kP = BM * BN * 2;
   static constexpr int oQ = 0;
   static constexpr int oKV = 2 * kQ;
   static constexpr int oP = oKV + NSLOT * kKV;
-  static constexpr int oBar = oP + 2 * kP;
-  static constexpr int bQ = 0, bQE = 1, bFull = 2, bEmpty = bFull + NSLOT, bS = bEmpty + NSLOT,
-                       bP = bS + 2, bO = bP + 2, bOF = bO + 2, bDone = bOF + 2, nBar = bDone + 1;
+  static constexpr int oBar = oP + (PT ? 0 : 2 * kP);
+  static constexpr int bQ = 0, bFull = 1, bEmpty = bFull + NSLOT, bS = bEmpty + NSLOT, bP = bS + 2,
+                       bO = bP + 2, bDone = bO + 2, nBar = bDone + 1;
   static constexpr int oMisc = oBar + nBar * 8;
   static constexpr int kBytes = oMisc + 16;
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
 };
 
-// k-th item of this CTA in the snake order (>= n_items when done).
-CP_DEV long long snake_item(long long k, int cta, int ctas) {
-  return k * ctas + ((k & 1) ? (ctas - 1 - cta) : cta);
-}
-
-template <int D>
+template <int D, bool PT>
 __global__ void __launch_bounds__(kThreads2, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_v, const TcParams p) {
-  using Ly = Layout2<D>;
+  using Ly = Layout2<D, PT>;
+  constexpr int NSLOT = Ly::NSLOT;
   constexpr int KB = D / 64;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cta = blockIdx.x, ctas = gridDim.x;
+  const Work w = decode_work(p, 2);
+  if (!w.valid) return;
+
+  if (w.ntiles == 0) {  // empty pair
+    if (warp >= 2) {
+      const int tile = (warp - 2) >> 2;
+      const int row = (warp & 3) * 32 + lane;
+      if (w.q_lo + row < w.q_hi)
+        p.lse[((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile] = -INFINITY;
+    }
+    return;
+  }
 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -678,7 +705,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Ly::bQ), 1);
-    mbar_init(bar(Ly::bQE), 1);
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(bar(Ly::bFull + s), 1);
       mbar_init(bar(Ly::bEmpty + s), 1);
@@ -687,7 +713,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_init(bar(Ly::bS + i), 1);
       mbar_init(bar(Ly::bP + i), 4);
       mbar_init(bar(Ly::bO + i), 1);
-      mbar_init(bar(Ly::bOF + i), 4);
     }
     mbar_init(bar(Ly::bDone), 1);
     misc[1] = 0u;
@@ -708,84 +733,69 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      int last0 = -1, last1 = -1, last2 = -1;  // phase of the last fill of each slot
-      uint32_t L = 0;                          // ring position (loads issued, all items)
-      int it = 0;                              // items with work done by this CTA
-      bool ok = true, q_issued = false;
-      int prow[BN / 16];  // pass-Q: element rows of the current tile's pages (K and V alike)
-      for (long long k = 0; ok; ++k) {
-        const long long item = snake_item(k, cta, ctas);
-        if (item >= p.n_items) break;
-        const Work w = decode_work(p, 2, item);
-        if (!w.valid || w.ntiles == 0) continue;
-        if (it > 0 && !mbar_wait(bar(Ly::bQE), (uint32_t)(it - 1) & 1u, abort_flag, p.budget)) {
-          ok = false;
-          break;
-        }
-        mbar_expect_tx(bar(Ly::bQ), 2 * Ly::kQ);
+      mbar_expect_tx(bar(Ly::bQ), 2 * Ly::kQ);
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+          tma_load_2d(sQ + i * Ly::kQ + kb * BM * 128, &map_q, (w.h + i) * D + kb * 64, w.q_row0,
+                      bar(Ly::bQ));
+      int last0 = -1, last1 = -1, last2 = -1;  // phase of the last fill of each slot
+      const int32_t* trow =
+          p.mode == CP_PASS_Q ? p.tables + ((long long)w.p * p.B + w.b) * p.max_blocks : nullptr;
+      int prow[BN / 16];  // pass-Q: element rows of the current tile's pages (K and V alike)
+      bool ok = true;
+      for (int i = 0; i < 2 * w.ntiles; ++i) {
+        const int slot = i % NSLOT;
+        const uint32_t ph = (uint32_t)(i / NSLOT) & 1u;
+        const int t = i >> 1;
+        const bool isV = (i & 1) != 0;
+        if (!mbar_wait(bar(Ly::bEmpty + slot), ph ^ 1u, abort_flag, p.budget)) { ok = false; break; }
+        if (isV && (p.debug & 1)) continue;  // testing: V never arrives
+        const uint32_t dst = sKV + slot * Ly::kKV;
+        const CUtensorMap* map = isV ? &map_v : &map_k;
+        mbar_expect_tx(bar(Ly::bFull + slot), Ly::kKV);
+        if (p.mode == CP_PASS_KV) {
+          const bool r0 = t < w.nt[0];
+          const int y = w.kv_row0 + (r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN);
 #pragma unroll
           for (int kb = 0; kb < KB; ++kb)
-            tma_load_2d(sQ + i * Ly::kQ + kb * BM * 128, &map_q, (w.h + i) * D + kb * 64, w.q_row0,
-                        bar(Ly::bQ));
-        q_issued = true;
-        const int32_t* trow =
-            p.mode == CP_PASS_Q ? p.tables + ((long long)w.p * p.B + w.b) * p.max_blocks : nullptr;
-        for (int i = 0; i < 2 * w.ntiles; ++i, ++L) {
-          const int slot = (int)(L % NSLOT);
-          const uint32_t ph = (L / NSLOT) & 1u;
-          const int t = i >> 1;
-          const bool isV = (i & 1) != 0;
-          if (!mbar_wait(bar(Ly::bEmpty + slot), ph ^ 1u, abort_flag, p.budget)) { ok = false; break; }
-          if (isV && (p.debug & 1)) continue;  // testing: V never arrives
-          const uint32_t dst = sKV + slot * Ly::kKV;
-          const CUtensorMap* map = isV ? &map_v : &map_k;
-          mbar_expect_tx(bar(Ly::bFull + slot), Ly::kKV);
-          if (p.mode == CP_PASS_KV) {
-            const bool r0 = t < w.nt[0];
-            const int y = w.kv_row0 + (r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN);
+            tma_load_2d(dst + kb * BN * 128, map, w.g * D + kb * 64, y, bar(Ly::bFull + slot));
+        } else {
+          if (!isV) {  // page rows of tile t (reused for its V load)
+            int last_good = -1;
 #pragma unroll
-            for (int kb = 0; kb < KB; ++kb)
-              tma_load_2d(dst + kb * BN * 128, map, w.g * D + kb * 64, y, bar(Ly::bFull + slot));
-          } else {
-            if (!isV) {  // page rows of tile t (reused for its V load)
-              int last_good = -1;
-#pragma unroll
-              for (int j = 0; j < BN / 16; ++j) {
-                const int l = t * BN + j * 16;
-                int pg = -1;
-                if (l < w.n_local) {
-                  const int col = l / 16;
-                  pg = col < p.max_blocks ? __ldg(trow + col) : -1;
-                  if (pg < 0 || pg >= p.pool) {
-                    report(p.err, CP_ERR_DEVICE_BOUNDS);
-                    pg = -1;
-                  }
+            for (int j = 0; j < BN / 16; ++j) {
+              const int l = t * BN + j * 16;
+              int pg = -1;
+              if (l < w.n_local) {
+                const int col = l / 16;
+                pg = col < p.max_blocks ? __ldg(trow + col) : -1;
+                if (pg < 0 || pg >= p.pool) {
+                  report(p.err, CP_ERR_DEVICE_BOUNDS);
+                  pg = -1;
                 }
-                if (pg >= 0) last_good = pg;
-                prow[j] = pg;
               }
-              if (last_good < 0) last_good = 0;
-#pragma unroll
-              for (int j = 0; j < BN / 16; ++j)
-                prow[j] = (int)((((long long)w.p * p.pool + (prow[j] >= 0 ? prow[j] : last_good)) *
-                                     p.Hkv + w.g) * 16);
+              if (pg >= 0) last_good = pg;
+              prow[j] = pg;
             }
+            if (last_good < 0) last_good = 0;
 #pragma unroll
             for (int j = 0; j < BN / 16; ++j)
-#pragma unroll
-              for (int kb = 0; kb < KB; ++kb)
-                tma_load_2d(dst + kb * BN * 128 + j * 16 * 128, map, kb * 64, prow[j],
-                            bar(Ly::bFull + slot));
+              prow[j] = (int)((((long long)w.p * p.pool + (prow[j] >= 0 ? prow[j] : last_good)) *
+                                   p.Hkv + w.g) * 16);
           }
-          if (slot == 0) last0 = (int)ph; else if (slot == 1) last1 = (int)ph; else last2 = (int)ph;
+#pragma unroll
+          for (int j = 0; j < BN / 16; ++j)
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb)
+              tma_load_2d(dst + kb * BN * 128 + j * 16 * 128, map, kb * 64, prow[j],
+                          bar(Ly::bFull + slot));
         }
-        ++it;
+        if (slot == 0) last0 = (int)ph; else if (slot == 1) last1 = (int)ph; else last2 = (int)ph;
       }
       if (!ok) fail_timeout(abort_flag, p.err);
-      // drain: every copy issued into this CTA's shared memory has landed before it exits
-      if (q_issued) mbar_wait(bar(Ly::bQ), (uint32_t)(it - 1) & 1u, nullptr, p.budget);
+      mbar_wait(bar(Ly::bQ), 0u, nullptr, p.budget);
       if (last0 >= 0) mbar_wait(bar(Ly::bFull + 0), (uint32_t)last0, nullptr, p.budget);
       if (last1 >= 0) mbar_wait(bar(Ly::bFull + 1), (uint32_t)last1, nullptr, p.budget);
       if (last2 >= 0) mbar_wait(bar(Ly::bFull + 2), (uint32_t)last2, nullptr, p.budget);
@@ -807,70 +817,59 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
       };
       auto issue_pv = [&](int tile, int slot, bool acc) {
-        const uint32_t pp = sP + tile * Ly::kP, v = sKV + slot * Ly::kKV;
+        const uint32_t v = sKV + slot * Ly::kKV;
         const uint32_t dO = tmem + 256u + (uint32_t)(tile * D);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t offp = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-          mma_ss(dO, desc_sw128(pp + offp, 16, 1024), desc_sw128(v + kk * 16 * 128, BN * 128, 1024),
-                 id_pv, (acc || kk > 0) ? 1u : 0u);
+          const uint64_t bd = desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
+          if constexpr (PT) {  // P: 8 packed columns per 16 keys
+            mma_ts(dO, tmem + (uint32_t)(tile * BN + kk * 8), bd, id_pv, (acc || kk > 0) ? 1u : 0u);
+          } else {
+            const uint32_t offp = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+            mma_ss(dO, desc_sw128(sP + tile * Ly::kP + offp, 16, 1024), bd, id_pv,
+                   (acc || kk > 0) ? 1u : 0u);
+          }
         }
       };
-      uint32_t L = 0, T = 0;  // ring position and tile steps, both counted across items
-      int it = 0;
-      bool ok = true;
-      for (long long k = 0; ok; ++k) {
-        const long long item = snake_item(k, cta, ctas);
-        if (item >= p.n_items) break;
-        const Work w = decode_work(p, 2, item);
-        if (!w.valid || w.ntiles == 0) continue;
-        ok = mbar_wait(bar(Ly::bQ), (uint32_t)it & 1u, abort_flag, p.budget);
-        if (ok) ok = mbar_wait(bar(Ly::bFull + L % NSLOT), (L / NSLOT) & 1u, abort_flag, p.budget);
+      bool ok = mbar_wait(bar(Ly::bQ), 0u, abort_flag, p.budget);
+      if (ok) ok = mbar_wait(bar(Ly::bFull + 0), 0u, abort_flag, p.budget);  // K(0): load 0
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0, 0);
+        mma_commit(bar(Ly::bS + 0));
+        issue_qk(1, 0);
+        mma_commit(bar(Ly::bS + 1));
+        mma_commit(bar(Ly::bEmpty + 0));
+      }
+      for (int t = 0; ok && t < w.ntiles; ++t) {
+        const int iv = 2 * t + 1, ik = 2 * t + 2;
+        const int sv = iv % NSLOT, sk = ik % NSLOT;
+        ok = mbar_wait(bar(Ly::bFull + sv), (uint32_t)(iv / NSLOT) & 1u, abort_flag, p.budget);
+        if (!ok) break;
+        ok = mbar_wait(bar(Ly::bP + 0), (uint32_t)t & 1u, abort_flag, p.budget);
         if (!ok) break;
         tc_fence_after();
-        issue_qk(0, (int)(L % NSLOT));
-        mma_commit(bar(Ly::bS + 0));
-        issue_qk(1, (int)(L % NSLOT));
-        mma_commit(bar(Ly::bS + 1));
-        mma_commit(bar(Ly::bEmpty + L % NSLOT));
-        for (int t = 0; ok && t < w.ntiles; ++t) {
-          const uint32_t iv = L + 2 * t + 1, ik = L + 2 * t + 2;
-          const int sv = (int)(iv % NSLOT), sk = (int)(ik % NSLOT);
-          const uint32_t step = T + t;
-          ok = mbar_wait(bar(Ly::bFull + sv), (iv / NSLOT) & 1u, abort_flag, p.budget);
-          if (ok) ok = mbar_wait(bar(Ly::bP + 0), step & 1u, abort_flag, p.budget);
-          if (ok && t == 0 && it > 0)  // the epilogue of the previous item has read O0
-            ok = mbar_wait(bar(Ly::bOF + 0), (uint32_t)(it - 1) & 1u, abort_flag, p.budget);
+        issue_pv(0, sv, t > 0);
+        mma_commit(bar(Ly::bO + 0));
+        const bool more = t + 1 < w.ntiles;
+        if (more) {
+          ok = mbar_wait(bar(Ly::bFull + sk), (uint32_t)(ik / NSLOT) & 1u, abort_flag, p.budget);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(0, sv, t > 0);
-          mma_commit(bar(Ly::bO + 0));
-          const bool more = t + 1 < w.ntiles;
-          if (more) {
-            ok = mbar_wait(bar(Ly::bFull + sk), (ik / NSLOT) & 1u, abort_flag, p.budget);
-            if (!ok) break;
-            tc_fence_after();
-            issue_qk(0, sk);
-            mma_commit(bar(Ly::bS + 0));
-          }
-          ok = mbar_wait(bar(Ly::bP + 1), step & 1u, abort_flag, p.budget);
-          if (ok && t == 0 && it > 0)
-            ok = mbar_wait(bar(Ly::bOF + 1), (uint32_t)(it - 1) & 1u, abort_flag, p.budget);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(1, sv, t > 0);
-          mma_commit(bar(Ly::bO + 1));
-          mma_commit(bar(Ly::bEmpty + sv));
-          if (more) {
-            issue_qk(1, sk);
-            mma_commit(bar(Ly::bS + 1));
-            mma_commit(bar(Ly::bEmpty + sk));
-          }
+          issue_qk(0, sk);
+          mma_commit(bar(Ly::bS + 0));
         }
-        mma_commit(bar(Ly::bQE));  // this item's MMAs are all issued: Q may be refilled after them
-        L += 2 * (uint32_t)w.ntiles;
-        T += (uint32_t)w.ntiles;
-        ++it;
+        ok = mbar_wait(bar(Ly::bP + 1), (uint32_t)t & 1u, abort_flag, p.budget);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(1, sv, t > 0);
+        mma_commit(bar(Ly::bO + 1));
+        mma_commit(bar(Ly::bEmpty + sv));
+        if (more) {
+          issue_qk(1, sk);
+          mma_commit(bar(Ly::bS + 1));
+          mma_commit(bar(Ly::bEmpty + sk));
+        }
       }
       if (!ok) fail_timeout(abort_flag, p.err);
       mma_commit(bar(Ly::bDone));
@@ -884,92 +883,57 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)(tile * BN);
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(tile * D);
-    const float sc = p.scale_log2;
-    uint32_t T = 0;
-    int it = 0;
+    const bool row_valid = w.q_lo + row < w.q_hi;
+    const long long qpos = w.qpos0 + row;
+    int nvis = 0;
+    if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
+    float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (long long k = 0; ok; ++k) {
-      const long long item = snake_item(k, cta, ctas);
-      if (item >= p.n_items) break;
-      const Work w = decode_work(p, 2, item);
-      if (!w.valid) continue;
-      const bool row_valid = w.q_lo + row < w.q_hi;
-      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile;
-      if (w.ntiles == 0) {  // no visible key in this pair: an empty partial
-        if (row_valid) p.lse[orow] = -INFINITY;
-        continue;
+    for (int t = 0; t < w.ntiles; ++t) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bS + tile), (uint32_t)t & 1u, abort_flag, p.budget));
+      if (!ok) break;
+      tc_fence_after();
+      float s0[32], s1[32], s2[32], s3[32];
+      load_row(tS, s0, s1, s2, s3);
+      int lim;
+      if (p.mode == CP_PASS_KV) {
+        const bool r0 = t < w.nt[0];
+        const int k0 = r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN;
+        const int ke = r0 ? w.ke[0] : w.ke[1];
+        lim = (int)min((long long)ke - 1, qpos) - k0;
+      } else {
+        lim = nvis - 1 - t * BN;
       }
-      const long long qpos = w.qpos0 + row;
-      int nvis = 0;
-      if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
-      float m = -INFINITY, l = 0.f;
-      for (int t = 0; t < w.ntiles; ++t) {
-        const uint32_t step = T + t;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bS + tile), step & 1u, abort_flag, p.budget));
-        if (!ok) break;
-        tc_fence_after();
-        float s0[32], s1[32], s2[32], s3[32];
-        load_row(tS, s0, s1, s2, s3);
-        int lim;
-        if (p.mode == CP_PASS_KV) {
-          const bool r0 = t < w.nt[0];
-          const int k0 = r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN;
-          const int ke = r0 ? w.ke[0] : w.ke[1];
-          lim = (int)min((long long)ke - 1, qpos) - k0;
-        } else {
-          lim = nvis - 1 - t * BN;
-        }
-        const float alpha = row_max_update(s0, s1, s2, s3, lim, sc, m);
+      const float alpha = row_max_update(s0, s1, s2, s3, lim, p.scale_log2, m);
+      if constexpr (PT) {
+        // S(t) complete implies PV(t-1) complete (it was issued before QK(t)): O is stable and
+        // the S columns may take P(t)
+        l = l * alpha + row_exp_tmem(s0, s1, s2, s3, p.scale_log2, m, tS);
+        if (t > 0) rescale_o<D>(tO, alpha);
+      } else {
         if (t > 0) {  // PV(t-1) of this tile finished before QK(t) began: P free, O stable
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO + tile), (step - 1) & 1u, abort_flag, p.budget));
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO + tile), (uint32_t)(t - 1) & 1u, abort_flag, p.budget));
           if (!ok) break;
           tc_fence_after();
         }
-        l = l * alpha + row_exp_store(s0, s1, s2, s3, sc, m, sP + tile * Ly::kP, row);
+        l = l * alpha + row_exp_store(s0, s1, s2, s3, p.scale_log2, m, sP + tile * Ly::kP, row);
         if (t > 0) rescale_o<D>(tO, alpha);
         fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Ly::bP + tile));
       }
-      if (ok)
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO + tile), (T + w.ntiles - 1) & 1u,
-                                               abort_flag, p.budget));
-      if (!ok) break;
-      tc_fence_after();
-      // O row in two halves: normalise + store the first while the second is read, then hand
-      // the accumulator back to the MMA issuer before the last stores
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool store = row_valid && l > 0.f;
-      float* dst = p.out + orow * D;
-#pragma unroll
-      for (int hf = 0; hf < (D + 63) / 64; ++hf) {
-        float oa[32], ob[32];
-        tmem_ld32(tO + hf * 64, oa);
-        if (D > 32) tmem_ld32(tO + hf * 64 + 32, ob);
-        tmem_wait_ld(oa);
-        if (D > 32) tmem_wait_ld(ob);
-        if (hf == (D + 63) / 64 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(Ly::bOF + tile));
-        }
-        if (store) {
-#pragma unroll
-          for (int kk = 0; kk < 32; kk += 4) {
-            *reinterpret_cast<float4*>(dst + hf * 64 + kk) =
-                make_float4(oa[kk] * inv_l, oa[kk + 1] * inv_l, oa[kk + 2] * inv_l, oa[kk + 3] * inv_l);
-            if (D > 32)
-              *reinterpret_cast<float4*>(dst + hf * 64 + 32 + kk) =
-                  make_float4(ob[kk] * inv_l, ob[kk + 1] * inv_l, ob[kk + 2] * inv_l, ob[kk + 3] * inv_l);
-          }
-        }
-      }
-      if (row_valid) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      T += (uint32_t)w.ntiles;
-      ++it;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(Ly::bP + tile));
     }
-    if (!ok) fail_timeout(abort_flag, p.err);
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO + tile), (uint32_t)(w.ntiles - 1) & 1u,
+                                             abort_flag, p.budget));
+    if (ok) {
+      tc_fence_after();
+      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile;
+      write_row<D>(tO, m, l, row_valid, p.out + orow * D, p.lse + orow);
+    } else {
+      fail_timeout(abort_flag, p.err);
+    }
   }
 
   tc_fence_before();
@@ -1060,18 +1024,13 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s) {
                          (a.num_q_heads / (pair ? 2 : 1));
   if (grid == 0) return cudaSuccess;
   if (grid >= (1ll << 31)) return cudaErrorInvalidConfiguration;
-  p.n_items = grid;
   cudaError_t e;
-  if (pair) {  // persistent: one CTA per SM walks the items
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (pair) {
+    const int smem = Layout2<D, kPInTmem>::kAlloc;
+    e = cudaFuncSetAttribute(prefill_tc2_kernel<D, kPInTmem>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const long long ctas = grid < sms ? grid : sms;
-    const int smem = Layout2<D>::kAlloc;
-    e = cudaFuncSetAttribute(prefill_tc2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    prefill_tc2_kernel<D><<<(unsigned)ctas, kThreads2, smem, s>>>(mq, mk, mv, p);
+    prefill_tc2_kernel<D, kPInTmem><<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, p);
   } else {
     const int smem = Layout<D>::kAlloc;
     e = cudaFuncSetAttribute(prefill_tc1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

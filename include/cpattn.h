@@ -246,6 +246,7 @@ cp_status cp_partial_attn_decode(const cp_decode_args* args, void* stream);
  * head) merges them (as cp_lse_merge) and writes
  *   out      device [B][Hq][d], dtype of q (bf16: round to nearest even)
  *   out_lse  device f32 [B][Hq] or NULL.
+ * Requires cp * num_splits <= 256.
  * workspace: device scratch of at least cp_decode_workspace_size() bytes, 256-byte aligned,
  * zero-filled before its first use (the call leaves it reusable: its counters return to
  * zero).  Calls that use the same workspace must not overlap on the GPU.
