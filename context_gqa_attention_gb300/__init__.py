@@ -23,7 +23,7 @@ __all__ = [
     "CPError", "load", "lib_path", "CP_F32", "CP_BF16", "CP_PASS_KV", "CP_PASS_Q",
     "CP_IMPL_AUTO", "CP_IMPL_TCGEN05", "CP_IMPL_SIMT", "CP_IMPL_TCGEN05_SINGLE", "cp_partition", "cp_kv_interleave_layout",
     "cp_partial_attn_prefill", "cp_decode_plan", "cp_partial_attn_decode", "cp_lse_merge",
-    "cp_decode_workspace_size", "cp_decode_attention", "STATUS",
+    "cp_decode_workspace_size", "cp_decode_attention", "cp_decode_attention_noalloc", "STATUS",
 ]
 
 CP_F32, CP_BF16 = 0, 1
@@ -93,6 +93,7 @@ _SIGS = [
     ("cp_decode_workspace_size", ctypes.c_int32, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_size_t)]),
     ("cp_decode_attention", ctypes.c_int32, [ctypes.POINTER(DecodeArgs), _vp, ctypes.c_size_t, _vp,
                                              _vp, _vp]),
+    ("cp_decode_attention_noalloc", ctypes.c_int32, [ctypes.POINTER(DecodeArgs), _vp, _vp, _vp]),
 ]
 
 EXPORTED = [s[0] for s in _SIGS]
@@ -360,6 +361,32 @@ def cp_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, cp, interle
                      split_tokens, softmax_scale, None, None, err)
     _check(_LIB.cp_decode_attention(ctypes.byref(a), _ptr(workspace), workspace.numel(), _ptr(out),
                                     _ptr(out_lse), _stream(stream)))
+    return out, out_lse
+
+
+NOALLOC_SCRATCH_BYTES = 48 * 1024 * 1024
+
+
+def cp_decode_attention_noalloc(q, k_cache, v_cache, block_tables, seq_lens, cp, interleave,
+                                out, *, num_splits, split_tokens, softmax_scale=0.0, out_lse=None,
+                                err=None, stream=None):
+    """cp_decode_attention for callers that cannot allocate device memory at call time.
+
+    Scratch comes from a 48 MiB array built into the library (one per GPU, kept until the
+    process exits), so neither this function nor the library allocates: the caller passes
+    `out` ([B, Hq, d], dtype of q) and optionally `out_lse` ([B, Hq] f32), and the split plan
+    explicitly (cp_decode_plan gives one).  Sizes that need more scratch than the array holds
+    raise CPError (CP_ERR_INVALID_ARG).  Calls share the array, so calls that overlap on the GPU
+    race; the first call on a device resolves the array's address and should come before any
+    stream capture.
+    """
+    load()
+    _dev(out, "out", q.dtype)
+    _dev(out_lse, "out_lse", torch.float32)
+    a = _decode_args(q, k_cache, v_cache, block_tables, seq_lens, cp, interleave, num_splits,
+                     split_tokens, softmax_scale, None, None, err)
+    _check(_LIB.cp_decode_attention_noalloc(ctypes.byref(a), _ptr(out), _ptr(out_lse),
+                                            _stream(stream)))
     return out, out_lse
 
 

@@ -540,3 +540,24 @@ static cp_status check_decode_args(const cp_decode_args* a, bool need_partials) 
 
 }  // extern "C"
 
+// ------------------------------------------------------------------ helpers for other units
+cp_status cp_check_decode_args_for_fused(const cp_decode_args* a, const void* out) {
+  const cp_status st = check_decode_args(a, false);
+  if (st != CP_OK) return st;
+  REQUIRE_PTR(out);
+  if ((long long)a->cp * a->num_splits > 256)
+    return fail(CP_ERR_UNSUPPORTED, "cp * num_splits must be <= 256 for the fused decode (got %d)",
+                a->cp * a->num_splits);
+  return CP_OK;
+}
+
+cp_status cp_fail_detail(cp_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  g_status = st;
+  return st;
+}
+
+cp_status cp_launch_status(cudaError_t e, const char* what) { return launched(e, what); }

@@ -107,3 +107,8 @@ inline size_t cp_decode_ws_layout(int B, int Hq, int Hkv, int d, int P, size_t* 
 }
 cudaError_t cp_launch_decode_fused(const cp_decode_args& a, float scale, const CpDecodeWorkspace& ws,
                                    void* out, float* out_lse, cudaStream_t s);
+
+// Host helpers exported by api.cu for entry points defined in other translation units.
+cp_status cp_check_decode_args_for_fused(const cp_decode_args* a, const void* out);
+cp_status cp_fail_detail(cp_status st, const char* fmt, ...);
+cp_status cp_launch_status(cudaError_t e, const char* what);

@@ -275,6 +275,29 @@ cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32
                        int64_t rows, int32_t num_heads, int32_t head_dim, void* out,
                        int32_t out_dtype, float* out_lse, void* stream);
 
+/* ------------------------------------------------------------------------------
+ * cp_decode_attention_noalloc -- cp_decode_attention for callers that cannot allocate
+ * device memory when they call (no counterpart on the pages: it exists for this library's
+ * users).
+ *
+ * Some callers have no device memory to give: a host framework that owns the whole GPU
+ * memory pool and hands out none after start-up, or a fixed-footprint serving process that
+ * must not allocate per request.  This entry point takes the same arguments as
+ * cp_decode_attention minus the workspace and uses instead a scratch array built into the
+ * library (CP_NOALLOC_SCRATCH_BYTES = 48 MiB per GPU, present on every GPU that loads the
+ * library until the process exits).  It allocates and frees nothing.
+ *   - Sizes whose scratch (cp_decode_workspace_size) exceeds CP_NOALLOC_SCRATCH_BYTES are
+ *     rejected with CP_ERR_INVALID_ARG and a message naming both sizes.
+ *   - The first call on a device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array: calls that overlap on the GPU (other streams, other
+ *     threads) race and must be serialised by the caller.  Each call clears the array's
+ *     arrival counters on `stream` before its launch.
+ * ---------------------------------------------------------------------------- */
+#define CP_NOALLOC_SCRATCH_BYTES (48u * 1024u * 1024u)
+cp_status cp_decode_attention_noalloc(const cp_decode_args* args, void* out, float* out_lse,
+                                      void* stream);
+
 /* sizeof() of the argument structs, so bindings can check their mirror. */
 size_t cp_prefill_args_size(void);
 size_t cp_decode_args_size(void);
