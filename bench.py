@@ -220,6 +220,66 @@ def prefill_config(w):
             "head_dim": w.head_dim, "mode": "pass_kv"}
 
 
+class PassQRunner:
+    """chunked prefill (pass-Q): partition of the new tokens -> round-robin layout of the kv
+    -> pass-Q partial attention over the paged cache -> merge."""
+
+    def __init__(self, w, dev, cpa):
+        self.w, self.dev, self.cpa = w, dev, cpa
+        x = wl.workload_inputs(w)
+        self.q = x["q"].to(dev)
+        self.kc = x["k_cache"].to(dev)
+        self.vc = x["v_cache"].to(dev)
+        self.tables = x["block_tables"].to(dev)
+        self.seq_lens = x["seq_lens"].to(dev)
+        self.cu_q = x["cu_seqlens_q"].to(dev)
+        cu = [0]
+        for L in x["seq_lens"].tolist():
+            cu.append(cu[-1] + L)
+        self.cu_kv = torch.tensor(cu, dtype=torch.int32, device=dev)
+        self.N = w.num_seqs * w.q_len
+        cp, Hq, d = w.cp, w.num_q_heads, w.head_dim
+        self.part = torch.empty(cp, self.N, Hq, d, dtype=torch.float32, device=dev)
+        self.plse = torch.empty(cp, self.N, Hq, dtype=torch.float32, device=dev)
+        self.out = torch.empty(self.N, Hq, d, dtype=w.dtype, device=dev)
+        self.local_lens = torch.empty(cp, w.num_seqs, dtype=torch.int32, device=dev)
+        self.perm = torch.empty(self.N, dtype=torch.int32, device=dev)
+        self.inv = torch.empty(self.N, dtype=torch.int32, device=dev)
+        self.so = torch.empty(cp + 1, dtype=torch.int32, device=dev)
+        self.cb = torch.empty(w.num_seqs, 2 * cp + 1, dtype=torch.int32, device=dev)
+        ctx = w.kv_len - w.q_len
+        pairs = sum(ctx + i + 1 for i in range(w.q_len)) * w.num_seqs
+        self.flops = 4.0 * d * Hq * pairs
+        self.launches_per_step = 4
+        self.impl = cpa.CP_IMPL_AUTO
+
+    def step(self, ev=None):
+        cpa, w = self.cpa, self.w
+        cpa.cp_partition(self.cu_q, w.cp, self.N, self.perm, self.inv, self.so, self.cb)
+        cpa.cp_kv_interleave_layout(self.cu_kv, w.cp, w.interleave, 0, w.block_size,
+                                    local_lens=self.local_lens, want_slots=False)
+        if ev is not None:
+            ev[0].record()
+        cpa.cp_partial_attn_prefill(self.q, self.cu_q, w.cp, mode=cpa.CP_PASS_Q, k_cache=self.kc,
+                                    v_cache=self.vc, block_tables=self.tables,
+                                    seq_lens_kv=self.seq_lens, interleave=w.interleave,
+                                    max_seqlen_q=w.q_len, out=self.part, lse=self.plse,
+                                    impl=self.impl)
+        if ev is not None:
+            ev[1].record()
+        cpa.cp_lse_merge(self.part, self.plse, out=self.out, want_lse=False)
+
+    def metric(self, seconds):
+        return self.flops / seconds / 1e12
+
+    def config(self):
+        w = self.w
+        return {"workload": f"chunked prefill pass-Q: {w.num_seqs} seqs x {w.q_len} new of "
+                            f"{w.kv_len} kv, {w.num_q_heads}/{w.num_kv_heads} heads, d={w.head_dim}, "
+                            f"paged bs={w.block_size}, cp={w.cp}, I={w.interleave}",
+                "mode": "pass_q"}
+
+
 class DecodeRunner:
     """decode: interleave layout -> per-rank split partials -> merge."""
 
@@ -247,7 +307,7 @@ class DecodeRunner:
         self.part = torch.empty(P, w.num_seqs, Hq, d, dtype=torch.float32, device=dev)
         self.plse = torch.empty(P, w.num_seqs, Hq, dtype=torch.float32, device=dev)
         self.out = torch.empty(w.num_seqs, Hq, d, dtype=w.dtype, device=dev)
-        self.fused = True
+        self.fused = False  # two launches measured faster than the fused one
         self.ws = torch.zeros(cpa.cp_decode_workspace_size(w.num_seqs, Hq, Hkv, d, cp, self.ns),
                               dtype=torch.uint8, device=dev)
         self.local_lens = torch.empty(cp, w.num_seqs, dtype=torch.int32, device=dev)
@@ -427,14 +487,14 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="full", choices=["full", "long", "tiny", "decode"])
+    ap.add_argument("--workload", default="full", choices=["full", "long", "tiny", "chunked", "decode"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--prefill-impl", default="auto", choices=["auto", "tcgen05", "simt"])
-    ap.add_argument("--decode-unfused", action="store_true",
-                    help="decode as two launches (partials, then cp_lse_merge)")
+    ap.add_argument("--decode-fused", action="store_true",
+                    help="decode as one launch (cp_decode_attention) instead of partials + merge")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's number of sequences (smaller profiling cases)")
     args = ap.parse_args()
@@ -453,9 +513,10 @@ def main():
     w = wl.WORKLOADS[args.workload]
     if args.batch > 0:
         w = dataclasses.replace(w, num_seqs=args.batch)
-    runner = DecodeRunner(w, dev, cpa) if w.kind == "decode" else PrefillRunner(w, dev, cpa)
+    runner = (DecodeRunner(w, dev, cpa) if w.kind == "decode" else
+              PassQRunner(w, dev, cpa) if w.kind == "pass_q" else PrefillRunner(w, dev, cpa))
     if isinstance(runner, DecodeRunner):
-        runner.fused = not args.decode_unfused
+        runner.fused = args.decode_fused
     runner.impl = {"auto": cpa.CP_IMPL_AUTO, "tcgen05": cpa.CP_IMPL_TCGEN05,
                    "simt": cpa.CP_IMPL_SIMT}[args.prefill_impl]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -477,7 +538,17 @@ def main():
     dom_s = statistics.mean(dom_ms) / 1e3
 
     # end to end: host buffers, copies inside the timed region
-    if isinstance(runner, PrefillRunner):
+    if isinstance(runner, PassQRunner):
+        e2e = None
+        peak, src = pk["bf16"]
+        achieved = runner.flops / dom_s / 1e12
+        roof = {"bound": "tensor", "kernel": "cp_partial_attn_prefill (pass-Q, paged)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{src} bf16 dense (burst)", "traffic": None,
+                "algorithmic": f"{runner.flops:.4e} causal FLOP per launch", "launch_ms": dom_s * 1e3}
+        metric = "causal GQA chunked-prefill TFLOP/s (pass-Q partial attention + LSE merge)"
+        unit = "TFLOP/s"
+    elif isinstance(runner, PrefillRunner):
         for _ in range(3):
             runner.e2e_step()
         torch.cuda.synchronize(dev)

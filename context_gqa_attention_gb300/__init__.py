@@ -23,7 +23,8 @@ __all__ = [
     "CPError", "load", "lib_path", "CP_F32", "CP_BF16", "CP_PASS_KV", "CP_PASS_Q",
     "CP_IMPL_AUTO", "CP_IMPL_TCGEN05", "CP_IMPL_SIMT", "CP_IMPL_TCGEN05_SINGLE", "cp_partition", "cp_kv_interleave_layout",
     "cp_partial_attn_prefill", "cp_decode_plan", "cp_partial_attn_decode", "cp_lse_merge",
-    "cp_decode_workspace_size", "cp_decode_attention", "cp_decode_attention_noalloc", "STATUS",
+    "cp_decode_workspace_size", "cp_decode_attention", "cp_decode_attention_noalloc",
+    "cp_kv_cache_write", "STATUS",
 ]
 
 CP_F32, CP_BF16 = 0, 1
@@ -85,6 +86,8 @@ _SIGS = [
                                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                  _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp,
                                                  _vp]),
+    ("cp_kv_cache_write", ctypes.c_int32, [_vp, _vp, _vp, _vp] + [ctypes.c_int32] * 8 +
+     [_vp, ctypes.c_int32, ctypes.c_int64, _vp, _vp, _vp, _vp]),
     ("cp_partial_attn_prefill", ctypes.c_int32, [ctypes.POINTER(PrefillArgs), _vp]),
     ("cp_decode_plan", ctypes.c_int32, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_int32)] * 2),
     ("cp_partial_attn_decode", ctypes.c_int32, [ctypes.POINTER(DecodeArgs), _vp]),
@@ -209,6 +212,24 @@ def cp_kv_interleave_layout(cu_seq_lens, cp, interleave, total_tokens, block_siz
         max_blocks, _ptr(local_lens), _ptr(rank_of_token), _ptr(local_of_token),
         _ptr(slot_of_token), _ptr(err), _stream(stream)))
     return local_lens, rank_of_token, local_of_token, slot_of_token
+
+
+def cp_kv_cache_write(k_new, v_new, cu_new, start_pos, k_cache, v_cache, block_tables, cp,
+                      interleave, err=None, stream=None):
+    """Store new K/V rows [N, Hkv, d] into the per-rank pools [cp, pool, Hkv, bs, d] at their
+    round-robin slots (see cpattn.h)."""
+    load()
+    N, Hkv, d = k_new.shape
+    B = cu_new.numel() - 1
+    for n, t, dt in (("k_new", k_new, None), ("v_new", v_new, k_new.dtype),
+                     ("cu_new", cu_new, torch.int32), ("start_pos", start_pos, torch.int32),
+                     ("k_cache", k_cache, k_new.dtype), ("v_cache", v_cache, k_new.dtype),
+                     ("block_tables", block_tables, torch.int32)):
+        _dev(t, n, dt)
+    _check(_LIB.cp_kv_cache_write(_ptr(k_new), _ptr(v_new), _ptr(cu_new), _ptr(start_pos), B, N,
+                                  Hkv, d, _cp_dtype(k_new), cp, interleave, k_cache.shape[3],
+                                  _ptr(block_tables), block_tables.shape[-1], k_cache.shape[1],
+                                  _ptr(k_cache), _ptr(v_cache), _ptr(err), _stream(stream)))
 
 
 def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=None,

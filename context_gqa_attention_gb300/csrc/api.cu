@@ -137,6 +137,34 @@ __global__ void interleave_kernel(const int32_t* __restrict__ cu, int B, int N, 
   }
 }
 
+// ---- cp_kv_cache_write: one thread per 16-byte vector of a new token's K and V rows.
+__global__ void kv_write_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                const int32_t* __restrict__ cu, const int32_t* __restrict__ start,
+                                int B, int N, int Hkv, int vecs, int cp, int I, int bs,
+                                const int32_t* __restrict__ tables, int max_blocks,
+                                long long pool, uint4* k_cache, uint4* v_cache, int32_t* err) {
+  const long long total = (long long)N * Hkv * vecs;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int vec = (int)(i % vecs);
+    const int g = (int)((i / vecs) % Hkv);
+    const int t = (int)(i / ((long long)vecs * Hkv));
+    const int b = seq_of_row(cu, B, t);
+    const long long pos = (long long)start[b] + (t - cu[b]);
+    const int r = (int)((pos / I) % cp);
+    const long long l = (pos / ((long long)I * cp)) * I + pos % I;
+    const long long col = l / bs;
+    const int page = col < max_blocks ? tables[((long long)r * B + b) * max_blocks + col] : -1;
+    if (page < 0 || page >= pool) {
+      report(err, CP_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    const long long dst = ((((long long)r * pool + page) * Hkv + g) * bs + l % bs) * vecs + vec;
+    k_cache[dst] = k_new[i];
+    v_cache[dst] = v_new[i];
+  }
+}
+
 // ---- cp_lse_merge: one warp per (row, head); lanes own D/32 consecutive floats.
 template <int D>
 struct MergeVec;
@@ -353,6 +381,35 @@ cp_status cp_kv_interleave_layout(const int32_t* cu_seq_lens, int32_t num_seqs,
       cu_seq_lens, num_seqs, total_tokens, cp, interleave, block_size, block_tables, max_blocks,
       local_lens, rank_of_token, local_of_token, slot_of_token, err);
   return launched(cudaGetLastError(), "cp_kv_interleave_layout launch");
+}
+
+cp_status cp_kv_cache_write(const void* k_new, const void* v_new, const int32_t* cu_new,
+                           const int32_t* start_pos, int32_t num_seqs, int32_t total_new,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t dtype, int32_t cp,
+                           int32_t interleave, int32_t block_size, const int32_t* block_tables,
+                           int32_t max_blocks, int64_t pool_pages, void* k_cache, void* v_cache,
+                           int32_t* err, void* stream) {
+  REQUIRE(num_seqs >= 1 && total_new >= 0 && num_kv_heads >= 1, "bad sizes");
+  REQUIRE(dtype == CP_F32 || dtype == CP_BF16, "dtype must be CP_F32 or CP_BF16");
+  REQUIRE(head_dim >= 8 && head_dim % 8 == 0, "head_dim must be a positive multiple of 8");
+  REQUIRE(cp >= 1 && cp <= 64 && interleave >= 1 && block_size >= 1, "bad cp / interleave / block_size");
+  REQUIRE(max_blocks >= 1 && pool_pages >= 1, "max_blocks and pool_pages must be >= 1");
+  REQUIRE(cu_new && start_pos && block_tables, "cu_new, start_pos and block_tables are required");
+  REQUIRE_PTR(k_new);
+  REQUIRE_PTR(v_new);
+  REQUIRE_PTR(k_cache);
+  REQUIRE_PTR(v_cache);
+  if (total_new == 0) return ok();
+  const int esz = dtype == CP_BF16 ? 2 : 4;
+  const int vecs = head_dim * esz / 16;
+  const long long items = (long long)total_new * num_kv_heads * vecs;
+  int blocks = (int)((items + 255) / 256);
+  blocks = blocks > 8 * 1184 ? 8 * 1184 : blocks;
+  cpattn::kv_write_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), cu_new, start_pos, num_seqs,
+      total_new, num_kv_heads, vecs, cp, interleave, block_size, block_tables, max_blocks,
+      pool_pages, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), err);
+  return launched(cudaGetLastError(), "cp_kv_cache_write launch");
 }
 
 cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32_t num_partials,

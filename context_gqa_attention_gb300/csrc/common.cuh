@@ -87,6 +87,11 @@ cudaError_t cp_launch_prefill_simt(const cp_prefill_args& a, float scale, cudaSt
 cudaError_t cp_launch_prefill_tc(const cp_prefill_args& a, float scale, cudaStream_t s);
 bool cp_prefill_tc_supported(const cp_prefill_args& a);
 cudaError_t cp_launch_decode(const cp_decode_args& a, float scale, cudaStream_t s);
+// 2D bf16 TMA descriptor (CUtensorMap, 64-byte aligned storage of 128 bytes) over `rows` rows
+// of `cols` elements, box of 64 columns x box_rows rows, 128-byte swizzle, zero fill.
+bool cp_make_bf16_map_2d(void* map, const void* base, unsigned long long cols,
+                         unsigned long long rows, unsigned long long pitch_elems,
+                         unsigned box_rows);
 
 // Scratch of the fused decode: arrival counters [B][Hkv] (zero between calls), partial LSEs
 // [cp*S][B][Hq] and partial outputs [cp*S][B][Hq][d], each region 256-byte aligned.

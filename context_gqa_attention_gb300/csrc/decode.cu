@@ -13,7 +13,10 @@
 
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace cpattn {
 namespace {
@@ -338,6 +341,313 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_kernel(const DecodePara
 
 }
 
+// ------------------------------------------------------------------------------ tensor-core decode
+// bf16 decode with the kv bytes moved by TMA and the arithmetic on tensor cores.  Per CTA:
+// 4 consumer warps and 1 producer warp, two CTAs per SM.  The producer streams every page's K and V rows of one
+// kv head (16 tokens x d, two 2D TMA boxes of 64 columns each, 128-byte swizzle) into a
+// 3-stage ring per consumer warp.  A consumer computes, for its page,
+//   S = Q K^T   with mma.sync m16n8k16: A = the G query heads (rows >= G are zero) kept in
+//               registers for the whole CTA, B = K from shared memory via ldmatrix;
+//   P           online softmax per head, in the fragment the MMA left it in (a row = a head,
+//               so the 16 tokens of a head live in the 4 lanes of a quad: two shuffles);
+//   O += P V    A = P (that same fragment, rounded to bf16), B = V via ldmatrix.trans.
+// The swizzled layout makes every ldmatrix phase touch 8 distinct bank groups.
+constexpr int kCW = 4;  // consumer warps (two CTAs share an SM)
+constexpr int kST = 3;  // ring stages per consumer warp
+constexpr long long kDecodeBudget = 4000000000ll;  // SM cycles per wait (~2 s)
+
+template <int D>
+struct MLayout {
+  static constexpr int kPageBytes = kPage * D * 2;  // one head's K (or V) rows of a page
+  static constexpr int kStage = 2 * kPageBytes;
+  static constexpr int oRing = 0;
+  static constexpr int kRing = kCW * kST * kStage;
+  static constexpr int oM = kRing;                  // m [kCW][8]
+  static constexpr int oL = oM + kCW * 8 * 4;       // l [kCW][8]
+  static constexpr int oBar = oL + kCW * 8 * 4;
+  static constexpr int nBar = 2 * kCW * kST;        // full, empty
+  static constexpr int oFlag = oBar + nBar * 8;     // page valid [kCW][kST], abort
+  static constexpr int kBytes = oFlag + (kCW * kST + 1) * 4;
+  static constexpr int kAlloc = kBytes + 1024;      // base rounded up to the 1 KB swizzle atom
+  static_assert(kCW * 8 * D * 4 <= kRing, "warp partials reuse the ring");
+  static_assert(kAlloc + 8 * 1024 + 64 <= 232448, "shared memory (incl. the fused merge) per CTA");
+};
+
+CP_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+CP_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+// D (16x8 f32) += A (16x16 bf16, rows gid / gid+8) * B (16x8 bf16); a1 = a3 = 0 (rows 8-15 unused)
+CP_DEV void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+// Byte address of the 16-byte chunk holding (token t, dim d) in a 128B-swizzled page half-box.
+CP_DEV uint32_t page_addr(uint32_t base, int t, int d) {
+  return base + (uint32_t)((d >> 6) * (kPage * 128) + t * 128 + ((((d & 63) >> 3) ^ (t & 7)) << 4));
+}
+
+template <int D, int G, bool FUSED>
+__global__ void __launch_bounds__((kCW + 1) * 32, 2)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_v, const DecodeParams p) {
+  using T = __nv_bfloat16;
+  using Ly = MLayout<D>;
+  constexpr int KB = D / 64;  // 64-column boxes per page row
+  static_assert(G <= 8, "query heads per kv head");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = sm100::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sb = smem_raw + (base - raw);
+  float* m_w = reinterpret_cast<float*>(sb + Ly::oM);
+  float* l_w = reinterpret_cast<float*>(sb + Ly::oL);
+  volatile int* flags = reinterpret_cast<volatile int*>(sb + Ly::oFlag);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sb + Ly::oFlag + kCW * kST * 4);
+  auto full = [&](int w, int s) -> uint32_t { return base + Ly::oBar + 8u * (uint32_t)(w * kST + s); };
+  auto empty = [&](int w, int s) -> uint32_t {
+    return base + Ly::oBar + 8u * (uint32_t)(kCW * kST + w * kST + s);
+  };
+  auto slot = [&](int w, int s) -> uint32_t { return base + Ly::oRing + (uint32_t)((w * kST + s) * Ly::kStage); };
+
+  const int split = blockIdx.x, g = blockIdx.y;
+  const int r = blockIdx.z % p.cp, b = blockIdx.z / p.cp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int L = __ldg(p.seq_lens + b);
+  const int n = rank_local_len(L, r, p.cp, p.I);
+  const int l0 = split * p.ST;
+  const int l1 = min(n, l0 + p.ST);
+  const int part = r * p.S + split;
+  const long long obase = ((long long)part * p.B + b) * p.Hq + (long long)g * G;
+  if (l0 >= l1) {
+    if (threadIdx.x < G) p.lse[obase + threadIdx.x] = -INFINITY;
+    if constexpr (FUSED) fused_tail<T, D, G>(p, b, g);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kCW; ++w)
+      for (int s = 0; s < kST; ++s) {
+        sm100::mbar_init(full(w, s), 1);
+        sm100::mbar_init(empty(w, s), 1);
+      }
+    *abort_flag = 0u;
+    sm100::fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int pg0 = l0 / kPage, pg1 = (l1 + kPage - 1) / kPage;
+  const int npages = pg1 - pg0;
+  const int32_t* trow = p.tables + ((long long)r * p.B + b) * p.max_blocks;
+
+  if (warp == kCW) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      sm100::tma_prefetch_desc(&map_k);
+      sm100::tma_prefetch_desc(&map_v);
+    }
+    int issued = 0;
+    bool ok = true;
+    for (int j0 = 0; ok && j0 < npages; j0 += 32) {
+      const int cnt = min(32, npages - j0);
+      int my_id = -1;
+      if (lane < cnt) {
+        const int pg = pg0 + j0 + lane;
+        my_id = pg < p.max_blocks ? __ldg(trow + pg) : -1;
+        if (my_id >= p.pool) my_id = -1;
+      }
+      for (int i = 0; i < cnt; ++i) {
+        const int id = __shfl_sync(0xffffffffu, my_id, i);
+        int good = 1;
+        if (lane == 0) {
+          const int j = j0 + i, w = j % kCW, k = j / kCW, st = k % kST;
+          const uint32_t ph = (uint32_t)(k / kST) & 1u;
+          if (!sm100::mbar_wait(empty(w, st), ph ^ 1u, abort_flag, kDecodeBudget)) {
+            good = 0;
+          } else {
+            flags[w * kST + st] = id >= 0;
+            if (id >= 0) {
+              const int y = (int)((((long long)r * p.pool + id) * p.Hkv + g) * kPage);
+              const uint32_t ks = slot(w, st);
+              sm100::mbar_expect_tx(full(w, st), 2 * Ly::kPageBytes);
+#pragma unroll
+              for (int kb = 0; kb < KB; ++kb) {
+                sm100::tma_load_2d(ks + kb * (kPage * 128), &map_k, kb * 64, y, full(w, st));
+                sm100::tma_load_2d(ks + Ly::kPageBytes + kb * (kPage * 128), &map_v, kb * 64, y,
+                                   full(w, st));
+              }
+            } else {
+              sm100::mbar_arrive(full(w, st));  // the consumer sees flag 0 and skips the page
+            }
+            issued = j + 1;
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (lane == 0) {
+      if (!ok) {
+        *abort_flag = 1u;
+        report(p.err, CP_ERR_TIMEOUT);
+      }
+      // drain: every copy issued into this CTA's shared memory has landed before it exits
+      for (int j = max(0, issued - kCW * kST); j < issued; ++j) {
+        const int w = j % kCW, k = j / kCW;
+        sm100::mbar_wait(full(w, k % kST), (uint32_t)(k / kST) & 1u, nullptr, kDecodeBudget);
+      }
+    }
+  }
+
+  const int gid = lane >> 2, tid = lane & 3;  // MMA fragment row (head) and column pair
+  float o[D / 8][4];
+  float m = -INFINITY, l = 0.f;
+#pragma unroll
+  for (int nb = 0; nb < D / 8; ++nb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[nb][e] = 0.f;
+  if (warp < kCW) {
+    // ------------------------------------------------------------------ consumers
+    // Q rows as MMA A fragments (bf16 pairs straight from memory; rows >= G are zero)
+    uint32_t qa0[D / 16], qa2[D / 16];
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        static_cast<const T*>(p.q) + ((long long)b * p.Hq + (long long)g * G + gid) * D);
+#pragma unroll
+    for (int ds = 0; ds < D / 16; ++ds) {
+      qa0[ds] = gid < G ? __ldg(qrow + ds * 8 + tid) : 0u;
+      qa2[ds] = gid < G ? __ldg(qrow + ds * 8 + 4 + tid) : 0u;
+    }
+    const float sc = p.scale_log2;
+    const int li = lane >> 3, lj = lane & 7;  // ldmatrix: matrix and row this lane addresses
+    const int nmine = npages > warp ? (npages - warp + kCW - 1) / kCW : 0;
+    for (int k = 0; k < nmine; ++k) {
+      const int st = k % kST;
+      const bool ok = __all_sync(0xffffffffu, sm100::mbar_wait(full(warp, st), (uint32_t)(k / kST) & 1u,
+                                                               abort_flag, kDecodeBudget));
+      if (!ok) {
+        if (lane == 0) {
+          *abort_flag = 1u;
+          report(p.err, CP_ERR_TIMEOUT);
+        }
+        break;
+      }
+      const int pg = pg0 + warp + k * kCW;
+      if (flags[warp * kST + st]) {
+        const uint32_t kp = slot(warp, st), vp = kp + Ly::kPageBytes;
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 0-7, 8-15
+#pragma unroll
+        for (int ds = 0; ds < D / 16; ++ds) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(page_addr(kp, ((li >> 1) << 3) + lj, ds * 16 + ((li & 1) << 3)), b0, b1, b2, b3);
+          mma16816(s0, qa0[ds], qa2[ds], b0, b1);
+          mma16816(s1, qa0[ds], qa2[ds], b2, b3);
+        }
+        // head gid, tokens 2tid, 2tid+1, 8+2tid, 9+2tid of this page
+        const int t0 = pg * kPage + 2 * tid;
+        float x0 = t0 < l1 ? s0[0] * sc : -INFINITY;
+        float x1 = t0 + 1 < l1 ? s0[1] * sc : -INFINITY;
+        float x2 = t0 + 8 < l1 ? s1[0] * sc : -INFINITY;
+        float x3 = t0 + 9 < l1 ? s1[1] * sc : -INFINITY;
+        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m, mx);
+        const float corr = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
+        const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - m_new);
+        const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - m_new);
+        const float p2 = x2 == -INFINITY ? 0.f : exp2f(x2 - m_new);
+        const float p3 = x3 == -INFINITY ? 0.f : exp2f(x3 - m_new);
+        float ps = (p0 + p1) + (p2 + p3);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        l = l * corr + ps;
+        m = m_new;
+        __nv_bfloat162 pa = __floats2bfloat162_rn(p0, p1), pb = __floats2bfloat162_rn(p2, p3);
+        const uint32_t pa0 = *reinterpret_cast<uint32_t*>(&pa), pa2 = *reinterpret_cast<uint32_t*>(&pb);
+#pragma unroll
+        for (int nb = 0; nb < D / 8; ++nb) {
+          o[nb][0] *= corr;
+          o[nb][1] *= corr;
+        }
+#pragma unroll
+        for (int nb = 0; nb < D / 16; ++nb) {
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_t(page_addr(vp, ((li & 1) << 3) + lj, nb * 16 + ((li >> 1) << 3)), v0, v1, v2, v3);
+          mma16816(o[2 * nb], pa0, pa2, v0, v1);
+          mma16816(o[2 * nb + 1], pa0, pa2, v2, v3);
+        }
+      } else if (lane == 0) {
+        report(p.err, CP_ERR_DEVICE_BOUNDS);
+      }
+      __syncwarp();
+      if (lane == 0) sm100::mbar_arrive(empty(warp, st));
+    }
+  }
+  __syncthreads();  // all pages consumed and all copies landed: the ring is free
+
+  // warps -> one partial for the CTA (o_w reuses the ring)
+  float* o_w = reinterpret_cast<float*>(sb + Ly::oRing);
+  if (warp < kCW && gid < G) {
+    if (tid == 0) {
+      m_w[warp * 8 + gid] = m;
+      l_w[warp * 8 + gid] = l;
+    }
+#pragma unroll
+    for (int nb = 0; nb < D / 8; ++nb) {
+      o_w[(warp * G + gid) * D + nb * 8 + 2 * tid] = o[nb][0];
+      o_w[(warp * G + gid) * D + nb * 8 + 2 * tid + 1] = o[nb][1];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    const int hh = i / D, dd = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) M = fmaxf(M, m_w[w * 8 + hh]);
+    float Ls = 0.f, Os = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) {
+      const float mw = m_w[w * 8 + hh];
+      const float e = mw > -INFINITY ? exp2f(mw - M) : 0.f;
+      Ls += e * l_w[w * 8 + hh];
+      Os += e * o_w[(w * G + hh) * D + dd];
+    }
+    if (Ls > 0.f) {
+      p.out[(obase + hh) * D + dd] = Os / Ls;
+      if (dd == 0) p.lse[obase + hh] = (M + log2f(Ls)) * kLn2;
+    } else if (dd == 0) {
+      p.lse[obase + hh] = -INFINITY;
+    }
+  }
+  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g);
+}
+
+template <int D, bool F>
+cudaError_t launch_mma_g(const DecodeParams& p, int G, dim3 grid, const CUtensorMap& mk,
+                         const CUtensorMap& mv, cudaStream_t s) {
+  auto go = [&](auto kern) -> cudaError_t {
+    const int smem = MLayout<D>::kAlloc;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, (kCW + 1) * 32, smem, s>>>(mk, mv, p);
+    return cudaGetLastError();
+  };
+  switch (G) {
+    case 1: return go(decode_mma_kernel<D, 1, F>);
+    case 2: return go(decode_mma_kernel<D, 2, F>);
+    case 4: return go(decode_mma_kernel<D, 4, F>);
+    case 8: return go(decode_mma_kernel<D, 8, F>);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <typename T, int D, bool F>
 cudaError_t launch_g(const DecodeParams& p, int G, dim3 grid, cudaStream_t s) {
   switch (G) {
@@ -353,9 +663,15 @@ cudaError_t launch_g(const DecodeParams& p, int G, dim3 grid, cudaStream_t s) {
 template <bool F>
 cudaError_t launch_all(const DecodeParams& p, const cp_decode_args& a, dim3 grid, cudaStream_t s) {
   const int G = a.num_q_heads / a.num_kv_heads;
-  if (a.dtype == CP_BF16)
-    return a.head_dim == 64 ? launch_g<__nv_bfloat16, 64, F>(p, G, grid, s)
-                            : launch_g<__nv_bfloat16, 128, F>(p, G, grid, s);
+  if (a.dtype == CP_BF16) {  // tensor-core kernel with TMA-staged pages
+    CUtensorMap mk, mv;
+    const unsigned long long rows = (unsigned long long)a.cp * a.pool_pages * a.num_kv_heads * kPage;
+    if (!cp_make_bf16_map_2d(&mk, a.k_cache, a.head_dim, rows, a.head_dim, kPage) ||
+        !cp_make_bf16_map_2d(&mv, a.v_cache, a.head_dim, rows, a.head_dim, kPage))
+      return cudaErrorInvalidValue;
+    return a.head_dim == 64 ? launch_mma_g<64, F>(p, G, grid, mk, mv, s)
+                            : launch_mma_g<128, F>(p, G, grid, mk, mv, s);
+  }
   return a.head_dim == 64 ? launch_g<float, 64, F>(p, G, grid, s) : launch_g<float, 128, F>(p, G, grid, s);
 }
 

@@ -65,6 +65,7 @@ struct Layout {
   // +1 KB so the base can be rounded up to the 1 KB swizzle-atom alignment; never below
   // 120 KB so that a single CTA (and its 512 TMEM columns) occupies an SM.
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+  static_assert(kAlloc <= 232448, "dynamic shared memory beyond the 227 KB per-CTA limit");
 };
 
 struct Work {
@@ -669,6 +670,7 @@ struct Layout2 {
   static constexpr int oMisc = oBar + nBar * 8;
   static constexpr int kBytes = oMisc + 16;
   static constexpr int kAlloc = (kBytes + 1024) > 120 * 1024 ? (kBytes + 1024) : 120 * 1024;
+  static_assert(kAlloc <= 232448, "dynamic shared memory beyond the 227 KB per-CTA limit");
 };
 
 template <int D, bool PT>
@@ -934,7 +936,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     } else {
       fail_timeout(abort_flag, p.err);
     }
-  }
+    }
 
   tc_fence_before();
   __syncthreads();
@@ -1042,6 +1044,12 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s) {
 
 }  // namespace
 }  // namespace cpattn
+
+bool cp_make_bf16_map_2d(void* map, const void* base, unsigned long long cols,
+                         unsigned long long rows, unsigned long long pitch_elems,
+                         unsigned box_rows) {
+  return cpattn::make_map(static_cast<CUtensorMap*>(map), base, cols, rows, pitch_elems, box_rows);
+}
 
 bool cp_prefill_tc_supported(const cp_prefill_args& a) {
   if (a.dtype != CP_BF16) return false;

@@ -75,6 +75,15 @@ SM100_DEV void tma_load_2d(uint32_t dst, const void* map, int x, int y, uint32_t
       : "memory");
 }
 
+// 1D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16) completing on an
+// mbarrier.
+SM100_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // ------------------------------------------------------------------------------ TMEM
 SM100_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

@@ -131,6 +131,28 @@ cp_status cp_kv_interleave_layout(const int32_t* cu_seq_lens, int32_t num_seqs,
                                   void* stream);
 
 /* ------------------------------------------------------------------------------
+ * cp_kv_cache_write -- store new tokens' K/V into the per-rank paged pools at their
+ * round-robin slots ([PKV] Purpose: KV kept round-robin on the CP ranks; [PCP] Purpose:
+ * per-rank block tables; [PCP] code-review summary: one interleave size for PCP and DCP).
+ *
+ * Sequence b's new rows cu_new[b] .. cu_new[b+1]-1 of k_new / v_new ([N][Hkv][d], token-major)
+ * hold positions start_pos[b], start_pos[b]+1, ...; each row goes to rank
+ * rho = floor(p/I) mod cp, local index l (see cp_kv_interleave_layout), i.e. to
+ * k_cache[rho][block_tables[rho][b][l/block_size]][h][l mod block_size][:] (same for v).
+ *   cu_new, start_pos  device int32 [B+1], [B];  block_tables device int32 [cp][B][max_blocks].
+ *   k_cache, v_cache   device [cp][pool_pages][Hkv][block_size][d] of `dtype`.
+ *   err  device int32 or NULL: CP_ERR_DEVICE_BOUNDS for a row whose table entry is missing
+ *        or outside the pool (that row is not written).
+ * A pure copy: bit-exact.  Rows of different calls that map to the same slot race.
+ * ---------------------------------------------------------------------------- */
+cp_status cp_kv_cache_write(const void* k_new, const void* v_new, const int32_t* cu_new,
+                           const int32_t* start_pos, int32_t num_seqs, int32_t total_new,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t dtype, int32_t cp,
+                           int32_t interleave, int32_t block_size, const int32_t* block_tables,
+                           int32_t max_blocks, int64_t pool_pages, void* k_cache, void* v_cache,
+                           int32_t* err, void* stream);
+
+/* ------------------------------------------------------------------------------
  * cp_partial_attn_prefill -- partial attention for every (Q shard, KV shard) pair
  * ([PKV] Purpose: pass-KV for full prefill, pass-Q for chunked prefill; the
  * exchange itself is logical here, so one launch covers every rotation step).

@@ -25,5 +25,5 @@ reading of the pages (both readings give the same attention output).
 from .cp_oracle import (  # noqa: F401
     chunk_bounds, shard_chunks, partition, interleave_deal, local_lengths, rank_positions,
     slot_mapping, partial_attention, attention, lse_merge, pass_kv_partials, pass_q_partials,
-    decode_partials, gather_rank_kv,
+    decode_partials, gather_rank_kv, kv_cache_write,
 )

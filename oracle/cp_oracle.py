@@ -350,3 +350,31 @@ def decode_partials(q, k_cache, v_cache, block_tables, seq_lens, cp: int, I: int
             O[r, i] = o[0]
             LSE[r, i] = l[0]
     return O, LSE
+
+
+def kv_cache_write(k_new, v_new, cu_new, start_pos, cp: int, I: int, block_size: int,
+                   block_tables, k_cache, v_cache):
+    """Place new tokens' K/V rows into the per-rank head-major page pools (in place).
+
+    "Add utility functions ...", Purpose (decode KV round-robin on the CP ranks) and "[Feature]
+    Prefill Context Parallel (PCP) basic support", Purpose (per-rank block tables): sequence b's
+    new rows cu_new[b]..cu_new[b+1]-1 sit at positions start_pos[b], start_pos[b]+1, ...; each
+    goes to the rank and local index the round-robin deal gives its position, i.e. to page
+    block_tables[rank][b][local // block_size], offset local % block_size.
+    k_new, v_new: [N, Hkv, d]; k_cache, v_cache: [cp, pages, Hkv, block_size, d] (modified).
+    """
+    cu = _i64(cu_new)
+    starts = _i64(start_pos)
+    bt = _i64(block_tables)
+    for b in range(cu.size - 1):
+        n = int(cu[b + 1] - cu[b])
+        if n == 0:
+            continue
+        end = int(starts[b]) + n
+        rank, local = interleave_deal(end, cp, I)
+        for i in range(n):
+            pos = int(starts[b]) + i
+            r, l = int(rank[pos]), int(local[pos])
+            page = int(bt[r, b, l // block_size])
+            k_cache[r, page, :, l % block_size, :] = k_new[int(cu[b]) + i]
+            v_cache[r, page, :, l % block_size, :] = v_new[int(cu[b]) + i]

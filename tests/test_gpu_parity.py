@@ -294,3 +294,42 @@ def test_decode_fused_rejects_small_workspace(lib):
         lib.cp_decode_attention(q, kc, kc, tables, lens, 1, 8, num_splits=1, split_tokens=16,
                                 workspace=ws)
     assert e.value.status == 1 and "workspace" in e.value.detail
+
+
+# ------------------------------------------------------------------------------------ cache write
+
+@pytest.mark.parametrize("dt,d,cp,I", [(torch.bfloat16, 128, 2, 8), (torch.float32, 64, 3, 4),
+                                       (torch.bfloat16, 64, 4, 1)])
+def test_kv_cache_write_bitexact(lib, dt, d, cp, I):
+    """New tokens written at their round-robin slots: every byte of the pools equals the oracle's
+    placement (untouched slots keep their old values)."""
+    g = torch.Generator().manual_seed(77 + cp)
+    Hkv, bs = 4, 16
+    cached = [100, 0, 37]
+    new = [5, 64, 1]
+    caps = [wl.block_capacity(c + n, cp, I, bs) for c, n in zip(cached, new)]
+    tables, pool = wl.shuffled_block_tables(caps, cp, g)
+    kc = wl.normal((cp, pool, Hkv, bs, d), dt, g)
+    vc = wl.normal((cp, pool, Hkv, bs, d), dt, g)
+    kn = wl.normal((sum(new), Hkv, d), dt, g)
+    vn = wl.normal((sum(new), Hkv, d), dt, g)
+    cu = _cu(new)
+    start = torch.tensor(cached, dtype=torch.int32)
+    kd, vd = kc.to(DEV), vc.to(DEV)
+    lib.cp_kv_cache_write(kn.to(DEV), vn.to(DEV), cu.to(DEV), start.to(DEV), kd, vd,
+                          tables.to(DEV), cp, I)
+    kr, vr = kc.clone(), vc.clone()
+    orc.kv_cache_write(kn, vn, cu, start, cp, I, bs, tables, kr, vr)
+    assert torch.equal(kd.cpu(), kr) and torch.equal(vd.cpu(), vr)
+
+
+def test_kv_cache_write_reports_missing_page(lib):
+    tables = torch.full((2, 1, 1), 0, dtype=torch.int32)     # one page: 16 local tokens per rank
+    kc = torch.zeros(2, 1, 1, 16, 64, dtype=torch.bfloat16, device=DEV)
+    kn = torch.ones(40, 1, 64, dtype=torch.bfloat16, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lib.cp_kv_cache_write(kn, kn, _cu([40]).to(DEV), torch.zeros(1, dtype=torch.int32, device=DEV),
+                          kc, kc.clone(), tables.to(DEV), 2, 8, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 5
+    assert int((kc != 0).any(dim=-1).sum().item()) == 32    # 16 slots per rank written

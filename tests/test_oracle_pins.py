@@ -457,7 +457,47 @@ def test_sharded_equals_unsharded():
     pin_pass_q_equals_attention()
 
 
-ALL_PINS = [pin_brute_force, pin_sdpa, pin_closed_forms, pin_softmax_rows, pin_merge,
+def pin_kv_cache_write(seed=8):
+    """Tokens written in several pieces land where a pure-Python deal says (round trip through
+    the gather that the pass-Q and decode flows use gives back the logical rows)."""
+    r = _rng(seed)
+    Hkv, d, bs, cp, I = 2, 4, 4, 3, 2
+    L = [23, 9]
+    caps = [-(-x // bs) + 2 for x in L]
+    pool = sum(caps)
+    tables = np.full((cp, 2, max(caps)), -1, np.int64)
+    for rr in range(cp):
+        perm = r.permutation(pool)
+        off = 0
+        for b, c in enumerate(caps):
+            tables[rr, b, :c] = perm[off:off + c]
+            off += c
+    kc = np.full((cp, pool, Hkv, bs, d), np.nan)
+    vc = np.full((cp, pool, Hkv, bs, d), np.nan)
+    logical = [(r.standard_normal((x, Hkv, d)), r.standard_normal((x, Hkv, d))) for x in L]
+    pieces = [(0, 10, 0, 4), (10, 23, 4, 9)]   # (start, end) per sequence in two writes
+    for (s0, e0, s1, e1) in pieces:
+        kn = np.concatenate([logical[0][0][s0:e0], logical[1][0][s1:e1]])
+        vn = np.concatenate([logical[0][1][s0:e0], logical[1][1][s1:e1]])
+        cu = np.array([0, e0 - s0, e0 - s0 + e1 - s1])
+        orc.kv_cache_write(kn, vn, cu, np.array([s0, s1]), cp, I, bs, tables, kc, vc)
+    for b, x in enumerate(L):
+        br, bl, _ = brute_deal(x, cp, I)
+        for p in range(x):
+            page = tables[br[p], b, bl[p] // bs]
+            assert np.array_equal(kc[br[p], page, :, bl[p] % bs], logical[b][0][p])
+            assert np.array_equal(vc[br[p], page, :, bl[p] % bs], logical[b][1][p])
+        for rr in range(cp):
+            pos = orc.rank_positions(x, rr, cp, I)
+            kg = orc.gather_rank_kv(kc[rr], tables[rr, b], pos.size, bs)
+            assert np.array_equal(kg, logical[b][0][pos])
+
+
+def test_kv_cache_write():
+    pin_kv_cache_write()
+
+
+ALL_PINS = [pin_brute_force, pin_kv_cache_write, pin_sdpa, pin_closed_forms, pin_softmax_rows, pin_merge,
             pin_partition_fixture, pin_partition_invariants, pin_load_balance, pin_interleave,
             pin_computed_tokens_fixture, pin_slot_mapping, pin_pass_kv_equals_attention,
             pin_pass_q_equals_attention]
