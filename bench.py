@@ -43,7 +43,11 @@ NCU_TRAFFIC = {
     "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
                 "sha1": "0111a2b9414ea34c639d21667f38c1984de07853", "bytes": 107174912,
                 "workload": "full"},
-    "decode": None,
+    # profiles/decode_mma_decode.md: a 16-sequence capture (1.1186 GB read + 7.65 MB written),
+    # scaled to the 64-sequence workload by algorithmic bytes (4.3933e9 / 1.1181e9)
+    "decode": {"file": "context_gqa_attention_gb300/csrc/decode.cu",
+               "sha1": "31b32a19d5725c80d520775a67b0090a375c7d0e", "bytes": 4425279389,
+               "workload": "decode"},
 }
 
 FALLBACK_HBM_GBS = 6800.0
@@ -176,13 +180,22 @@ class PrefillRunner:
         self.so = torch.empty(cp + 1, dtype=torch.int32, device=dev)
         self.cb = torch.empty(len(lens), 2 * cp + 1, dtype=torch.int32, device=dev)
         self.flops = 4.0 * d * Hq * causal_pairs_pass_kv(lens)
-        self.launches_per_step = 3
         self.impl = cpa.CP_IMPL_AUTO
+        self.fused = False
         self.out_host = torch.empty(self.out.shape, dtype=w.dtype).pin_memory()
 
     def step(self, ev=None):
         cpa, w = self.cpa, self.w
         cpa.cp_partition(self.cu, w.cp, self.N, self.perm, self.inv, self.so, self.cb)
+        if self.fused:  # every kv shard walked inside one item: final output, no partials
+            if ev is not None:
+                ev[0].record()
+            cpa.cp_attn_prefill_fused(self.q, self.cu, w.cp, self.k, self.v,
+                                      max_seqlen_q=max(self.lens), out=self.out, out_lse=self.olse,
+                                      impl=self.impl)
+            if ev is not None:
+                ev[1].record()
+            return
         if ev is not None:
             ev[0].record()
         cpa.cp_partial_attn_prefill(self.q, self.cu, w.cp, k=self.k, v=self.v,
@@ -191,6 +204,10 @@ class PrefillRunner:
         if ev is not None:
             ev[1].record()
         cpa.cp_lse_merge(self.part, self.plse, out=self.out, out_lse=self.olse)
+
+    @property
+    def launches_per_step(self):
+        return 2 if self.fused else 3
 
     def e2e_step(self):
         """Host buffers in, host result out: the same step with the copies inside."""
@@ -319,6 +336,19 @@ class DecodeRunner:
         self.bytes = (sum(lens) * Hkv * d * 2 * el + 2 * w.num_seqs * Hq * d * el + pages * 4)
         self.kv_bytes = sum(lens) * Hkv * d * 2 * el
         self.pool = pool
+
+    def resplit(self, split_tokens):
+        w = self.w
+        share = self.ns * self.st  # the planned split covers the largest rank share
+        self.st = split_tokens
+        self.ns = -(-share // split_tokens)
+        P = w.cp * self.ns
+        Hq, d = w.num_q_heads, w.head_dim
+        self.part = torch.empty(P, w.num_seqs, Hq, d, dtype=torch.float32, device=self.dev)
+        self.plse = torch.empty(P, w.num_seqs, Hq, dtype=torch.float32, device=self.dev)
+        self.ws = torch.zeros(self.cpa.cp_decode_workspace_size(w.num_seqs, Hq, w.num_kv_heads, d,
+                                                                w.cp, self.ns),
+                              dtype=torch.uint8, device=self.dev)
 
     @property
     def launches_per_step(self):
@@ -493,8 +523,12 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--prefill-impl", default="auto", choices=["auto", "tcgen05", "simt"])
+    ap.add_argument("--prefill-fused", action="store_true",
+                    help="prefill as one launch (cp_attn_prefill_fused) instead of partials + merge")
     ap.add_argument("--decode-fused", action="store_true",
                     help="decode as one launch (cp_decode_attention) instead of partials + merge")
+    ap.add_argument("--decode-split-tokens", type=int, default=0,
+                    help="override the decode plan's rank-local tokens per split (multiple of 16)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's number of sequences (smaller profiling cases)")
     args = ap.parse_args()
@@ -517,6 +551,10 @@ def main():
               PassQRunner(w, dev, cpa) if w.kind == "pass_q" else PrefillRunner(w, dev, cpa))
     if isinstance(runner, DecodeRunner):
         runner.fused = args.decode_fused
+        if args.decode_split_tokens > 0:
+            runner.resplit(args.decode_split_tokens)
+    if isinstance(runner, PrefillRunner) and not isinstance(runner, PassQRunner):
+        runner.fused = args.prefill_fused
     runner.impl = {"auto": cpa.CP_IMPL_AUTO, "tcgen05": cpa.CP_IMPL_TCGEN05,
                    "simt": cpa.CP_IMPL_SIMT}[args.prefill_impl]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -564,13 +602,15 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         peak, src = pk["bf16"]
         achieved = runner.flops / dom_s / 1e12
-        roof = {"bound": "tensor", "kernel": "cp_partial_attn_prefill (pass-KV)",
+        roof = {"bound": "tensor", "kernel": "cp_attn_prefill_fused (pass-KV, merged in-kernel)"
+                if runner.fused else "cp_partial_attn_prefill (pass-KV)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": f"{src} bf16 dense (burst)",
                 "traffic": ncu_traffic("prefill", w.name),
                 "algorithmic": f"{runner.flops:.4e} causal FLOP per launch",
                 "launch_ms": dom_s * 1e3}
-        metric = "causal GQA prefill TFLOP/s (pass-KV partial attention + LSE merge)"
+        metric = ("causal GQA prefill TFLOP/s (pass-KV, shards merged in-kernel)" if runner.fused
+                  else "causal GQA prefill TFLOP/s (pass-KV partial attention + LSE merge)")
         unit = "TFLOP/s"
     else:
         e2e = None
@@ -597,18 +637,39 @@ def main():
         line["e2e"] = e2e
 
     if not args.no_secondary and w.kind != "decode":
-        dr = DecodeRunner(wl.WORKLOADS["decode"], dev, cpa)
-        ds, dd, _ = time_steps(dr, max(10, args.steps // 5), 3, flush, dev, stream)
-        d_s = statistics.mean(dd) / 1e3
+        sec = {}
+        if isinstance(runner, PrefillRunner) and not isinstance(runner, PassQRunner):
+            # the same workload as one launch (cp_attn_prefill_fused): no partial round trip
+            runner.fused = not runner.fused
+            fs, fd, _ = time_steps(runner, max(10, args.steps // 2), 3, flush, dev, stream)
+            f_s = statistics.mean(fd) / 1e3
+            bf, bsrc = pk["bf16"]
+            sec["prefill_fused" if runner.fused else "prefill_partials"] = {
+                "value": runner.metric(statistics.mean(fs) / 1e3), "unit": "TFLOP/s",
+                "roofline": {"bound": "tensor",
+                             "kernel": "cp_attn_prefill_fused" if runner.fused else
+                             "cp_partial_attn_prefill (pass-KV)",
+                             "achieved": runner.flops / f_s / 1e12, "peak": bf, "unit": "TFLOP/s",
+                             "frac": runner.flops / f_s / 1e12 / bf,
+                             "peak_source": f"{bsrc} bf16 dense (burst)", "launch_ms": f_s * 1e3}}
+            runner.fused = not runner.fused
         hbm, hsrc = pk["hbm"]
-        line["secondary"] = {
-            "decode": {"value": dr.metric(statistics.mean(ds) / 1e3), "unit": "GB/s",
-                       "config": dr.config(),
-                       "roofline": {"bound": "hbm", "kernel": "cp_decode_attention (fused)",
-                                    "achieved": dr.bytes / d_s / 1e9, "peak": hbm,
-                                    "unit": "GB/s", "frac": dr.bytes / d_s / 1e9 / hbm,
-                                    "peak_source": f"{hsrc} HBM copy", "launch_ms": d_s * 1e3}}}
-        del dr
+        for fused in (False, True):
+            dr = DecodeRunner(wl.WORKLOADS["decode"], dev, cpa)
+            dr.fused = fused
+            ds, dd, _ = time_steps(dr, max(10, args.steps // 5), 3, flush, dev, stream)
+            d_s = statistics.mean(dd) / 1e3
+            sec["decode_fused" if fused else "decode"] = {
+                "value": dr.metric(statistics.mean(ds) / 1e3), "unit": "GB/s",
+                "config": dr.config(),
+                "roofline": {"bound": "hbm",
+                             "kernel": "cp_decode_attention (partials + merge, one launch)" if fused
+                             else "cp_partial_attn_decode (+ cp_lse_merge)",
+                             "achieved": dr.bytes / d_s / 1e9, "peak": hbm,
+                             "unit": "GB/s", "frac": dr.bytes / d_s / 1e9 / hbm,
+                             "peak_source": f"{hsrc} HBM copy", "launch_ms": d_s * 1e3}}
+            del dr
+        line["secondary"] = sec
 
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and w.kind == "pass_kv":
         f, t, n = oracle_sample(w, args.cpu_rows, 777)

@@ -24,7 +24,7 @@ __all__ = [
     "CP_IMPL_AUTO", "CP_IMPL_TCGEN05", "CP_IMPL_SIMT", "CP_IMPL_TCGEN05_SINGLE", "cp_partition", "cp_kv_interleave_layout",
     "cp_partial_attn_prefill", "cp_decode_plan", "cp_partial_attn_decode", "cp_lse_merge",
     "cp_decode_workspace_size", "cp_decode_attention", "cp_decode_attention_noalloc",
-    "cp_kv_cache_write", "STATUS",
+    "cp_kv_cache_write", "cp_select_prefill_mode", "cp_attn_prefill_fused", "STATUS",
 ]
 
 CP_F32, CP_BF16 = 0, 1
@@ -88,6 +88,8 @@ _SIGS = [
                                                  _vp]),
     ("cp_kv_cache_write", ctypes.c_int32, [_vp, _vp, _vp, _vp] + [ctypes.c_int32] * 8 +
      [_vp, ctypes.c_int32, ctypes.c_int64, _vp, _vp, _vp, _vp]),
+    ("cp_attn_prefill_fused", ctypes.c_int32, [ctypes.POINTER(PrefillArgs), _vp, _vp, _vp]),
+    ("cp_select_prefill_mode", ctypes.c_int32, [ctypes.c_int64, ctypes.c_int64] + [ctypes.c_int32] * 4),
     ("cp_partial_attn_prefill", ctypes.c_int32, [ctypes.POINTER(PrefillArgs), _vp]),
     ("cp_decode_plan", ctypes.c_int32, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_int32)] * 2),
     ("cp_partial_attn_decode", ctypes.c_int32, [ctypes.POINTER(DecodeArgs), _vp]),
@@ -232,6 +234,13 @@ def cp_kv_cache_write(k_new, v_new, cu_new, start_pos, k_cache, v_cache, block_t
                                   _ptr(k_cache), _ptr(v_cache), _ptr(err), _stream(stream)))
 
 
+def cp_select_prefill_mode(q_len, kv_len, num_q_heads, num_kv_heads, head_dim, elem_bytes=2):
+    """CP_PASS_KV or CP_PASS_Q by the bytes each would exchange between ranks (see cpattn.h)."""
+    load()
+    return _LIB.cp_select_prefill_mode(q_len, kv_len, num_q_heads, num_kv_heads, head_dim,
+                                       elem_bytes)
+
+
 def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=None,
                             k_cache=None, v_cache=None, block_tables=None, seq_lens_kv=None,
                             interleave=8, max_seqlen_q=None, softmax_scale=0.0,
@@ -284,6 +293,33 @@ def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=N
         a.seq_lens_kv = _ptr(seq_lens_kv)
     _check(_LIB.cp_partial_attn_prefill(ctypes.byref(a), _stream(stream)))
     return out, lse
+
+
+def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k, v, *, max_seqlen_q=None, softmax_scale=0.0,
+                          impl=CP_IMPL_AUTO, out=None, out_lse=None, stream=None):
+    """Pass-KV prefill with the merge folded in (see cpattn.h): exact causal attention
+    out [Nq, Hq, d] bf16 and lse [Nq, Hq] f32 without partials."""
+    load()
+    Nq, Hq, d = q.shape
+    B = cu_seqlens_q.numel() - 1
+    if out is None:
+        out = torch.empty(Nq, Hq, d, dtype=torch.bfloat16, device=q.device)
+    if out_lse is None:
+        out_lse = torch.empty(Nq, Hq, dtype=torch.float32, device=q.device)
+    for n, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                     ("cu_seqlens_q", cu_seqlens_q, torch.int32), ("out", out, torch.bfloat16),
+                     ("out_lse", out_lse, torch.float32)):
+        _dev(t, n, dt)
+    if max_seqlen_q is None:
+        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B else 0
+    a = PrefillArgs()
+    a.mode, a.dtype, a.impl = CP_PASS_KV, CP_BF16, impl
+    a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.cp = B, Hq, k.shape[1], d, cp
+    a.softmax_scale, a.total_q, a.max_seqlen_q = softmax_scale, Nq, max_seqlen_q
+    a.q_shard = a.kv_shard = -1
+    a.cu_seqlens_q, a.q, a.k, a.v = _ptr(cu_seqlens_q), _ptr(q), _ptr(k), _ptr(v)
+    _check(_LIB.cp_attn_prefill_fused(ctypes.byref(a), _ptr(out), _ptr(out_lse), _stream(stream)))
+    return out, out_lse
 
 
 def cp_decode_plan(num_seqs, num_kv_heads, cp, interleave, block_size, max_seq_len):

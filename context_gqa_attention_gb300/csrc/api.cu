@@ -383,6 +383,14 @@ cp_status cp_kv_interleave_layout(const int32_t* cu_seq_lens, int32_t num_seqs,
   return launched(cudaGetLastError(), "cp_kv_interleave_layout launch");
 }
 
+int32_t cp_select_prefill_mode(int64_t q_len, int64_t kv_len, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t elem_bytes) {
+  const double kv = (double)kv_len * 2.0 * num_kv_heads * head_dim * elem_bytes;
+  const double q = (double)q_len * num_q_heads * head_dim * elem_bytes +
+                   (double)q_len * num_q_heads * (head_dim + 1) * 4.0;
+  return q < kv ? CP_PASS_Q : CP_PASS_KV;
+}
+
 cp_status cp_kv_cache_write(const void* k_new, const void* v_new, const int32_t* cu_new,
                            const int32_t* start_pos, int32_t num_seqs, int32_t total_new,
                            int32_t num_kv_heads, int32_t head_dim, int32_t dtype, int32_t cp,
@@ -492,6 +500,30 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   return launched(cp_launch_prefill_simt(*a, scale, as_stream(stream)), "prefill (simt) launch");
 }
 
+cp_status cp_attn_prefill_fused(const cp_prefill_args* a, void* out, float* out_lse, void* stream) {
+  REQUIRE(a != nullptr, "args is null");
+  REQUIRE(a->mode == CP_PASS_KV, "the fused prefill is pass-KV");
+  if (a->dtype != CP_BF16) return fail(CP_ERR_UNSUPPORTED, "the fused prefill takes bf16 inputs");
+  if (a->head_dim != 64 && a->head_dim != 128)
+    return fail(CP_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", a->head_dim);
+  REQUIRE(a->num_seqs >= 1 && a->num_kv_heads >= 1 && a->num_q_heads % a->num_kv_heads == 0,
+          "bad head counts");
+  REQUIRE(a->cp >= 1 && a->cp <= 64, "cp must be in [1, 64]");
+  REQUIRE(a->q_shard == -1 && a->kv_shard == -1, "the fused prefill covers every pair");
+  REQUIRE(a->total_q >= 0 && a->max_seqlen_q >= 0, "bad total_q / max_seqlen_q");
+  REQUIRE(a->cu_seqlens_q != nullptr, "cu_seqlens_q is null");
+  REQUIRE_PTR(a->q);
+  REQUIRE_PTR(a->k);
+  REQUIRE_PTR(a->v);
+  REQUIRE_PTR(out);
+  REQUIRE(out_lse != nullptr, "out_lse is null");
+  REQUIRE(a->debug == 0, "debug must be 0");
+  if (a->total_q == 0) return ok();
+  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
+  return launched(cp_launch_prefill_fused(*a, scale, out, out_lse, as_stream(stream)),
+                  "fused prefill launch");
+}
+
 cp_status cp_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t cp, int32_t interleave,
                          int32_t block_size, int32_t max_seq_len, int32_t* num_splits,
                          int32_t* split_tokens) {
@@ -503,9 +535,10 @@ cp_status cp_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t cp, int
   const long long group = (long long)interleave * cp;
   long long rem = max_seq_len % group;
   const long long share = (max_seq_len / group) * interleave + (rem < interleave ? rem : interleave);
-  // target ~1024 local tokens per CTA and at least ~8 CTAs per SM over 152 SMs in total
+  // target ~2048 local tokens per CTA (measured best between 1024 and 6144 on the 64-sequence
+  // decode workload) and at least ~8 CTAs per SM over 152 SMs in total
   const long long base = (long long)num_seqs * num_kv_heads * cp;
-  long long S = (share + 1023) / 1024;
+  long long S = (share + 2047) / 2048;
   const long long want = (8ll * 152 + base - 1) / base;
   if (S < want) S = want;
   const long long max_S = (share + block_size - 1) / block_size;

@@ -459,7 +459,7 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
       if (lane < cnt) {
         const int pg = pg0 + j0 + lane;
         my_id = pg < p.max_blocks ? __ldg(trow + pg) : -1;
-        if (my_id >= p.pool) my_id = -1;
+        if (my_id >= p.pool || my_id < 0) my_id = -1;
       }
       for (int i = 0; i < cnt; ++i) {
         const int id = __shfl_sync(0xffffffffu, my_id, i);
@@ -481,7 +481,8 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
                 sm100::tma_load_2d(ks + Ly::kPageBytes + kb * (kPage * 128), &map_v, kb * 64, y,
                                    full(w, st));
               }
-            } else {
+            } else {  // a table entry outside the pool: the page is skipped and reported
+              report(p.err, CP_ERR_DEVICE_BOUNDS);
               sm100::mbar_arrive(full(w, st));  // the consumer sees flag 0 and skips the page
             }
             issued = j + 1;

@@ -46,6 +46,11 @@ struct TcParams {
   float* out;
   float* lse;
   int32_t* err;
+  // fused pass-KV: one item covers every kv shard (keys [0, q_hi)) and writes the final bf16
+  // output [Nq][Hq][d] and LSE [Nq][Hq] instead of partials
+  int fused;
+  __nv_bfloat16* out_final;
+  float* lse_final;
 };
 
 template <int D>
@@ -78,6 +83,43 @@ struct Work {
   int ntiles;
 };
 
+// pass-Q: block-table entries of key tile t (NP pages of 16 rank-local tokens).  Entries past
+// the table's width read as -1; rows past the rank's visible tokens are not loaded.
+template <int NP>
+CP_DEV void fetch_page_ids(const int32_t* trow, int t, int n_local, int max_blocks, int (&id)[NP]) {
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    const int col = t * NP + j;
+    id[j] = (col * 16 < n_local && col < max_blocks) ? __ldg(trow + col) : -1;
+  }
+}
+
+// Tensor-map row of each page of key tile t.  A visible page whose entry is outside the pool
+// flags CP_ERR_DEVICE_BOUNDS; it and the pages past the visible range reload the tile's last
+// valid page (finite data, masked by the softmax) so every stage receives the same byte count.
+template <int NP>
+CP_DEV void page_rows(const int (&id)[NP], int t, int n_local, long long pool, int Hkv, int rank, int g,
+                      int* err, int (&row)[NP]) {
+  int last_good = -1;
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    int pg = -1;
+    if ((t * NP + j) * 16 < n_local) {
+      pg = id[j];
+      if (pg < 0 || pg >= pool) {
+        report(err, CP_ERR_DEVICE_BOUNDS);
+        pg = -1;
+      }
+    }
+    if (pg >= 0) last_good = pg;
+    row[j] = pg;
+  }
+  if (last_good < 0) last_good = 0;
+#pragma unroll
+  for (int j = 0; j < NP; ++j)
+    row[j] = (int)((((long long)rank * pool + (row[j] >= 0 ? row[j] : last_good)) * Hkv + g) * 16);
+}
+
 // blockIdx.x -> (q tile slot, sequence, kv shard, head group of `hpc` consecutive q heads).
 // Slots run heaviest first (last chunk, last tile) so long items start early.
 CP_DEV Work decode_work(const TcParams& p, int hpc) {
@@ -87,8 +129,8 @@ CP_DEV Work decode_work(const TcParams& p, int hpc) {
   const int groups = p.Hq / hpc;
   w.h = (int)(lin % groups) * hpc;
   lin /= groups;
-  if (p.kv_shard >= 0) {
-    w.p = p.kv_shard;
+  if (p.kv_shard >= 0 || p.fused) {
+    w.p = p.fused ? 0 : p.kv_shard;
   } else {
     w.p = (int)(lin % p.cp);
     lin /= p.cp;
@@ -110,7 +152,15 @@ CP_DEV Work decode_work(const TcParams& p, int hpc) {
   w.g = w.h / (p.Hq / p.Hkv);
   w.q_row0 = q0 + w.q_lo;
   w.ntiles = 0;
-  if (p.mode == CP_PASS_KV) {
+  if (p.mode == CP_PASS_KV && p.fused) {  // the union of all shards' keys: [0, q_hi)
+    w.qpos0 = w.q_lo;
+    w.kv_row0 = q0;
+    w.ks[0] = 0;
+    w.ke[0] = w.q_hi;
+    w.nt[0] = (w.q_hi + BN - 1) / BN;
+    w.ks[1] = w.ke[1] = w.nt[1] = 0;
+    w.ntiles = w.nt[0];
+  } else if (p.mode == CP_PASS_KV) {
     w.qpos0 = w.q_lo;
     w.kv_row0 = q0;
 #pragma unroll
@@ -186,15 +236,32 @@ CP_DEV void load_row(uint32_t tS, float (&v0)[32], float (&v1)[32], float (&v2)[
   tmem_wait_ld(v3);
 }
 
+// Four independent packed partial sums keep the additions off one serial dependency chain.
 CP_DEV void exp_chunk(float (&a)[32], uint64_t sc2, uint64_t n2, uint64_t& sum2) {
+  uint64_t acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
   for (int k = 0; k < 32; k += 2) {
     float x0, x1;
     f2u(ffma2(f2(a[k], a[k + 1]), sc2, n2), x0, x1);
     a[k] = ex2(x0);
     a[k + 1] = ex2(x1);
-    sum2 = fadd2(sum2, f2(a[k], a[k + 1]));
+    acc[(k >> 1) & 3] = fadd2(acc[(k >> 1) & 3], f2(a[k], a[k + 1]));
   }
+  sum2 = fadd2(sum2, fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])));
+}
+
+// Row max of four 32-column chunks with four independent accumulators.
+CP_DEV float max4x32(const float (&v0)[32], const float (&v1)[32], const float (&v2)[32],
+                     const float (&v3)[32]) {
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < 32; k += 2) {
+    m0 = fmax3(m0, v0[k], v0[k + 1]);
+    m1 = fmax3(m1, v1[k], v1[k + 1]);
+    m2 = fmax3(m2, v2[k], v2[k + 1]);
+    m3 = fmax3(m3, v3[k], v3[k + 1]);
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
 // Online-softmax step of one row over a 128-key tile: columns > lim are masked (skipped when
@@ -212,13 +279,7 @@ CP_DEV float row_softmax(float (&v0)[32], float (&v1)[32], float (&v2)[32], floa
       v3[k] = k + 96 <= lim ? v3[k] : -INFINITY;
     }
   }
-  float mx = -INFINITY;
-#pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    mx = fmax3(mx, v0[k], v1[k]);
-    mx = fmax3(mx, v2[k], v3[k]);
-  }
-  const float m_tile = mx * sc;
+  const float m_tile = max4x32(v0, v1, v2, v3) * sc;
   float alpha = 1.f;
   if (m_tile > m + kRescaleThreshold) {  // first visible tile, or the max grew a lot
     alpha = ex2(m - m_tile);
@@ -250,13 +311,7 @@ CP_DEV float row_max_update(float (&v0)[32], float (&v1)[32], float (&v2)[32], f
       v3[k] = k + 96 <= lim ? v3[k] : -INFINITY;
     }
   }
-  float mx = -INFINITY;
-#pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    mx = fmax3(mx, v0[k], v1[k]);
-    mx = fmax3(mx, v2[k], v3[k]);
-  }
-  const float m_tile = mx * sc;
+  const float m_tile = max4x32(v0, v1, v2, v3) * sc;
   float alpha = 1.f;
   if (m_tile > m + kRescaleThreshold) {
     alpha = ex2(m - m_tile);
@@ -373,6 +428,27 @@ CP_DEV void write_row(uint32_t tO, float m, float l, bool row_valid, float* dst,
   if (row_valid) *lse_dst = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
+// Final O row / l -> bf16 output (round to nearest even) and its LSE (warp-collective).
+template <int D>
+CP_DEV void write_row_bf16(uint32_t tO, float m, float l, bool row_valid, __nv_bfloat16* dst,
+                           float* lse_dst) {
+  const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    float o[32];
+    tmem_ld32(tO + c * 32, o);
+    tmem_wait_ld(o);
+    if (row_valid) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 8)
+        *reinterpret_cast<uint4*>(dst + c * 32 + k) = make_uint4(
+            pack_bf16(o[k] * inv_l, o[k + 1] * inv_l), pack_bf16(o[k + 2] * inv_l, o[k + 3] * inv_l),
+            pack_bf16(o[k + 4] * inv_l, o[k + 5] * inv_l), pack_bf16(o[k + 6] * inv_l, o[k + 7] * inv_l));
+    }
+  }
+  if (row_valid) *lse_dst = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
 // ---------------------------------------------------------------------------------- kernel
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -443,6 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int lk0 = -1, lk1 = -1, lv0 = -1, lv1 = -1;  // phase of the last K / V fill per stage
       const int32_t* trow =
           p.mode == CP_PASS_Q ? p.tables + ((long long)w.p * p.B + w.b) * p.max_blocks : nullptr;
+      int pid[BN / 16];  // pass-Q: page ids of the next tile, loaded one tile ahead
+      if (p.mode == CP_PASS_Q) fetch_page_ids(trow, 0, w.n_local, p.max_blocks, pid);
       bool ok = true;
       for (int t = 0; t < w.ntiles; ++t) {
         const int s = t % NS;
@@ -466,31 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kb = 0; kb < KB; ++kb)
             tma_load_2d(dV + kb * BN * 128, &map_v, w.g * D + kb * 64, y, bar(Ly::bVF + s));
         } else {
-          // 8 pages of 16 rank-local tokens; pages past the visible range reload the last
-          // valid page (finite data, masked by the softmax) so the byte count is constant
           int rows[BN / 16];
-          int last_good = -1;
-#pragma unroll
-          for (int i = 0; i < BN / 16; ++i) {
-            const int l = t * BN + i * 16;
-            int pg = -1;
-            if (l < w.n_local) {
-              const int col = l / 16;
-              pg = col < p.max_blocks ? __ldg(trow + col) : -1;
-              if (pg < 0 || pg >= p.pool) {
-                report(p.err, CP_ERR_DEVICE_BOUNDS);
-                pg = -1;
-              }
-            }
-            if (pg >= 0) last_good = pg;
-            rows[i] = pg;
-          }
-          if (last_good < 0) last_good = 0;
-#pragma unroll
-          for (int i = 0; i < BN / 16; ++i) {
-            const int pg = rows[i] >= 0 ? rows[i] : last_good;
-            rows[i] = (int)((((long long)w.p * p.pool + pg) * p.Hkv + w.g) * 16);
-          }
+          page_rows(pid, t, w.n_local, p.pool, p.Hkv, w.p, w.g, p.err, rows);
+          if (t + 1 < w.ntiles) fetch_page_ids(trow, t + 1, w.n_local, p.max_blocks, pid);
           mbar_expect_tx(bar(Ly::bKF + s), Ly::kKV);
 #pragma unroll
           for (int i = 0; i < BN / 16; ++i)
@@ -626,8 +682,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              abort_flag, p.budget));
     if (ok) {
       tc_fence_after();
-      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h;
-      write_row<D>(tO + lane_off, m, l, row_valid, p.out + orow * D, p.lse + orow);
+      if (p.fused) {
+        const long long frow = (long long)(w.q_row0 + row) * p.Hq + w.h;
+        write_row_bf16<D>(tO + lane_off, m, l, row_valid, p.out_final + frow * D, p.lse_final + frow);
+      } else {
+        const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h;
+        write_row<D>(tO + lane_off, m, l, row_valid, p.out + orow * D, p.lse + orow);
+      }
     } else {
       fail_timeout(abort_flag, p.err);
     }
@@ -746,6 +807,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const int32_t* trow =
           p.mode == CP_PASS_Q ? p.tables + ((long long)w.p * p.B + w.b) * p.max_blocks : nullptr;
       int prow[BN / 16];  // pass-Q: element rows of the current tile's pages (K and V alike)
+      int pid[BN / 16];   // pass-Q: page ids of the next tile, loaded one tile ahead
+      if (p.mode == CP_PASS_Q) fetch_page_ids(trow, 0, w.n_local, p.max_blocks, pid);
       bool ok = true;
       for (int i = 0; i < 2 * w.ntiles; ++i) {
         const int slot = i % NSLOT;
@@ -765,27 +828,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
             tma_load_2d(dst + kb * BN * 128, map, w.g * D + kb * 64, y, bar(Ly::bFull + slot));
         } else {
           if (!isV) {  // page rows of tile t (reused for its V load)
-            int last_good = -1;
-#pragma unroll
-            for (int j = 0; j < BN / 16; ++j) {
-              const int l = t * BN + j * 16;
-              int pg = -1;
-              if (l < w.n_local) {
-                const int col = l / 16;
-                pg = col < p.max_blocks ? __ldg(trow + col) : -1;
-                if (pg < 0 || pg >= p.pool) {
-                  report(p.err, CP_ERR_DEVICE_BOUNDS);
-                  pg = -1;
-                }
-              }
-              if (pg >= 0) last_good = pg;
-              prow[j] = pg;
-            }
-            if (last_good < 0) last_good = 0;
-#pragma unroll
-            for (int j = 0; j < BN / 16; ++j)
-              prow[j] = (int)((((long long)w.p * p.pool + (prow[j] >= 0 ? prow[j] : last_good)) *
-                                   p.Hkv + w.g) * 16);
+            page_rows(pid, t, w.n_local, p.pool, p.Hkv, w.p, w.g, p.err, prow);
+            if (t + 1 < w.ntiles) fetch_page_ids(trow, t + 1, w.n_local, p.max_blocks, pid);
           }
 #pragma unroll
           for (int j = 0; j < BN / 16; ++j)
@@ -931,8 +975,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
                                              abort_flag, p.budget));
     if (ok) {
       tc_fence_after();
-      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile;
-      write_row<D>(tO, m, l, row_valid, p.out + orow * D, p.lse + orow);
+      if (p.fused) {
+        const long long frow = (long long)(w.q_row0 + row) * p.Hq + w.h + tile;
+        write_row_bf16<D>(tO, m, l, row_valid, p.out_final + frow * D, p.lse_final + frow);
+      } else {
+        const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile;
+        write_row<D>(tO, m, l, row_valid, p.out + orow * D, p.lse + orow);
+      }
     } else {
       fail_timeout(abort_flag, p.err);
     }
@@ -981,7 +1030,8 @@ bool make_map(CUtensorMap* m, const void* base, unsigned long long cols, unsigne
 }
 
 template <int D>
-cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s) {
+cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* fused_out,
+                   float* fused_lse) {
   CUtensorMap mq, mk, mv;
   const unsigned long long Nq = (unsigned long long)a.total_q;
   if (!make_map(&mq, a.q, (unsigned long long)a.num_q_heads * D, Nq,
@@ -1019,11 +1069,14 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s) {
   p.out = a.out;
   p.lse = a.lse;
   p.err = a.err;
+  p.fused = fused_out != nullptr;
+  p.out_final = static_cast<__nv_bfloat16*>(fused_out);
+  p.lse_final = fused_lse;
   // two heads per CTA when the heads of a kv group pair up, unless one head per CTA is forced
   const int G = a.num_q_heads / a.num_kv_heads;
   const bool pair = (G % 2 == 0) && a.impl != CP_IMPL_TCGEN05_SINGLE;
-  const long long grid = (long long)2 * a.cp * p.TPC * a.num_seqs * (a.kv_shard >= 0 ? 1 : a.cp) *
-                         (a.num_q_heads / (pair ? 2 : 1));
+  const long long grid = (long long)2 * a.cp * p.TPC * a.num_seqs *
+                         ((a.kv_shard >= 0 || p.fused) ? 1 : a.cp) * (a.num_q_heads / (pair ? 2 : 1));
   if (grid == 0) return cudaSuccess;
   if (grid >= (1ll << 31)) return cudaErrorInvalidConfiguration;
   cudaError_t e;
@@ -1059,5 +1112,12 @@ bool cp_prefill_tc_supported(const cp_prefill_args& a) {
 }
 
 cudaError_t cp_launch_prefill_tc(const cp_prefill_args& a, float scale, cudaStream_t s) {
-  return a.head_dim == 64 ? cpattn::launch<64>(a, scale, s) : cpattn::launch<128>(a, scale, s);
+  return a.head_dim == 64 ? cpattn::launch<64>(a, scale, s, nullptr, nullptr)
+                          : cpattn::launch<128>(a, scale, s, nullptr, nullptr);
+}
+
+cudaError_t cp_launch_prefill_fused(const cp_prefill_args& a, float scale, void* out, float* lse,
+                                    cudaStream_t s) {
+  return a.head_dim == 64 ? cpattn::launch<64>(a, scale, s, out, lse)
+                          : cpattn::launch<128>(a, scale, s, out, lse);
 }

@@ -153,6 +153,21 @@ cp_status cp_kv_cache_write(const void* k_new, const void* v_new, const int32_t*
                            int32_t* err, void* stream);
 
 /* ------------------------------------------------------------------------------
+ * cp_select_prefill_mode -- pass-KV or pass-Q for a prefill chunk ([PKV] Purpose: passing KV
+ * suits full prefill because a KV head serves more than two query heads in most models; passing
+ * Q suits chunked prefill when the cached context is much longer than the new queries).
+ *
+ * The rule made quantitative by the bytes one rank would exchange with the others:
+ *   pass-KV  moves its KV shard:  kv_len * 2 * Hkv * d * elem_bytes
+ *   pass-Q   moves its Q shard and gets its partials back:
+ *            q_len * Hq * d * elem_bytes  +  q_len * Hq * (d + 1) * 4
+ * (both per cp-th of the sequence).  Returns CP_PASS_Q when that is smaller, else CP_PASS_KV.
+ * Host-only and pure; kv_len counts cached + new tokens, q_len the new ones.
+ * ---------------------------------------------------------------------------- */
+int32_t cp_select_prefill_mode(int64_t q_len, int64_t kv_len, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t elem_bytes);
+
+/* ------------------------------------------------------------------------------
  * cp_partial_attn_prefill -- partial attention for every (Q shard, KV shard) pair
  * ([PKV] Purpose: pass-KV for full prefill, pass-Q for chunked prefill; the
  * exchange itself is logical here, so one launch covers every rotation step).
@@ -210,6 +225,21 @@ typedef struct cp_prefill_args {
 } cp_prefill_args;
 
 cp_status cp_partial_attn_prefill(const cp_prefill_args* args, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * cp_attn_prefill_fused -- pass-KV prefill with the merge folded in ([PKV] Purpose: the
+ * partials of all KV shards of a Q row are combined; here one work item walks every shard's
+ * keys -- for a query tile of chunk c the union of the shards' visible keys is the contiguous
+ * range of earlier positions -- with one online softmax, so no partial is written).
+ *
+ * Same arguments as cp_partial_attn_prefill with mode CP_PASS_KV, dtype CP_BF16 and
+ * q_shard = kv_shard = -1 (args->out / args->lse are not used); writes
+ *   out      device bf16 [Nq][Hq][d]: exact causal attention (round to nearest even)
+ *   out_lse  device f32 [Nq][Hq] natural-log LSE (NULL not allowed).
+ * Equals cp_lse_merge applied to cp_partial_attn_prefill's partials, up to rounding.
+ * ---------------------------------------------------------------------------- */
+cp_status cp_attn_prefill_fused(const cp_prefill_args* args, void* out, float* out_lse,
+                                void* stream);
 
 /* ------------------------------------------------------------------------------
  * cp_partial_attn_decode -- per-rank partial attention of one new query token per

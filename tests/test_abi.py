@@ -88,3 +88,18 @@ def test_decode_plan_covers_every_rank_share(lib):
         share = (L // group) * I + min(L % group, I)
         assert st.value % 16 == 0 and ns.value * st.value >= share
         assert (ns.value - 1) * st.value < max(share, 1)
+
+
+def test_prefill_mode_selector_follows_the_pages_rule(lib):
+    """Full prefill with more than two query heads per kv head -> pass-KV; chunked prefill with
+    a context much longer than the new queries -> pass-Q; the crossover moves with G."""
+    sel = lib.cp_select_prefill_mode
+    assert sel(8192, 8192, 16, 2, 128, 2) == 0          # full prefill, G = 8
+    assert sel(8192, 8192, 4, 2, 128, 2) == 0           # full prefill, G = 2
+    assert sel(2048, 32768, 16, 2, 128, 2) == 1         # the chunked workload: pass-Q
+    assert sel(2048, 4096, 16, 2, 128, 2) == 0          # context only 2x the chunk: pass-KV
+    # crossover: pass-Q once kv_len / q_len exceeds (G/2) (1 + 2 (d + 1) / d)
+    G, d = 8, 128
+    ratio = G / 2 * (1 + 2 * (d + 1) / d)
+    assert sel(1000, int(1000 * ratio) + 8, 8 * G, 8, d, 2) == 1
+    assert sel(1000, int(1000 * ratio) - 8, 8 * G, 8, d, 2) == 0

@@ -190,17 +190,33 @@ def test_pass_q_parity(lib, case, impl):
     check_merged(mo, ml, Om, Lm, what=f"pass-Q {impl} merged")
 
 
-def test_pass_q_reports_bad_page(lib):
-    x = _paged_case(1, [20], [100], 4, 1, 64, torch.bfloat16, 2, 8, 9)
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
+def test_pass_q_reports_bad_page(lib, impl):
+    """Block-table entries outside the pool (too large, negative) are checked before any read:
+    the kernel flags CP_ERR_DEVICE_BOUNDS and the next valid call still matches the oracle."""
+    x = _paged_case(1, [20], [300], 4, 1, 64, torch.bfloat16, 2, 8, 9)
+    dev = {n: x[n].to(DEV) for n in ("q", "cu_seqlens_q", "k_cache", "v_cache", "seq_lens")}
     tables = x["block_tables"].clone()
-    tables[1, 0, 1] = 10 ** 6          # outside the pool: the kernel checks before reading
+    tables[1, 0, 1] = 10 ** 6          # outside the pool
+    tables[0, 0, 3] = -5
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    lib.cp_partial_attn_prefill(x["q"].to(DEV), x["cu_seqlens_q"].to(DEV), 2, mode=lib.CP_PASS_Q,
-                                k_cache=x["k_cache"].to(DEV), v_cache=x["v_cache"].to(DEV),
-                                block_tables=tables.to(DEV), seq_lens_kv=x["seq_lens"].to(DEV),
-                                interleave=8, impl=lib.CP_IMPL_SIMT, err=err, max_seqlen_q=20)
+
+    def run(t):
+        return lib.cp_partial_attn_prefill(
+            dev["q"], dev["cu_seqlens_q"], 2, mode=lib.CP_PASS_Q, k_cache=dev["k_cache"],
+            v_cache=dev["v_cache"], block_tables=t.to(DEV), seq_lens_kv=dev["seq_lens"],
+            interleave=8, impl=_impl_code(lib, impl), err=err, max_seqlen_q=20)
+
+    run(tables)
     torch.cuda.synchronize()
     assert int(err.item()) == 5
+    err.zero_()
+    out, lse = run(x["block_tables"])
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    O, L = orc.pass_q_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                               x["cu_seqlens_q"], x["seq_lens"], 2, 8, 16, 1 / 8)
+    check_partials(out, lse, O, L, what=f"pass-Q {impl} after a bad table")
 
 
 # ------------------------------------------------------------------------------------ decode
@@ -284,6 +300,37 @@ def test_decode_fused_parity(lib, case):
     assert (mo.float() - outs[0].float()).abs().max().item() <= 1e-2
 
 
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_decode_reports_bad_page(lib, dt):
+    """Decode (tensor-core bf16 and CUDA-core f32 kernels) checks every visible page id: an entry
+    outside the pool is skipped and flagged, and the next valid call still matches."""
+    B, Hq, Hkv, d, cp, I = 2, 16, 4, 128, 2, 8
+    lens = [700, 300]
+    x = wl.paged_inputs(B, 1, lens, Hq, Hkv, d, dt, cp, I, 16, 21, 22, q_is_decode=True)
+    dev = {n: x[n].to(DEV) for n in ("q", "k_cache", "v_cache", "seq_lens")}
+    tables = x["block_tables"].clone()
+    tables[0, 0, 2] = 10 ** 6
+    tables[1, 1, 0] = -1
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def run(t):
+        return lib.cp_partial_attn_decode(dev["q"], dev["k_cache"], dev["v_cache"], t.to(DEV),
+                                          dev["seq_lens"], cp, I, max_seq_len=max(lens), err=err)
+
+    run(tables)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 5
+    err.zero_()
+    out, lse = run(x["block_tables"])
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    O, L = orc.decode_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                               x["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
+    mo, ml = lib.cp_lse_merge(out, lse, out_dtype=dt)
+    Om, Lm = orc.lse_merge(O, L)
+    check_merged(mo, ml, Om, Lm, what="decode after a bad table")
+
+
 def test_decode_fused_rejects_small_workspace(lib):
     q = torch.zeros(2, 8, 128, dtype=torch.bfloat16, device=DEV)
     kc = torch.zeros(1, 4, 2, 16, 128, dtype=torch.bfloat16, device=DEV)
@@ -333,3 +380,17 @@ def test_kv_cache_write_reports_missing_page(lib):
     torch.cuda.synchronize()
     assert int(err.item()) == 5
     assert int((kc != 0).any(dim=-1).sum().item()) == 32    # 16 slots per rank written
+
+
+# ------------------------------------------------------------------------------------ fused prefill
+
+@pytest.mark.parametrize("case", [1, 2, 3, 4, 6])
+def test_fused_prefill_parity(lib, case):
+    """cp_attn_prefill_fused = merged pass-KV partials = plain causal attention."""
+    lens, Hq, Hkv, d, dt, cp = PASS_KV_CASES[case]
+    x = wl.prefill_inputs(lens, Hq, Hkv, d, dt, seed=100 + case)
+    out, lse = lib.cp_attn_prefill_fused(x["q"].to(DEV), x["cu_seqlens"].to(DEV), cp,
+                                         x["k"].to(DEV), x["v"].to(DEV), max_seqlen_q=max(lens))
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], cp, 1 / math.sqrt(d))
+    Om, Lm = orc.lse_merge(O, L)
+    check_merged(out, lse, Om, Lm, what="fused prefill")
