@@ -20,6 +20,7 @@
 // Every wait is bounded; on expiry the CTA raises CP_ERR_TIMEOUT, drains its own copies and
 // MMAs, frees TMEM and returns.
 #include <cuda.h>
+#include <cstring>
 
 #include "common.cuh"
 #include "sm100.cuh"
@@ -51,6 +52,8 @@ struct TcParams {
   int fused;
   __nv_bfloat16* out_final;
   float* lse_final;
+  // 1: the output tensor map is valid and full 32-row groups are written by TMA stores
+  int tma_out;
 };
 
 template <int D>
@@ -449,6 +452,43 @@ CP_DEV void write_row_bf16(uint32_t tO, float m, float l, bool row_valid, __nv_b
   if (row_valid) *lse_dst = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
+// Final O rows of one warp (its 32 TMEM lanes = 32 query rows, scaled by 1/l) staged in shared
+// memory as the 128-byte-swizzled boxes of the output tensor map: f32 boxes of 32 columns x 32
+// rows (4 KB each, 16-byte chunk j of row r at chunk j ^ (r % 8)), or bf16 boxes of 64 columns.
+// One TMA store per box then writes whole 128-byte lines instead of one 16-byte piece per row.
+template <int D>
+CP_DEV void stage_rows_f32(uint32_t tO, float inv_l, uint32_t sbase, int lane) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    float o[32];
+    tmem_ld32(tO + c * 32, o);
+    tmem_wait_ld(o);
+    const uint32_t rb = sbase + (uint32_t)(c * 4096 + lane * 128);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(rb + ((uint32_t)(j ^ (lane & 7)) << 4), __float_as_uint(o[4 * j] * inv_l),
+                   __float_as_uint(o[4 * j + 1] * inv_l), __float_as_uint(o[4 * j + 2] * inv_l),
+                   __float_as_uint(o[4 * j + 3] * inv_l));
+  }
+}
+template <int D>
+CP_DEV void stage_rows_bf16(uint32_t tO, float inv_l, uint32_t sbase, int lane) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    float o[32];
+    tmem_ld32(tO + c * 32, o);
+    tmem_wait_ld(o);
+    const uint32_t rb = sbase + (uint32_t)((c >> 1) * 4096 + lane * 128);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st_shared_v4(rb + ((uint32_t)(((c & 1) * 4 + j) ^ (lane & 7)) << 4),
+                   pack_bf16(o[8 * j] * inv_l, o[8 * j + 1] * inv_l),
+                   pack_bf16(o[8 * j + 2] * inv_l, o[8 * j + 3] * inv_l),
+                   pack_bf16(o[8 * j + 4] * inv_l, o[8 * j + 5] * inv_l),
+                   pack_bf16(o[8 * j + 6] * inv_l, o[8 * j + 7] * inv_l));
+  }
+}
+
 // ---------------------------------------------------------------------------------- kernel
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -738,7 +778,8 @@ template <int D, bool PT>
 __global__ void __launch_bounds__(kThreads2, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
-                       const __grid_constant__ CUtensorMap map_v, const TcParams p) {
+                       const __grid_constant__ CUtensorMap map_v,
+                       const __grid_constant__ CUtensorMap map_o, const TcParams p) {
   using Ly = Layout2<D, PT>;
   constexpr int NSLOT = Ly::NSLOT;
   constexpr int KB = D / 64;
@@ -975,11 +1016,31 @@ __global__ void __launch_bounds__(kThreads2, 1)
                                              abort_flag, p.budget));
     if (ok) {
       tc_fence_after();
-      if (p.fused) {
-        const long long frow = (long long)(w.q_row0 + row) * p.Hq + w.h + tile;
+      const long long frow = (long long)(w.q_row0 + row) * p.Hq + w.h + tile;
+      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile;
+      if (p.tma_out && w.q_lo + q4 * 32 + 32 <= w.q_hi) {
+        // all 32 rows of this warp are real: stage them and store by TMA.  Head 0 stages in
+        // the Q tiles (free: its last PV completed after the other head's last QK), head 1 in
+        // the K/V ring (free: its last PV is the CTA's last MMA).
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const uint32_t sb = (tile == 0 ? sQ : sKV) + (uint32_t)(q4 * 32 * D * (p.fused ? 2 : 4));
+        if (p.fused) stage_rows_bf16<D>(tO, inv_l, sb, lane);
+        else stage_rows_f32<D>(tO, inv_l, sb, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int z = (p.fused ? 0 : w.p * p.Nq) + w.q_row0 + q4 * 32;
+          const int nbox = p.fused ? D / 64 : D / 32, bw = p.fused ? 64 : 32;
+          for (int bx = 0; bx < nbox; ++bx) tma_store_3d(&map_o, sb + bx * 4096, bx * bw, w.h + tile, z);
+          bulk_commit();
+          bulk_wait_read_all();  // the staging buffer is released at kernel exit
+        }
+        const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        if (p.fused) p.lse_final[frow] = lse_v;
+        else p.lse[orow] = lse_v;
+      } else if (p.fused) {
         write_row_bf16<D>(tO, m, l, row_valid, p.out_final + frow * D, p.lse_final + frow);
       } else {
-        const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile;
         write_row<D>(tO, m, l, row_valid, p.out + orow * D, p.lse + orow);
       }
     } else {
@@ -1029,6 +1090,22 @@ bool make_map(CUtensorMap* m, const void* base, unsigned long long cols, unsigne
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3D map over an output [rows][H][D] (f32 partials or the bf16 final output) for TMA stores of
+// {128-byte column block, 1 head, 32 rows} boxes, 128-byte swizzle.
+bool make_out_map(CUtensorMap* m, void* base, bool bf16, unsigned long long D, unsigned long long H,
+                  unsigned long long rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || base == nullptr || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return false;
+  const unsigned long long es = bf16 ? 2 : 4;
+  cuuint64_t dims[3] = {D, H, rows};
+  cuuint64_t strides[2] = {D * es, H * D * es};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1, 32};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base,
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* fused_out,
                    float* fused_lse) {
@@ -1072,6 +1149,10 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   p.fused = fused_out != nullptr;
   p.out_final = static_cast<__nv_bfloat16*>(fused_out);
   p.lse_final = fused_lse;
+  CUtensorMap mo;
+  std::memset(&mo, 0, sizeof(mo));
+  p.tma_out = p.fused ? make_out_map(&mo, fused_out, true, D, a.num_q_heads, Nq)
+                      : make_out_map(&mo, a.out, false, D, a.num_q_heads, (unsigned long long)a.cp * Nq);
   // two heads per CTA when the heads of a kv group pair up, unless one head per CTA is forced
   const int G = a.num_q_heads / a.num_kv_heads;
   const bool pair = (G % 2 == 0) && a.impl != CP_IMPL_TCGEN05_SINGLE;
@@ -1085,7 +1166,7 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
     e = cudaFuncSetAttribute(prefill_tc2_kernel<D, kPInTmem>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    prefill_tc2_kernel<D, kPInTmem><<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, p);
+    prefill_tc2_kernel<D, kPInTmem><<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, mo, p);
   } else {
     const int smem = Layout<D>::kAlloc;
     e = cudaFuncSetAttribute(prefill_tc1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

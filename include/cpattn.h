@@ -185,8 +185,9 @@ int32_t cp_select_prefill_mode(int64_t q_len, int64_t kv_len, int32_t num_q_head
  *   2cp-1-r of the new tokens (the math does not depend on this split).
  *
  * Outputs: out[p][row][h][:] f32 (normalised over partial p's keys) and
- * lse[p][row][h] f32, p = kv shard / kv rank, row = token-major query row.  Pairs
- * with no visible key get lse = -inf and their out rows are left unwritten.
+ * lse[p][row][h] f32, p = kv shard / kv rank, row = token-major query row.  A
+ * (row, partial) with no visible key gets lse = -inf and its out row holds zeros or
+ * is left unwritten (the merge never reads it).
  * q_shard / kv_shard >= 0 restrict the launch to that Q shard / KV shard (one
  * logical rotation step); outputs of other pairs are left untouched.
  * ---------------------------------------------------------------------------- */
