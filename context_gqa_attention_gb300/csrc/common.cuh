@@ -26,12 +26,18 @@ template <> struct Elem<__nv_bfloat16> {
 
 // Chunk bounds of the load-balanced partition: b_k = floor(k*T/(2cp)).
 CP_DEV int chunk_bound(int k, int T, int cp) {
-  return (int)(((long long)k * T) / (2 * cp));
+  // k, T >= 0; 32-bit division whenever k*T fits (64-bit division is a long software routine)
+  const unsigned long long num = (unsigned long long)k * (unsigned)T;
+  const unsigned den = 2u * (unsigned)cp;
+  if (num <= 0xffffffffull) return (int)((unsigned)num / den);
+  return (int)(num / den);
 }
 
 // Chunk index c (0..2cp-1) of within-sequence offset t (0 <= t < T).
 CP_DEV int chunk_of(int t, int T, int cp) {
-  int c = (int)(((long long)t * 2 * cp) / T);  // lower estimate
+  const unsigned long long num = (unsigned long long)t * (2u * (unsigned)cp);
+  int c = num <= 0xffffffffull ? (int)((unsigned)num / (unsigned)T)  // lower estimate
+                               : (int)(num / (unsigned)T);
   // b_c <= t < b_{c+1}; the estimate is within one of the answer.
   while (c + 1 < 2 * cp && chunk_bound(c + 1, T, cp) <= t) ++c;
   while (c > 0 && chunk_bound(c, T, cp) > t) --c;
@@ -42,6 +48,11 @@ CP_DEV int shard_of_chunk(int c, int cp) { return c < cp ? c : 2 * cp - 1 - c; }
 
 // Round-robin interleave: tokens of rank r among positions [0, L).
 CP_DEV int rank_local_len(long long L, int r, int cp, int I) {
+  if (L >= 0 && L <= 0x7fffffffll && (long long)I * cp <= 0x7fffffffll) {  // 32-bit division
+    const unsigned g = (unsigned)I * (unsigned)cp, l = (unsigned)L;
+    const int rem = (int)(l % g) - r * I;
+    return (int)(l / g) * I + (rem < 0 ? 0 : (rem > I ? I : rem));
+  }
   long long group = (long long)I * cp;
   long long full = (L / group) * I;
   long long rem = L % group - (long long)r * I;

@@ -128,18 +128,18 @@ CP_DEV void page_rows(const int (&id)[NP], int t, int n_local, long long pool, i
 CP_DEV Work decode_work(const TcParams& p, int hpc) {
   Work w;
   w.valid = 0;
-  long long lin = blockIdx.x;
-  const int groups = p.Hq / hpc;
+  unsigned lin = blockIdx.x;  // 32-bit divisions: the grid is below 2^31 blocks
+  const unsigned groups = (unsigned)(p.Hq / hpc);
   w.h = (int)(lin % groups) * hpc;
   lin /= groups;
   if (p.kv_shard >= 0 || p.fused) {
     w.p = p.fused ? 0 : p.kv_shard;
   } else {
-    w.p = (int)(lin % p.cp);
-    lin /= p.cp;
+    w.p = (int)(lin % (unsigned)p.cp);
+    lin /= (unsigned)p.cp;
   }
-  w.b = (int)(lin % p.B);
-  lin /= p.B;
+  w.b = (int)(lin % (unsigned)p.B);
+  lin /= (unsigned)p.B;
   const int slot = (int)lin;  // heaviest tiles first: last chunk, last tile
   const int c = 2 * p.cp - 1 - slot / p.TPC;
   const int j = p.TPC - 1 - slot % p.TPC;
@@ -821,6 +821,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
     mbar_init(bar(Ly::bDone), 1);
     misc[1] = 0u;
     fence_mbar_init();
+    // the Q tiles of both heads load while the CTA is still setting up (TMEM, barriers)
+    tma_prefetch_desc(&map_q);
+    mbar_expect_tx(bar(Ly::bQ), 2 * Ly::kQ);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int kb = 0; kb < KB; ++kb)
+        tma_load_2d(sQ + i * Ly::kQ + kb * BM * 128, &map_q, (w.h + i) * D + kb * 64, w.q_row0,
+                    bar(Ly::bQ));
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), 512);
@@ -834,16 +843,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      mbar_expect_tx(bar(Ly::bQ), 2 * Ly::kQ);
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb)
-          tma_load_2d(sQ + i * Ly::kQ + kb * BM * 128, &map_q, (w.h + i) * D + kb * 64, w.q_row0,
-                      bar(Ly::bQ));
       int last0 = -1, last1 = -1, last2 = -1;  // phase of the last fill of each slot
       const int32_t* trow =
           p.mode == CP_PASS_Q ? p.tables + ((long long)w.p * p.B + w.b) * p.max_blocks : nullptr;
