@@ -39,14 +39,14 @@ import workloads as wl  # noqa: E402
 # each from one ncu capture summarised under profiles/.  A figure is reported only while the
 # kernel's source file still has the SHA-1 the capture was taken on; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # profiles/prefill_tc2_full_prefill.md: dram read 42.06 MB + write 65.12 MB
+    # profiles/prefill_tc2_full_prefill.md: dram read 42.03 MB + write 62.33 MB
     "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                "sha1": "0111a2b9414ea34c639d21667f38c1984de07853", "bytes": 107174912,
+                "sha1": "2c98202c8af4deb6ae39b8b89e5b84fb5d41e4ce", "bytes": 104365312,
                 "workload": "full"},
-    # profiles/decode_mma_decode.md: a 16-sequence capture (1.1186 GB read + 7.65 MB written),
+    # profiles/decode_mma_decode.md: a 16-sequence capture (1.1186 GB read + 5.91 MB written),
     # scaled to the 64-sequence workload by algorithmic bytes (4.3933e9 / 1.1181e9)
     "decode": {"file": "context_gqa_attention_gb300/csrc/decode.cu",
-               "sha1": "31b32a19d5725c80d520775a67b0090a375c7d0e", "bytes": 4425279389,
+               "sha1": "655e1e332d0a1f3ddfc3fe833fc0b4024140e3fb", "bytes": 4418570000,
                "workload": "decode"},
 }
 
