@@ -758,7 +758,7 @@ constexpr bool kPInTmem = true;
 
 template <int D, bool PT>
 struct Layout2 {
-  static constexpr int NSLOT = PT ? 5 : 3;
+  static constexpr int NSLOT = PT ? 4 : 3;  // 4 measured ~1.5% faster than 5 (P in TMEM)
   static constexpr int kQ = BM * D * 2;
   static constexpr int kKV = BN * D * 2;
   static constexpr int kP = BM * BN * 2;
@@ -845,7 +845,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (lane == 0) {
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      int last0 = -1, last1 = -1, last2 = -1;  // phase of the last fill of each slot
+      int lastph[NSLOT];  // parity of the last fill of each slot (-1: never filled)
+#pragma unroll
+      for (int i = 0; i < NSLOT; ++i) lastph[i] = -1;
       const int32_t* trow =
           p.mode == CP_PASS_Q ? p.tables + ((long long)w.p * p.B + w.b) * p.max_blocks : nullptr;
       int prow[BN / 16];  // pass-Q: element rows of the current tile's pages (K and V alike)
@@ -880,13 +882,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
               tma_load_2d(dst + kb * BN * 128 + j * 16 * 128, map, kb * 64, prow[j],
                           bar(Ly::bFull + slot));
         }
-        if (slot == 0) last0 = (int)ph; else if (slot == 1) last1 = (int)ph; else last2 = (int)ph;
+#pragma unroll
+        for (int k = 0; k < NSLOT; ++k)
+          if (k == slot) lastph[k] = (int)ph;
       }
       if (!ok) fail_timeout(abort_flag, p.err);
       mbar_wait(bar(Ly::bQ), 0u, nullptr, p.budget);
-      if (last0 >= 0) mbar_wait(bar(Ly::bFull + 0), (uint32_t)last0, nullptr, p.budget);
-      if (last1 >= 0) mbar_wait(bar(Ly::bFull + 1), (uint32_t)last1, nullptr, p.budget);
-      if (last2 >= 0) mbar_wait(bar(Ly::bFull + 2), (uint32_t)last2, nullptr, p.budget);
+#pragma unroll
+      for (int k = 0; k < NSLOT; ++k)
+        if (lastph[k] >= 0) mbar_wait(bar(Ly::bFull + k), (uint32_t)lastph[k], nullptr, p.budget);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
