@@ -39,9 +39,9 @@ import workloads as wl  # noqa: E402
 # each from one ncu capture summarised under profiles/.  A figure is reported only while the
 # kernel's source file still has the SHA-1 the capture was taken on; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # profiles/prefill_tc2_full_prefill.md: dram read 42.03 MB + write 62.33 MB
+    # profiles/prefill_tc2_full_prefill.md: dram read 42.04 MB + write 62.85 MB
     "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                "sha1": "2c98202c8af4deb6ae39b8b89e5b84fb5d41e4ce", "bytes": 104365312,
+                "sha1": "205aee9ddf47fa4436468e88db20c48e37cff1c9", "bytes": 104890624,
                 "workload": "full"},
     # profiles/decode_mma_decode.md: a 16-sequence capture (1.1186 GB read + 5.91 MB written),
     # scaled to the 64-sequence workload by algorithmic bytes (4.3933e9 / 1.1181e9)
@@ -264,8 +264,15 @@ class PrefillRunner:
         stream.wait_stream(self.s_out)
         t1.record(stream)
         torch.cuda.synchronize(dev)
+        self.e2e_last = self.outs_host[(steps - 1) % 2]
         self._use(self.sets[0])
         return t0.elapsed_time(t1) / 1e3
+
+    def e2e_check(self):
+        """The host copy of the last pipelined step equals a fresh device-only step."""
+        self.step()
+        torch.cuda.synchronize(self.dev)
+        return bool(torch.equal(self.out.cpu(), self.e2e_last))
 
     def e2e_bytes(self):
         h2d = sum(t.numel() * t.element_size() for t in self.host.values())
@@ -638,11 +645,14 @@ def main():
     elif isinstance(runner, PrefillRunner):
         runner.e2e_run(3, stream)
         e2e_s = max_over_ranks(runner.e2e_run(args.steps, stream), ws, dev)
+        if not runner.e2e_check():
+            raise RuntimeError("end-to-end output differs from the device-only step")
         h2d, d2h = runner.e2e_bytes()
         e2e = {"value": runner.metric(e2e_s / args.steps) * ws, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "pipelining": "inputs of step i+1 and output of step i-1 copied on two copy "
-                             "streams while step i computes (double-buffered device sets)"}
+                             "streams while step i computes (double-buffered device sets)",
+               "checked": "last host output == device-only step (bitwise)"}
         peak, src = pk["bf16"]
         achieved = runner.flops / dom_s / 1e12
         roof = {"bound": "tensor", "kernel": "cp_attn_prefill_fused (pass-KV, merged in-kernel)"

@@ -215,9 +215,10 @@ CP_DEV void merge_store(void* out, float* out_lse, long long u, int lane, const 
   if (out_lse && lane == 0) out_lse[u] = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
 }
 
-// Few partials (the prefill case): every LSE and output load is issued before any arithmetic,
-// one memory round trip per unit.  An empty partial's row is loaded but given weight 0 by a
-// select, so whatever its unwritten memory holds never reaches the result.
+// Few partials (the prefill case): the P LSEs of a unit are loaded together, then the rows of
+// the non-empty partials together (an empty partial's row is never read: in causal prefill
+// about one row in eight is empty, and measured, skipping those reads beats issuing every
+// load in one round trip).
 template <int D, bool BF16_OUT, int P>
 __global__ void __launch_bounds__(256) merge_small_kernel(const float* __restrict__ po,
                                                           const float* __restrict__ pl,
@@ -231,9 +232,13 @@ __global__ void __launch_bounds__(256) merge_small_kernel(const float* __restric
   float lp[P];
   V x[P];
 #pragma unroll
+  for (int p = 0; p < P; ++p) lp[p] = __ldg(pl + (long long)p * units + u) * kLog2e;
+#pragma unroll
   for (int p = 0; p < P; ++p) {
-    lp[p] = __ldg(pl + (long long)p * units + u) * kLog2e;
-    x[p] = __ldg(reinterpret_cast<const V*>(po + ((long long)p * units + u) * D + lane * E));
+    if (lp[p] > -INFINITY)
+      x[p] = __ldg(reinterpret_cast<const V*>(po + ((long long)p * units + u) * D + lane * E));
+    else
+      x[p] = V{};
   }
   float M = -INFINITY;
 #pragma unroll
