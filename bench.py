@@ -430,6 +430,36 @@ class DecodeRunner:
             ev[1].record()
         cpa.cp_lse_merge(self.part, self.plse, out=self.out, want_lse=False)
 
+    def e2e_run(self, steps, stream):
+        """Every step copies its per-step inputs from pinned host memory (new query tokens,
+        sequence lengths, block tables, cumulative lengths; the paged kv cache stays resident,
+        as it would in serving) and reads the merged output back.  Returns seconds."""
+        if not hasattr(self, "host"):
+            self.host = {n: t.cpu().pin_memory() for n, t in
+                         (("q", self.q), ("seq_lens", self.seq_lens), ("tables", self.tables),
+                          ("cu", self.cu))}
+            self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            for n in ("q", "seq_lens", "tables", "cu"):
+                getattr(self, n).copy_(self.host[n], non_blocking=True)
+            self.step()
+            self.out_host.copy_(self.out, non_blocking=True)
+        t1.record(stream)
+        torch.cuda.synchronize(self.dev)
+        return t0.elapsed_time(t1) / 1e3
+
+    def e2e_bytes(self):
+        h2d = sum(t.numel() * t.element_size() for t in self.host.values())
+        return h2d, self.out.numel() * self.out.element_size()
+
+    def e2e_check(self):
+        last = self.out_host.clone()
+        self.step()
+        torch.cuda.synchronize(self.dev)
+        return bool(torch.equal(self.out.cpu(), last))
+
     def metric(self, seconds):
         return self.bytes / seconds / 1e9
 
@@ -577,7 +607,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=256)
-    ap.add_argument("--cpu-rows", type=int, default=1024)
+    # cpu baseline: every query row of the full workload (~8-10 s of float64 oracle work)
+    ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--prefill-impl", default="auto", choices=["auto", "tcgen05", "simt"])
     ap.add_argument("--prefill-fused", action="store_true",
                     help="prefill as one launch (cp_attn_prefill_fused) instead of partials + merge")
@@ -666,7 +697,14 @@ def main():
                   else "causal GQA prefill TFLOP/s (pass-KV partial attention + LSE merge)")
         unit = "TFLOP/s"
     else:
-        e2e = None
+        runner.e2e_run(3, stream)
+        e2e_s = max_over_ranks(runner.e2e_run(args.steps, stream), ws, dev)
+        if not runner.e2e_check():
+            raise RuntimeError("end-to-end output differs from the device-only step")
+        h2d, d2h = runner.e2e_bytes()
+        e2e = {"value": runner.metric(e2e_s / args.steps) * ws, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "checked": "last host output == device-only step (bitwise)"}
         peak, src = pk["hbm"]
         achieved = runner.bytes / dom_s / 1e9
         roof = {"bound": "hbm", "kernel": "cp_partial_attn_decode", "achieved": achieved,
@@ -691,7 +729,8 @@ def main():
 
     if not args.no_secondary and w.kind != "decode":
         sec = {}
-        if isinstance(runner, PrefillRunner) and not isinstance(runner, PassQRunner):
+        if (isinstance(runner, PrefillRunner) and not isinstance(runner, PassQRunner)
+                and w.dtype == torch.bfloat16):  # the fused launch takes bf16
             # the same workload as one launch (cp_attn_prefill_fused): no partial round trip
             runner.fused = not runner.fused
             fs, fd, _ = time_steps(runner, max(10, args.steps // 2), 3, flush, dev, stream)
@@ -728,8 +767,10 @@ def main():
         f, t, n = oracle_sample(w, args.cpu_rows, 777)
         line["cpu_baseline"] = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
                                 "kind": "oracle",
-                                "sample": f"{n} stratified query rows x {w.num_q_heads} heads of the "
-                                          f"{w.name} workload, float64 NumPy oracle, {t:.1f} s"}
+                                "sample": (f"all {n} query rows" if n >= w.seq_len * w.num_seqs
+                                           else f"{n} stratified query rows")
+                                          + f" x {w.num_q_heads} heads of the {w.name} workload, "
+                                          f"float64 NumPy oracle, {t:.1f} s"}
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:

@@ -540,10 +540,11 @@ cp_status cp_decode_plan(int32_t num_seqs, int32_t num_kv_heads, int32_t cp, int
   const long long group = (long long)interleave * cp;
   long long rem = max_seq_len % group;
   const long long share = (max_seq_len / group) * interleave + (rem < interleave ? rem : interleave);
-  // target ~2048 local tokens per CTA (measured best between 1024 and 6144 on the 64-sequence
-  // decode workload) and at least ~8 CTAs per SM over 152 SMs in total
+  // target ~4096 local tokens per CTA (measured best between 512 and 6144 on the 64-sequence
+  // decode workload: fewer CTAs means fewer prologues, partials and, when fused, end-of-CTA
+  // fences) and at least ~8 CTAs per SM over 152 SMs in total
   const long long base = (long long)num_seqs * num_kv_heads * cp;
-  long long S = (share + 2047) / 2048;
+  long long S = (share + 4095) / 4096;
   const long long want = (8ll * 152 + base - 1) / base;
   if (S < want) S = want;
   const long long max_S = (share + block_size - 1) / block_size;

@@ -1,6 +1,8 @@
-"""The decode path (layout -> per-rank split partials -> merge) captured in a CUDA graph and
-replayed: same results as the eager calls, over several replays (the pages disable prefill CP
-under full CUDA graphs; this library's decode path is capturable)."""
+"""Hot paths captured in a CUDA graph and replayed: same results (bitwise) as the eager calls,
+over several replays.  The pages turn prefill CP off under full CUDA graphs; here the
+prefill path (partition -> partials -> merge, or the fused launch) and the decode path (layout
+-> split partials -> merge, or the fused launch with its self-resetting counters) are
+capturable: every call is stream-ordered and allocates nothing when its outputs are given."""
 import pytest
 import torch
 
@@ -9,13 +11,38 @@ import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-def test_decode_path_in_a_cuda_graph(lib):
+def _capture_and_replay(step, outs):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()                                  # eager warm-up (attributes, tensor maps)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    refs = [o.clone() for o in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        for o in outs:
+            o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for o, r in zip(outs, refs):
+            assert torch.equal(o, r)
+
+
+def _decode_setup(lib):
     B, Hq, Hkv, d, cp, I = 6, 32, 8, 128, 2, 8
     lens = wl.decode_lengths(B, 100, 5000, seed=71).tolist()
     x = wl.paged_inputs(B, 1, lens, Hq, Hkv, d, torch.bfloat16, cp, I, 16, 72, 73, q_is_decode=True)
     dev = {n: x[n].cuda() for n in ("q", "k_cache", "v_cache", "block_tables", "seq_lens")}
     cu = torch.tensor([0] + torch.tensor(lens).cumsum(0).tolist(), dtype=torch.int32, device="cuda")
     ns, st = lib.cp_decode_plan(B, Hkv, cp, I, 16, max(lens))
+    return B, Hq, Hkv, d, cp, I, lens, dev, cu, ns, st
+
+
+def test_decode_path_in_a_cuda_graph(lib):
+    B, Hq, Hkv, d, cp, I, lens, dev, cu, ns, st = _decode_setup(lib)
     part = torch.empty(cp * ns, B, Hq, d, device="cuda")
     plse = torch.empty(cp * ns, B, Hq, device="cuda")
     out = torch.empty(B, Hq, d, dtype=torch.bfloat16, device="cuda")
@@ -29,19 +56,49 @@ def test_decode_path_in_a_cuda_graph(lib):
                                    out=part, lse=plse)
         lib.cp_lse_merge(part, plse, out=out, out_lse=lse)
 
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        step()                                  # eager warm-up (attributes, tensor maps)
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    ref, ref_lse = out.clone(), lse.clone()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        step()
-    for _ in range(3):
-        out.zero_()
-        lse.zero_()
-        g.replay()
-        torch.cuda.synchronize()
-        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+    _capture_and_replay(step, [out, lse])
+
+
+def test_fused_decode_in_a_cuda_graph(lib):
+    """The arrival counters in the workspace return to zero after every launch, so the same
+    captured launch replays correctly."""
+    B, Hq, Hkv, d, cp, I, lens, dev, cu, ns, st = _decode_setup(lib)
+    ws = torch.zeros(lib.cp_decode_workspace_size(B, Hq, Hkv, d, cp, ns), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(B, Hq, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, Hq, device="cuda")
+
+    def step():
+        lib.cp_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_tables"],
+                                dev["seq_lens"], cp, I, num_splits=ns, split_tokens=st,
+                                workspace=ws, out=out, out_lse=lse)
+
+    _capture_and_replay(step, [out, lse])
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_prefill_path_in_a_cuda_graph(lib, fused):
+    lens, Hq, Hkv, d, cp = [1000, 2300], 8, 2, 128, 2
+    x = wl.prefill_inputs(lens, Hq, Hkv, d, torch.bfloat16, seed=74)
+    q, k, v, cu = (x[n].cuda() for n in ("q", "k", "v", "cu_seqlens"))
+    N = sum(lens)
+    perm = torch.empty(N, dtype=torch.int32, device="cuda")
+    inv = torch.empty(N, dtype=torch.int32, device="cuda")
+    so = torch.empty(cp + 1, dtype=torch.int32, device="cuda")
+    cb = torch.empty(len(lens), 2 * cp + 1, dtype=torch.int32, device="cuda")
+    part = torch.empty(cp, N, Hq, d, device="cuda")
+    plse = torch.empty(cp, N, Hq, device="cuda")
+    out = torch.empty(N, Hq, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(N, Hq, device="cuda")
+
+    def step():
+        lib.cp_partition(cu, cp, N, perm, inv, so, cb)
+        if fused:
+            lib.cp_attn_prefill_fused(q, cu, cp, k, v, max_seqlen_q=max(lens), out=out,
+                                      out_lse=lse)
+        else:
+            lib.cp_partial_attn_prefill(q, cu, cp, k=k, v=v, max_seqlen_q=max(lens), out=part,
+                                        lse=plse)
+            lib.cp_lse_merge(part, plse, out=out, out_lse=lse)
+
+    _capture_and_replay(step, [out, lse, perm])

@@ -185,6 +185,8 @@ def sample_rows(n_rows: int, chunk_starts, count: int, seed: int):
     (``chunk_starts`` lists chunk start rows, with the end as last entry); the rest is
     spread over the chunks in proportion to their size.
     """
+    if count >= n_rows:
+        return list(range(n_rows))
     g = torch.Generator().manual_seed(seed)
     keep = {0, n_rows - 1}
     for a, b in zip(chunk_starts[:-1], chunk_starts[1:]):
