@@ -105,6 +105,10 @@ cudaError_t cp_launch_decode(const cp_decode_args& a, float scale, cudaStream_t 
 bool cp_make_bf16_map_2d(void* map, const void* base, unsigned long long cols,
                          unsigned long long rows, unsigned long long pitch_elems,
                          unsigned box_rows);
+// 3D bf16 TMA descriptor over a paged pool of `rows` rows of d = 128 elements seen as
+// {64 columns, rows, 2 column halves}: one box {64, 16, 2} is a whole 16-row page, landing in
+// shared memory as [half][16 rows][128 bytes] (128-byte swizzle).  False if the driver refuses.
+bool cp_make_bf16_page_map(void* map, const void* base, unsigned long long rows);
 
 // Scratch of the fused decode: arrival counters [B][Hkv] (zero between calls), partial LSEs
 // [cp*S][B][Hq] and partial outputs [cp*S][B][Hq][d], each region 256-byte aligned.

@@ -41,6 +41,9 @@ struct DecodeParams {
   int32_t* counters;
   void* final_out;
   float* final_lse;
+  // d = 128 tensor-core path: 1 = the maps are whole-page 3D boxes (one copy per page of K and
+  // one of V), 0 = 2D boxes of 64 columns (two copies each)
+  int page_box;
 };
 
 template <typename T> struct Vec;
@@ -475,11 +478,16 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
               const int y = (int)((((long long)r * p.pool + id) * p.Hkv + g) * kPage);
               const uint32_t ks = slot(w, st);
               sm100::mbar_expect_tx(full(w, st), 2 * Ly::kPageBytes);
+              if (KB == 2 && p.page_box) {  // [half][16 rows][128 B], the layout read below
+                sm100::tma_load_3d(ks, &map_k, 0, y, 0, full(w, st));
+                sm100::tma_load_3d(ks + Ly::kPageBytes, &map_v, 0, y, 0, full(w, st));
+              } else {
 #pragma unroll
-              for (int kb = 0; kb < KB; ++kb) {
-                sm100::tma_load_2d(ks + kb * (kPage * 128), &map_k, kb * 64, y, full(w, st));
-                sm100::tma_load_2d(ks + Ly::kPageBytes + kb * (kPage * 128), &map_v, kb * 64, y,
-                                   full(w, st));
+                for (int kb = 0; kb < KB; ++kb) {
+                  sm100::tma_load_2d(ks + kb * (kPage * 128), &map_k, kb * 64, y, full(w, st));
+                  sm100::tma_load_2d(ks + Ly::kPageBytes + kb * (kPage * 128), &map_v, kb * 64, y,
+                                     full(w, st));
+                }
               }
             } else {  // a table entry outside the pool: the page is skipped and reported
               report(p.err, CP_ERR_DEVICE_BOUNDS);
@@ -662,14 +670,22 @@ cudaError_t launch_g(const DecodeParams& p, int G, dim3 grid, cudaStream_t s) {
 }
 
 template <bool F>
-cudaError_t launch_all(const DecodeParams& p, const cp_decode_args& a, dim3 grid, cudaStream_t s) {
+cudaError_t launch_all(const DecodeParams& p0, const cp_decode_args& a, dim3 grid, cudaStream_t s) {
   const int G = a.num_q_heads / a.num_kv_heads;
+  DecodeParams p = p0;
+  p.page_box = 0;
   if (a.dtype == CP_BF16) {  // tensor-core kernel with TMA-staged pages
     CUtensorMap mk, mv;
     const unsigned long long rows = (unsigned long long)a.cp * a.pool_pages * a.num_kv_heads * kPage;
-    if (!cp_make_bf16_map_2d(&mk, a.k_cache, a.head_dim, rows, a.head_dim, kPage) ||
-        !cp_make_bf16_map_2d(&mv, a.v_cache, a.head_dim, rows, a.head_dim, kPage))
+    // d = 128: one whole-page box per page of K and of V (half the copies of 64-column boxes;
+    // the copy engine's per-box cost bounds this kernel), else 64-column boxes
+    if (a.head_dim == 128 && cp_make_bf16_page_map(&mk, a.k_cache, rows) &&
+        cp_make_bf16_page_map(&mv, a.v_cache, rows)) {
+      p.page_box = 1;
+    } else if (!cp_make_bf16_map_2d(&mk, a.k_cache, a.head_dim, rows, a.head_dim, kPage) ||
+               !cp_make_bf16_map_2d(&mv, a.v_cache, a.head_dim, rows, a.head_dim, kPage)) {
       return cudaErrorInvalidValue;
+    }
     return a.head_dim == 64 ? launch_mma_g<64, F>(p, G, grid, mk, mv, s)
                             : launch_mma_g<128, F>(p, G, grid, mk, mv, s);
   }
@@ -699,6 +715,7 @@ DecodeParams make_params(const cp_decode_args& a, float scale) {
   p.counters = nullptr;
   p.final_out = nullptr;
   p.final_lse = nullptr;
+  p.page_box = 0;
   return p;
 }
 

@@ -54,6 +54,9 @@ struct TcParams {
   float* lse_final;
   // 1: the output tensor map is valid and full 32-row groups are written by TMA stores
   int tma_out;
+  // pass-Q, two-head kernel, d = 128: V pages arrive as whole-page boxes, page-major in the
+  // slot ([page][half][16 rows][128 B])
+  int page_v;
 };
 
 template <int D>
@@ -875,12 +878,18 @@ __global__ void __launch_bounds__(kThreads2, 1)
             page_rows(pid, t, w.n_local, p.pool, p.Hkv, w.p, w.g, p.err, prow);
             if (t + 1 < w.ntiles) fetch_page_ids(trow, t + 1, w.n_local, p.max_blocks, pid);
           }
+          if (isV && D == 128 && p.page_v) {
 #pragma unroll
-          for (int j = 0; j < BN / 16; ++j)
+            for (int j = 0; j < BN / 16; ++j)
+              tma_load_3d(dst + j * 4096, map, 0, prow[j], 0, bar(Ly::bFull + slot));
+          } else {
 #pragma unroll
-            for (int kb = 0; kb < KB; ++kb)
-              tma_load_2d(dst + kb * BN * 128 + j * 16 * 128, map, kb * 64, prow[j],
-                          bar(Ly::bFull + slot));
+            for (int j = 0; j < BN / 16; ++j)
+#pragma unroll
+              for (int kb = 0; kb < KB; ++kb)
+                tma_load_2d(dst + kb * BN * 128 + j * 16 * 128, map, kb * 64, prow[j],
+                            bar(Ly::bFull + slot));
+          }
         }
 #pragma unroll
         for (int k = 0; k < NSLOT; ++k)
@@ -913,7 +922,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint32_t dO = tmem + 256u + (uint32_t)(tile * D);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
+          // 16 keys = one page: page-major slot (halves 2 KB apart) or the tiled layout
+          const uint64_t bd = p.page_v ? desc_sw128(v + kk * 4096, 2048, 1024)
+                                       : desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
           if constexpr (PT) {  // P: 8 packed columns per 16 keys
             mma_ts(dO, tmem + (uint32_t)(tile * BN + kk * 8), bd, id_pv, (acc || kk > 0) ? 1u : 0u);
           } else {
@@ -1123,12 +1134,21 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
     const unsigned long long hd = (unsigned long long)a.num_kv_heads * D;
     if (!make_map(&mk, a.k, hd, Nq, hd, BN) || !make_map(&mv, a.v, hd, Nq, hd, BN))
       return cudaErrorInvalidValue;
-  } else {
+  }
+  // two heads per CTA when the heads of a kv group pair up, unless one head per CTA is forced
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const bool pair = (G % 2 == 0) && a.impl != CP_IMPL_TCGEN05_SINGLE;
+  int page_v = 0;
+  if (a.mode != CP_PASS_KV) {
     const unsigned long long rows = (unsigned long long)a.cp * a.pool_pages * a.num_kv_heads * 16;
-    if (!make_map(&mk, a.k_cache, D, rows, D, 16) || !make_map(&mv, a.v_cache, D, rows, D, 16))
-      return cudaErrorInvalidValue;
+    if (!make_map(&mk, a.k_cache, D, rows, D, 16)) return cudaErrorInvalidValue;
+    // pass-Q V of the two-head kernel at d = 128: one whole-page box per page (the PV MMA reads
+    // the page-major layout); K stays in 64-column boxes (its K-major operand needs them)
+    if (pair && D == 128 && cp_make_bf16_page_map(&mv, a.v_cache, rows)) page_v = 1;
+    else if (!make_map(&mv, a.v_cache, D, rows, D, 16)) return cudaErrorInvalidValue;
   }
   TcParams p;
+  p.page_v = page_v;
   p.mode = a.mode;
   p.B = a.num_seqs;
   p.Hq = a.num_q_heads;
@@ -1158,9 +1178,6 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   std::memset(&mo, 0, sizeof(mo));
   p.tma_out = p.fused ? make_out_map(&mo, fused_out, true, D, a.num_q_heads, Nq)
                       : make_out_map(&mo, a.out, false, D, a.num_q_heads, (unsigned long long)a.cp * Nq);
-  // two heads per CTA when the heads of a kv group pair up, unless one head per CTA is forced
-  const int G = a.num_q_heads / a.num_kv_heads;
-  const bool pair = (G % 2 == 0) && a.impl != CP_IMPL_TCGEN05_SINGLE;
   const long long grid = (long long)2 * a.cp * p.TPC * a.num_seqs *
                          ((a.kv_shard >= 0 || p.fused) ? 1 : a.cp) * (a.num_q_heads / (pair ? 2 : 1));
   if (grid == 0) return cudaSuccess;
@@ -1188,6 +1205,19 @@ bool cp_make_bf16_map_2d(void* map, const void* base, unsigned long long cols,
                          unsigned long long rows, unsigned long long pitch_elems,
                          unsigned box_rows) {
   return cpattn::make_map(static_cast<CUtensorMap*>(map), base, cols, rows, pitch_elems, box_rows);
+}
+
+bool cp_make_bf16_page_map(void* map, const void* base, unsigned long long rows) {
+  cpattn::EncodeTiledFn fn = cpattn::encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {64, rows, 2};
+  cuuint64_t strides[2] = {128 * 2, 128};  // next row; the second 64-column half
+  cuuint32_t box[3] = {64, 16, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool cp_prefill_tc_supported(const cp_prefill_args& a) {

@@ -88,6 +88,15 @@ SM100_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "m
 // Waits until every committed bulk store of this thread has finished reading shared memory.
 SM100_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
+// 3D tiled bulk copy global -> shared completing on an mbarrier (same rules as the 2D form).
+SM100_DEV void tma_load_3d(uint32_t dst, const void* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
 // 1D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16) completing on an
 // mbarrier.
 SM100_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
