@@ -109,6 +109,10 @@ bool cp_make_bf16_map_2d(void* map, const void* base, unsigned long long cols,
 // {64 columns, rows, 2 column halves}: one box {64, 16, 2} is a whole 16-row page, landing in
 // shared memory as [half][16 rows][128 bytes] (128-byte swizzle).  False if the driver refuses.
 bool cp_make_bf16_page_map(void* map, const void* base, unsigned long long rows);
+// 4D variant for MMA operands: {64 columns, 8 rows, 2 halves, rows / 8 row groups}, box
+// {64, 8, 2, 2} = one 16-row page landing as [row group][half][8 rows][128 bytes], so that
+// consecutive 8-row groups of consecutive pages sit a uniform 2 KB apart.
+bool cp_make_bf16_page_map4(void* map, const void* base, unsigned long long rows);
 
 // Scratch of the fused decode: arrival counters [B][Hkv] (zero between calls), partial LSEs
 // [cp*S][B][Hq] and partial outputs [cp*S][B][Hq][d], each region 256-byte aligned.

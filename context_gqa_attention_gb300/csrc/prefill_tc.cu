@@ -54,9 +54,9 @@ struct TcParams {
   float* lse_final;
   // 1: the output tensor map is valid and full 32-row groups are written by TMA stores
   int tma_out;
-  // pass-Q, two-head kernel, d = 128: V pages arrive as whole-page boxes, page-major in the
-  // slot ([page][half][16 rows][128 B])
-  int page_v;
+  // pass-Q, two-head kernel, d = 128: K and V pages arrive as whole-page boxes laid out
+  // [page][row group][half][8 rows][128 B] in the slot
+  int page_kv;
 };
 
 template <int D>
@@ -878,10 +878,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
             page_rows(pid, t, w.n_local, p.pool, p.Hkv, w.p, w.g, p.err, prow);
             if (t + 1 < w.ntiles) fetch_page_ids(trow, t + 1, w.n_local, p.max_blocks, pid);
           }
-          if (isV && D == 128 && p.page_v) {
+          if (D == 128 && p.page_kv) {
 #pragma unroll
             for (int j = 0; j < BN / 16; ++j)
-              tma_load_3d(dst + j * 4096, map, 0, prow[j], 0, bar(Ly::bFull + slot));
+              tma_load_4d(dst + j * 4096, map, 0, 0, 0, prow[j] >> 3, bar(Ly::bFull + slot));
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 16; ++j)
@@ -912,9 +912,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offq = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-          const uint32_t offk = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-          mma_ss(dS, desc_sw128(q + offq, 16, 1024), desc_sw128(k + offk, 16, 1024), id_qk,
-                 kk > 0 ? 1u : 0u);
+          // paged slot: 64-column block at +1 KB, 8-key groups 2 KB apart; tiled: block at
+          // +BN x 128 B, groups 1 KB apart
+          const uint32_t offk = (kk / 4) * (p.page_kv ? 1024u : (uint32_t)(BN * 128)) + (kk % 4) * 32;
+          mma_ss(dS, desc_sw128(q + offq, 16, 1024),
+                 desc_sw128(k + offk, 16, p.page_kv ? 2048u : 1024u), id_qk, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int tile, int slot, bool acc) {
@@ -922,9 +924,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint32_t dO = tmem + 256u + (uint32_t)(tile * D);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          // 16 keys = one page: page-major slot (halves 2 KB apart) or the tiled layout
-          const uint64_t bd = p.page_v ? desc_sw128(v + kk * 4096, 2048, 1024)
-                                       : desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
+          // 16 keys = one page: paged slot (halves 1 KB apart, 8-key groups 2 KB apart) or
+          // the tiled layout (halves BN x 128 B apart, groups 1 KB apart)
+          const uint64_t bd = p.page_kv ? desc_sw128(v + kk * 4096, 1024, 2048)
+                                        : desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
           if constexpr (PT) {  // P: 8 packed columns per 16 keys
             mma_ts(dO, tmem + (uint32_t)(tile * BN + kk * 8), bd, id_pv, (acc || kk > 0) ? 1u : 0u);
           } else {
@@ -1138,17 +1141,22 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   // two heads per CTA when the heads of a kv group pair up, unless one head per CTA is forced
   const int G = a.num_q_heads / a.num_kv_heads;
   const bool pair = (G % 2 == 0) && a.impl != CP_IMPL_TCGEN05_SINGLE;
-  int page_v = 0;
+  int page_kv = 0;
   if (a.mode != CP_PASS_KV) {
     const unsigned long long rows = (unsigned long long)a.cp * a.pool_pages * a.num_kv_heads * 16;
-    if (!make_map(&mk, a.k_cache, D, rows, D, 16)) return cudaErrorInvalidValue;
-    // pass-Q V of the two-head kernel at d = 128: one whole-page box per page (the PV MMA reads
-    // the page-major layout); K stays in 64-column boxes (its K-major operand needs them)
-    if (pair && D == 128 && cp_make_bf16_page_map(&mv, a.v_cache, rows)) page_v = 1;
-    else if (!make_map(&mv, a.v_cache, D, rows, D, 16)) return cudaErrorInvalidValue;
+    // pass-Q, two-head kernel, d = 128: one whole-page box per page of K and of V (a quarter
+    // of the copies of 64-column x 16-row boxes; the copy engine's per-box cost bounded this
+    // path); else 64-column boxes
+    if (pair && D == 128 && cp_make_bf16_page_map4(&mk, a.k_cache, rows) &&
+        cp_make_bf16_page_map4(&mv, a.v_cache, rows)) {
+      page_kv = 1;
+    } else if (!make_map(&mk, a.k_cache, D, rows, D, 16) ||
+               !make_map(&mv, a.v_cache, D, rows, D, 16)) {
+      return cudaErrorInvalidValue;
+    }
   }
   TcParams p;
-  p.page_v = page_v;
+  p.page_kv = page_kv;
   p.mode = a.mode;
   p.B = a.num_seqs;
   p.Hq = a.num_q_heads;
@@ -1205,6 +1213,19 @@ bool cp_make_bf16_map_2d(void* map, const void* base, unsigned long long cols,
                          unsigned long long rows, unsigned long long pitch_elems,
                          unsigned box_rows) {
   return cpattn::make_map(static_cast<CUtensorMap*>(map), base, cols, rows, pitch_elems, box_rows);
+}
+
+bool cp_make_bf16_page_map4(void* map, const void* base, unsigned long long rows) {
+  cpattn::EncodeTiledFn fn = cpattn::encode_fn();
+  if (fn == nullptr || rows % 8 != 0) return false;
+  cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+  cuuint64_t strides[3] = {128 * 2, 128, 8 * 128 * 2};  // next row; second half; next 8 rows
+  cuuint32_t box[4] = {64, 8, 2, 2};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool cp_make_bf16_page_map(void* map, const void* base, unsigned long long rows) {

@@ -97,6 +97,15 @@ SM100_DEV void tma_load_3d(uint32_t dst, const void* map, int x, int y, int z, u
       : "memory");
 }
 
+// 4D tiled bulk copy global -> shared completing on an mbarrier.
+SM100_DEV void tma_load_4d(uint32_t dst, const void* map, int x, int y, int z, int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
 // 1D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16) completing on an
 // mbarrier.
 SM100_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
