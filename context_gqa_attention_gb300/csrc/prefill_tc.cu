@@ -54,9 +54,6 @@ struct TcParams {
   float* lse_final;
   // 1: the output tensor map is valid and full 32-row groups are written by TMA stores
   int tma_out;
-  // pass-Q, two-head kernel, d = 128: K and V pages arrive as whole-page boxes laid out
-  // [page][row group][half][8 rows][128 B] in the slot
-  int page_kv;
 };
 
 template <int D>
@@ -777,7 +774,7 @@ struct Layout2 {
   static_assert(kAlloc <= 232448, "dynamic shared memory beyond the 227 KB per-CTA limit");
 };
 
-template <int D, bool PT>
+template <int D, bool PT, bool PG>  // PG: paged K/V as whole-page boxes (pass-Q, d = 128)
 __global__ void __launch_bounds__(kThreads2, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -878,7 +875,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             page_rows(pid, t, w.n_local, p.pool, p.Hkv, w.p, w.g, p.err, prow);
             if (t + 1 < w.ntiles) fetch_page_ids(trow, t + 1, w.n_local, p.max_blocks, pid);
           }
-          if (D == 128 && p.page_kv) {
+          if constexpr (PG) {
 #pragma unroll
             for (int j = 0; j < BN / 16; ++j)
               tma_load_4d(dst + j * 4096, map, 0, 0, 0, prow[j] >> 3, bar(Ly::bFull + slot));
@@ -914,9 +911,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
           const uint32_t offq = (kk / 4) * (BM * 128) + (kk % 4) * 32;
           // paged slot: 64-column block at +1 KB, 8-key groups 2 KB apart; tiled: block at
           // +BN x 128 B, groups 1 KB apart
-          const uint32_t offk = (kk / 4) * (p.page_kv ? 1024u : (uint32_t)(BN * 128)) + (kk % 4) * 32;
-          mma_ss(dS, desc_sw128(q + offq, 16, 1024),
-                 desc_sw128(k + offk, 16, p.page_kv ? 2048u : 1024u), id_qk, kk > 0 ? 1u : 0u);
+          const uint32_t offk = (kk / 4) * (PG ? 1024u : (uint32_t)(BN * 128)) + (kk % 4) * 32;
+          mma_ss(dS, desc_sw128(q + offq, 16, 1024), desc_sw128(k + offk, 16, PG ? 2048u : 1024u),
+                 id_qk, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int tile, int slot, bool acc) {
@@ -926,8 +923,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
         for (int kk = 0; kk < BN / 16; ++kk) {
           // 16 keys = one page: paged slot (halves 1 KB apart, 8-key groups 2 KB apart) or
           // the tiled layout (halves BN x 128 B apart, groups 1 KB apart)
-          const uint64_t bd = p.page_kv ? desc_sw128(v + kk * 4096, 1024, 2048)
-                                        : desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
+          const uint64_t bd = PG ? desc_sw128(v + kk * 4096, 1024, 2048)
+                                 : desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
           if constexpr (PT) {  // P: 8 packed columns per 16 keys
             mma_ts(dO, tmem + (uint32_t)(tile * BN + kk * 8), bd, id_pv, (acc || kk > 0) ? 1u : 0u);
           } else {
@@ -1156,7 +1153,6 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
     }
   }
   TcParams p;
-  p.page_kv = page_kv;
   p.mode = a.mode;
   p.B = a.num_seqs;
   p.Hq = a.num_q_heads;
@@ -1193,10 +1189,13 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   cudaError_t e;
   if (pair) {
     const int smem = Layout2<D, kPInTmem>::kAlloc;
-    e = cudaFuncSetAttribute(prefill_tc2_kernel<D, kPInTmem>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // pass-Q at d = 128 (page_kv): K and V pages arrive as whole-page boxes laid out
+    // [page][row group][half][8 rows][128 B] in the slot
+    auto kern = page_kv ? prefill_tc2_kernel<D, kPInTmem, (D == 128)>
+                        : prefill_tc2_kernel<D, kPInTmem, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    prefill_tc2_kernel<D, kPInTmem><<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, mo, p);
+    kern<<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, mo, p);
   } else {
     const int smem = Layout<D>::kAlloc;
     e = cudaFuncSetAttribute(prefill_tc1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
