@@ -39,14 +39,14 @@ import workloads as wl  # noqa: E402
 # each from one ncu capture summarised under profiles/.  A figure is reported only while the
 # kernel's source file still has the SHA-1 the capture was taken on; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # profiles/prefill_tc2_full_prefill.md: dram read 42.04 MB + write 62.85 MB
+    # profiles/prefill_tc2_full_prefill.md: dram read 42.03 MB + write 62.49 MB
     "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                "sha1": "205aee9ddf47fa4436468e88db20c48e37cff1c9", "bytes": 104890624,
+                "sha1": "42181699a6fdc7a50284337b0f71d2c6a20ca6ea", "bytes": 104521472,
                 "workload": "full"},
-    # profiles/decode_mma_decode.md: a 16-sequence capture (1.1186 GB read + 5.91 MB written),
+    # profiles/decode_mma_decode.md: a 16-sequence capture (1.1187 GB read + 5.28 MB written),
     # scaled to the 64-sequence workload by algorithmic bytes (4.3933e9 / 1.1181e9)
     "decode": {"file": "context_gqa_attention_gb300/csrc/decode.cu",
-               "sha1": "655e1e332d0a1f3ddfc3fe833fc0b4024140e3fb", "bytes": 4418570000,
+               "sha1": "933f13647945ffea306dd32d47393f3451c3ae50", "bytes": 4416280000,
                "workload": "decode"},
 }
 
