@@ -77,6 +77,7 @@ _LIB = None
 _SIGS = [
     ("cp_status_string", ctypes.c_char_p, [ctypes.c_int32]),
     ("cp_last_error", ctypes.c_int32, [ctypes.c_char_p, ctypes.c_size_t]),
+    ("cp_last_error_detail", ctypes.c_int32, [ctypes.c_char_p, ctypes.c_size_t]),
     ("cp_abi_version", ctypes.c_int32, []),
     ("cp_prefill_args_size", ctypes.c_size_t, []),
     ("cp_decode_args_size", ctypes.c_size_t, []),

@@ -338,6 +338,8 @@ int32_t cp_last_error(char* buf, size_t n) {
   return g_status;
 }
 
+int32_t cp_last_error_detail(char* buf, size_t n) { return cp_last_error(buf, n); }
+
 int32_t cp_abi_version(void) { return CPATTN_ABI_VERSION; }
 size_t cp_prefill_args_size(void) { return sizeof(cp_prefill_args); }
 size_t cp_decode_args_size(void) { return sizeof(cp_decode_args); }

@@ -75,6 +75,8 @@ const char* cp_status_string(int32_t status);
 /* Copies the reason for the calling thread's last failed call into buf (NUL-
  * terminated, truncated to n bytes) and returns that call's status. */
 int32_t cp_last_error(char* buf, size_t n);
+/* The same call under its longer name. */
+int32_t cp_last_error_detail(char* buf, size_t n);
 
 /* CPATTN_ABI_VERSION of the loaded library. */
 int32_t cp_abi_version(void);

@@ -105,7 +105,8 @@ PASS_KV_CASES = [
     ([515], 4, 4, 64, torch.bfloat16, 3),
     ([300, 5], 8, 1, 128, torch.bfloat16, 8),
     ([640], 8, 2, 128, torch.float32, 1),
-    ([4096], 16, 2, 128, torch.bfloat16, 2),      # ~512 work items: several per persistent CTA
+    ([4096], 16, 2, 128, torch.bfloat16, 2),      # ~512 work items: several waves of CTAs
+    ([777, 64], 8, 2, 64, torch.bfloat16, 2),     # two-head kernel at d = 64, ragged tiles
 ]
 
 
@@ -384,7 +385,7 @@ def test_kv_cache_write_reports_missing_page(lib):
 
 # ------------------------------------------------------------------------------------ fused prefill
 
-@pytest.mark.parametrize("case", [1, 2, 3, 4, 6])
+@pytest.mark.parametrize("case", [1, 2, 3, 4, 6, 7])
 def test_fused_prefill_parity(lib, case):
     """cp_attn_prefill_fused = merged pass-KV partials = plain causal attention."""
     lens, Hq, Hkv, d, dt, cp = PASS_KV_CASES[case]
