@@ -219,44 +219,59 @@ CP_DEV void merge_store(void* out, float* out_lse, long long u, int lane, const 
 // the non-empty partials together (an empty partial's row is never read: in causal prefill
 // about one row in eight is empty, and measured, skipping those reads beats issuing every
 // load in one round trip).
+// (row, head) units per warp in merge_small_kernel: 2 measured best (1: 4 µs slower on the
+// full prefill's merge, 4: 2 µs slower)
+constexpr int kMergeUnits = 2;
+
 template <int D, bool BF16_OUT, int P>
 __global__ void __launch_bounds__(256) merge_small_kernel(const float* __restrict__ po,
                                                           const float* __restrict__ pl,
                                                           long long units, void* out,
                                                           float* out_lse) {
-  constexpr int E = D / 32;
+  constexpr int E = D / 32, U = kMergeUnits;
   using V = typename MergeVec<D>::T;
-  const long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  // U units per warp, every load of all of them issued before any arithmetic (twice the
+  // bytes in flight of one unit per warp)
+  const long long u0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * U;
   const int lane = threadIdx.x & 31;
-  if (u >= units) return;
-  float lp[P];
-  V x[P];
+  if (u0 >= units) return;
+  float lp[U][P];
+  V x[U][P];
 #pragma unroll
-  for (int p = 0; p < P; ++p) lp[p] = __ldg(pl + (long long)p * units + u) * kLog2e;
+  for (int j = 0; j < U; ++j)
 #pragma unroll
-  for (int p = 0; p < P; ++p) {
-    if (lp[p] > -INFINITY)
-      x[p] = __ldg(reinterpret_cast<const V*>(po + ((long long)p * units + u) * D + lane * E));
-    else
-      x[p] = V{};
-  }
-  float M = -INFINITY;
+    for (int p = 0; p < P; ++p)
+      lp[j][p] = u0 + j < units ? __ldg(pl + (long long)p * units + u0 + j) * kLog2e : -INFINITY;
 #pragma unroll
-  for (int p = 0; p < P; ++p) M = fmaxf(M, lp[p]);
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M > -INFINITY) {
+  for (int j = 0; j < U; ++j)
 #pragma unroll
     for (int p = 0; p < P; ++p) {
-      const bool live = lp[p] > -INFINITY;
-      const float w = live ? exp2f(lp[p] - M) : 0.f;
-      wsum += w;
-      if (live) MergeVec<D>::fma(acc, w, x[p]);
+      if (lp[j][p] > -INFINITY)
+        x[j][p] = __ldg(reinterpret_cast<const V*>(po + ((long long)p * units + u0 + j) * D + lane * E));
+      else
+        x[j][p] = V{};
     }
+#pragma unroll
+  for (int j = 0; j < U; ++j) {
+    if (u0 + j >= units) break;
+    float M = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < P; ++p) M = fmaxf(M, lp[j][p]);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    if (M > -INFINITY) {
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        const bool live = lp[j][p] > -INFINITY;
+        const float w = live ? exp2f(lp[j][p] - M) : 0.f;
+        wsum += w;
+        if (live) MergeVec<D>::fma(acc, w, x[j][p]);
+      }
+    }
+    merge_store<D, BF16_OUT>(out, out_lse, u0 + j, lane, acc, wsum, M);
   }
-  merge_store<D, BF16_OUT>(out, out_lse, u, lane, acc, wsum, M);
 }
 
 // Any number of partials (the decode case, cp x splits): LSEs read 32 at a time across the
@@ -443,13 +458,14 @@ cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32
   REQUIRE(blocks < (1ll << 31), "too many rows");
   cudaStream_t s = as_stream(stream);
   const unsigned nb = (unsigned)blocks;
+  const unsigned nbs = (unsigned)((units + 8ll * cpattn::kMergeUnits - 1) / (8ll * cpattn::kMergeUnits));
 #define CP_MERGE_SMALL(D, BF)                                                                 \
   switch (num_partials) {                                                                   \
-    case 1: cpattn::merge_small_kernel<D, BF, 1><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
-    case 2: cpattn::merge_small_kernel<D, BF, 2><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
-    case 3: cpattn::merge_small_kernel<D, BF, 3><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
-    case 4: cpattn::merge_small_kernel<D, BF, 4><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
-    case 8: cpattn::merge_small_kernel<D, BF, 8><<<nb, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    case 1: cpattn::merge_small_kernel<D, BF, 1><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    case 2: cpattn::merge_small_kernel<D, BF, 2><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    case 3: cpattn::merge_small_kernel<D, BF, 3><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    case 4: cpattn::merge_small_kernel<D, BF, 4><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
+    case 8: cpattn::merge_small_kernel<D, BF, 8><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
     default: cpattn::merge_kernel<D, BF><<<nb, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse); \
   }
   if (head_dim == 128) {
