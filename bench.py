@@ -156,6 +156,23 @@ def causal_pairs_pass_kv(lens):
     return sum(T * (T + 1) // 2 for T in lens)
 
 
+def run_with_side_maps(runner, maps, attention):
+    """One step: the map kernels (`maps`) on a side stream, concurrent with the attention
+    kernels (`attention`) on the current stream, which derive their chunk bounds / rank
+    lengths themselves; the side stream is joined before the step ends."""
+    main = torch.cuda.current_stream(runner.dev)
+    if getattr(runner, "s_side", None) is None:
+        runner.s_side = torch.cuda.Stream(runner.dev)
+    side = runner.s_side
+    side.wait_stream(main)
+    with torch.cuda.stream(side):
+        maps()
+    try:
+        attention()
+    finally:
+        main.wait_stream(side)
+
+
 class PrefillRunner:
     """pass-KV prefill: partition -> partial attention -> merge."""
 
@@ -187,7 +204,13 @@ class PrefillRunner:
 
     def step(self, ev=None):
         cpa, w = self.cpa, self.w
-        cpa.cp_partition(self.cu, w.cp, self.N, self.perm, self.inv, self.so, self.cb)
+        run_with_side_maps(
+            self, lambda: cpa.cp_partition(self.cu, w.cp, self.N, self.perm, self.inv, self.so,
+                                           self.cb),
+            lambda: self._attention(ev))
+
+    def _attention(self, ev=None):
+        cpa, w = self.cpa, self.w
         if self.fused:  # every kv shard walked inside one item: final output, no partials
             if ev is not None:
                 ev[0].record()
@@ -328,9 +351,16 @@ class PassQRunner:
 
     def step(self, ev=None):
         cpa, w = self.cpa, self.w
-        cpa.cp_partition(self.cu_q, w.cp, self.N, self.perm, self.inv, self.so, self.cb)
-        cpa.cp_kv_interleave_layout(self.cu_kv, w.cp, w.interleave, 0, w.block_size,
-                                    local_lens=self.local_lens, want_slots=False)
+
+        def maps():
+            cpa.cp_partition(self.cu_q, w.cp, self.N, self.perm, self.inv, self.so, self.cb)
+            cpa.cp_kv_interleave_layout(self.cu_kv, w.cp, w.interleave, 0, w.block_size,
+                                        local_lens=self.local_lens, want_slots=False)
+
+        run_with_side_maps(self, maps, lambda: self._attention(ev))
+
+    def _attention(self, ev=None):
+        cpa, w = self.cpa, self.w
         if ev is not None:
             ev[0].record()
         cpa.cp_partial_attn_prefill(self.q, self.cu_q, w.cp, mode=cpa.CP_PASS_Q, k_cache=self.kc,
@@ -412,8 +442,13 @@ class DecodeRunner:
 
     def step(self, ev=None):
         cpa, w = self.cpa, self.w
-        cpa.cp_kv_interleave_layout(self.cu, w.cp, w.interleave, 0, w.block_size,
-                                    local_lens=self.local_lens, want_slots=False)
+        run_with_side_maps(
+            self, lambda: cpa.cp_kv_interleave_layout(self.cu, w.cp, w.interleave, 0, w.block_size,
+                                                      local_lens=self.local_lens, want_slots=False),
+            lambda: self._attention(ev))
+
+    def _attention(self, ev=None):
+        cpa, w = self.cpa, self.w
         if ev is not None:
             ev[0].record()
         if self.fused:  # partials + merge in one launch
