@@ -529,9 +529,11 @@ def time_steps(runner, steps, warmup, flush, dev, stream, dominant=True, stretch
     for i in range(steps):
         for _ in range(1 + extra):
             flush.zero_()
+        torch.cuda.nvtx.range_push(f"{type(runner).__name__} step {i}")  # profiler timelines
         starts[i].record(stream)
         runner.step(dom[i])
         ends[i].record(stream)
+        torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     t1 = time.time()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
