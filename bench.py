@@ -69,6 +69,20 @@ def ncu_traffic(kind, workload):
     return rec["bytes"]
 
 
+def source_sha1():
+    """SHA-1 over the library's sources (kernels, host code, header): names the exact build a
+    line was measured on (the GPU machine's copy of the tree has no git metadata)."""
+    import glob
+    import hashlib
+    h = hashlib.sha1()
+    files = sorted(glob.glob(os.path.join(ROOT, "context_gqa_attention_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "cpattn.h"))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -655,6 +669,9 @@ def main():
                     help="override the decode plan's rank-local tokens per split (multiple of 16)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's number of sequences (smaller profiling cases)")
+    ap.add_argument("--cp", type=int, default=0, help="override the number of logical CP ranks")
+    ap.add_argument("--interleave", type=int, default=0, help="override the interleave size")
+    ap.add_argument("--seed", type=int, default=-1, help="override the value seed")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -671,6 +688,12 @@ def main():
     w = wl.WORKLOADS[args.workload]
     if args.batch > 0:
         w = dataclasses.replace(w, num_seqs=args.batch)
+    if args.cp > 0:
+        w = dataclasses.replace(w, cp=args.cp)
+    if args.interleave > 0:
+        w = dataclasses.replace(w, interleave=args.interleave)
+    if args.seed >= 0:
+        w = dataclasses.replace(w, seed=args.seed)
     runner = (DecodeRunner(w, dev, cpa) if w.kind == "decode" else
               PassQRunner(w, dev, cpa) if w.kind == "pass_q" else PrefillRunner(w, dev, cpa))
     if isinstance(runner, DecodeRunner):
@@ -760,7 +783,8 @@ def main():
             "config": dict(runner.config(), l2="flushed between timed steps (512 MB write)",
                            parallelism=f"replicas x{ws} (logical CP shards on each GPU)"),
             "roofline": roof, "clocks": clk,
-            "gpu_launches": runner.launches_per_step * args.steps}
+            "gpu_launches": runner.launches_per_step * args.steps,
+            "source_sha1": source_sha1()}
     if e2e is not None:
         line["e2e"] = e2e
 
