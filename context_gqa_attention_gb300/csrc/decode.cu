@@ -648,10 +648,14 @@ cudaError_t launch_mma_g(const DecodeParams& p, int G, dim3 grid, const CUtensor
     kern<<<grid, (kCW + 1) * 32, smem, s>>>(mk, mv, p);
     return cudaGetLastError();
   };
-  switch (G) {
+  switch (G) {  // query heads per kv head = MMA rows in use (of 8)
     case 1: return go(decode_mma_kernel<D, 1, F>);
     case 2: return go(decode_mma_kernel<D, 2, F>);
+    case 3: return go(decode_mma_kernel<D, 3, F>);
     case 4: return go(decode_mma_kernel<D, 4, F>);
+    case 5: return go(decode_mma_kernel<D, 5, F>);
+    case 6: return go(decode_mma_kernel<D, 6, F>);
+    case 7: return go(decode_mma_kernel<D, 7, F>);
     case 8: return go(decode_mma_kernel<D, 8, F>);
     default: return cudaErrorInvalidValue;
   }
@@ -662,7 +666,11 @@ cudaError_t launch_g(const DecodeParams& p, int G, dim3 grid, cudaStream_t s) {
   switch (G) {
     case 1: decode_kernel<T, D, 1, F><<<grid, kWarps * 32, 0, s>>>(p); break;
     case 2: decode_kernel<T, D, 2, F><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 3: decode_kernel<T, D, 3, F><<<grid, kWarps * 32, 0, s>>>(p); break;
     case 4: decode_kernel<T, D, 4, F><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 5: decode_kernel<T, D, 5, F><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 6: decode_kernel<T, D, 6, F><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 7: decode_kernel<T, D, 7, F><<<grid, kWarps * 32, 0, s>>>(p); break;
     case 8: decode_kernel<T, D, 8, F><<<grid, kWarps * 32, 0, s>>>(p); break;
     default: return cudaErrorInvalidValue;
   }

@@ -228,6 +228,9 @@ DECODE_CASES = [
     (3, (1, 40), 16, 2, 64, torch.bfloat16, 4, 8),
     (7, (500, 900), 8, 8, 128, torch.float32, 3, 4),
     (2, (1000, 2000), 16, 16, 64, torch.bfloat16, 1, 8),
+    (4, (100, 2500), 28, 4, 128, torch.bfloat16, 2, 8),   # G = 7
+    (3, (50, 700), 15, 5, 64, torch.bfloat16, 3, 16),     # G = 3
+    (2, (200, 900), 10, 2, 128, torch.float32, 2, 8),     # G = 5, CUDA-core kernel
 ]
 
 
