@@ -827,6 +827,8 @@ def main():
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and w.kind == "pass_kv":
         f, t, n = oracle_sample(w, args.cpu_rows, 777)
         line["cpu_baseline"] = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
+                                "cpu_count": os.cpu_count(), "seconds": t,
+                                "rows_per_s": n * w.num_q_heads / t,
                                 "kind": "oracle",
                                 "sample": (f"all {n} query rows" if n >= w.seq_len * w.num_seqs
                                            else f"{n} stratified query rows")
