@@ -629,8 +629,9 @@ static cp_status check_decode_args(const cp_decode_args* a, bool need_partials) 
   REQUIRE(a->num_kv_heads >= 1 && a->num_q_heads % a->num_kv_heads == 0,
           "num_q_heads must be a multiple of num_kv_heads");
   const int G = a->num_q_heads / a->num_kv_heads;
-  if (G < 1 || G > 8)
-    return fail(CP_ERR_UNSUPPORTED, "q heads per kv head must be 1 .. 8 (got %d)", G);
+  if (G < 1 || G > (a->dtype == CP_BF16 ? 16 : 8))
+    return fail(CP_ERR_UNSUPPORTED, "q heads per kv head must be 1 .. %d for this dtype (got %d)",
+                a->dtype == CP_BF16 ? 16 : 8, G);
   if (a->head_dim != 64 && a->head_dim != 128)
     return fail(CP_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", a->head_dim);
   if (a->block_size != 16)

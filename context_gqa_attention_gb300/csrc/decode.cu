@@ -365,15 +365,15 @@ struct MLayout {
   static constexpr int kStage = 2 * kPageBytes;
   static constexpr int oRing = 0;
   static constexpr int kRing = kCW * kST * kStage;
-  static constexpr int oM = kRing;                  // m [kCW][8]
-  static constexpr int oL = oM + kCW * 8 * 4;       // l [kCW][8]
-  static constexpr int oBar = oL + kCW * 8 * 4;
+  static constexpr int oM = kRing;                  // m [kCW][16] (one per MMA row)
+  static constexpr int oL = oM + kCW * 16 * 4;      // l [kCW][16]
+  static constexpr int oBar = oL + kCW * 16 * 4;
   static constexpr int nBar = 2 * kCW * kST;        // full, empty
   static constexpr int oFlag = oBar + nBar * 8;     // page valid [kCW][kST], abort
   static constexpr int kBytes = oFlag + (kCW * kST + 1) * 4;
   static constexpr int kAlloc = kBytes + 1024;      // base rounded up to the 1 KB swizzle atom
-  static_assert(kCW * 8 * D * 4 <= kRing, "warp partials reuse the ring");
-  static_assert(kAlloc + 8 * 1024 + 64 <= 232448, "shared memory (incl. the fused merge) per CTA");
+  static_assert(kCW * 16 * D * 4 <= kRing, "warp partials reuse the ring");
+  static_assert(kAlloc + 16 * 1024 + 64 <= 232448, "shared memory (incl. the fused merge) per CTA");
 };
 
 CP_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -384,13 +384,15 @@ CP_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, u
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
-// D (16x8 f32) += A (16x16 bf16, rows gid / gid+8) * B (16x8 bf16); a1 = a3 = 0 (rows 8-15 unused)
-CP_DEV void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+// D (16x8 f32) += A (16x16 bf16, rows gid / gid+8) * B (16x8 bf16).  a1, a3 (rows 8-15) are 0
+// when at most 8 query heads share the kv head.
+CP_DEV void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                     uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 // Byte address of the 16-byte chunk holding (token t, dim d) in a 128B-swizzled page half-box.
 CP_DEV uint32_t page_addr(uint32_t base, int t, int d) {
@@ -404,7 +406,8 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
   using T = __nv_bfloat16;
   using Ly = MLayout<D>;
   constexpr int KB = D / 64;  // 64-column boxes per page row
-  static_assert(G <= 8, "query heads per kv head");
+  static_assert(G <= 16, "query heads per kv head (MMA rows)");
+  constexpr bool TWO = G > 8;  // rows gid + 8 hold heads 8 .. G-1
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = sm100::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -517,7 +520,7 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
 
   const int gid = lane >> 2, tid = lane & 3;  // MMA fragment row (head) and column pair
   float o[D / 8][4];
-  float m = -INFINITY, l = 0.f;
+  float m = -INFINITY, l = 0.f, m2 = -INFINITY, l2 = 0.f;  // rows gid and gid + 8
 #pragma unroll
   for (int nb = 0; nb < D / 8; ++nb)
 #pragma unroll
@@ -525,13 +528,16 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
   if (warp < kCW) {
     // ------------------------------------------------------------------ consumers
     // Q rows as MMA A fragments (bf16 pairs straight from memory; rows >= G are zero)
-    uint32_t qa0[D / 16], qa2[D / 16];
+    uint32_t qa0[D / 16], qa2[D / 16], qa1[D / 16], qa3[D / 16];
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
         static_cast<const T*>(p.q) + ((long long)b * p.Hq + (long long)g * G + gid) * D);
+    const uint32_t* qrow8 = qrow + 8 * (D / 2);  // head gid + 8
 #pragma unroll
     for (int ds = 0; ds < D / 16; ++ds) {
       qa0[ds] = gid < G ? __ldg(qrow + ds * 8 + tid) : 0u;
       qa2[ds] = gid < G ? __ldg(qrow + ds * 8 + 4 + tid) : 0u;
+      qa1[ds] = TWO && gid + 8 < G ? __ldg(qrow8 + ds * 8 + tid) : 0u;
+      qa3[ds] = TWO && gid + 8 < G ? __ldg(qrow8 + ds * 8 + 4 + tid) : 0u;
     }
     const float sc = p.scale_log2;
     const int li = lane >> 3, lj = lane & 7;  // ldmatrix: matrix and row this lane addresses
@@ -555,8 +561,8 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
         for (int ds = 0; ds < D / 16; ++ds) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4(page_addr(kp, ((li >> 1) << 3) + lj, ds * 16 + ((li & 1) << 3)), b0, b1, b2, b3);
-          mma16816(s0, qa0[ds], qa2[ds], b0, b1);
-          mma16816(s1, qa0[ds], qa2[ds], b2, b3);
+          mma16816(s0, qa0[ds], qa1[ds], qa2[ds], qa3[ds], b0, b1);
+          mma16816(s1, qa0[ds], qa1[ds], qa2[ds], qa3[ds], b2, b3);
         }
         // head gid, tokens 2tid, 2tid+1, 8+2tid, 9+2tid of this page
         const int t0 = pg * kPage + 2 * tid;
@@ -580,17 +586,46 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
         m = m_new;
         __nv_bfloat162 pa = __floats2bfloat162_rn(p0, p1), pb = __floats2bfloat162_rn(p2, p3);
         const uint32_t pa0 = *reinterpret_cast<uint32_t*>(&pa), pa2 = *reinterpret_cast<uint32_t*>(&pb);
+        uint32_t pa1 = 0u, pa3 = 0u;
+        float corr2 = 1.f;
+        if constexpr (TWO) {  // the same online softmax for head gid + 8 (fragment elements 2, 3)
+          const float y0 = t0 < l1 ? s0[2] * sc : -INFINITY;
+          const float y1 = t0 + 1 < l1 ? s0[3] * sc : -INFINITY;
+          const float y2 = t0 + 8 < l1 ? s1[2] * sc : -INFINITY;
+          const float y3 = t0 + 9 < l1 ? s1[3] * sc : -INFINITY;
+          float my = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
+          my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
+          my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
+          const float m2_new = fmaxf(m2, my);
+          corr2 = m2_new == -INFINITY ? 1.f : exp2f(m2 - m2_new);
+          const float q0 = y0 == -INFINITY ? 0.f : exp2f(y0 - m2_new);
+          const float q1 = y1 == -INFINITY ? 0.f : exp2f(y1 - m2_new);
+          const float q2 = y2 == -INFINITY ? 0.f : exp2f(y2 - m2_new);
+          const float q3 = y3 == -INFINITY ? 0.f : exp2f(y3 - m2_new);
+          float qs = (q0 + q1) + (q2 + q3);
+          qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+          qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+          l2 = l2 * corr2 + qs;
+          m2 = m2_new;
+          __nv_bfloat162 qa = __floats2bfloat162_rn(q0, q1), qb = __floats2bfloat162_rn(q2, q3);
+          pa1 = *reinterpret_cast<uint32_t*>(&qa);
+          pa3 = *reinterpret_cast<uint32_t*>(&qb);
+        }
 #pragma unroll
         for (int nb = 0; nb < D / 8; ++nb) {
           o[nb][0] *= corr;
           o[nb][1] *= corr;
+          if constexpr (TWO) {
+            o[nb][2] *= corr2;
+            o[nb][3] *= corr2;
+          }
         }
 #pragma unroll
         for (int nb = 0; nb < D / 16; ++nb) {
           uint32_t v0, v1, v2, v3;
           ldsm_x4_t(page_addr(vp, ((li & 1) << 3) + lj, nb * 16 + ((li >> 1) << 3)), v0, v1, v2, v3);
-          mma16816(o[2 * nb], pa0, pa2, v0, v1);
-          mma16816(o[2 * nb + 1], pa0, pa2, v2, v3);
+          mma16816(o[2 * nb], pa0, pa1, pa2, pa3, v0, v1);
+          mma16816(o[2 * nb + 1], pa0, pa1, pa2, pa3, v2, v3);
         }
       } else if (lane == 0) {
         report(p.err, CP_ERR_DEVICE_BOUNDS);
@@ -605,8 +640,8 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
   float* o_w = reinterpret_cast<float*>(sb + Ly::oRing);
   if (warp < kCW && gid < G) {
     if (tid == 0) {
-      m_w[warp * 8 + gid] = m;
-      l_w[warp * 8 + gid] = l;
+      m_w[warp * 16 + gid] = m;
+      l_w[warp * 16 + gid] = l;
     }
 #pragma unroll
     for (int nb = 0; nb < D / 8; ++nb) {
@@ -614,18 +649,31 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
       o_w[(warp * G + gid) * D + nb * 8 + 2 * tid + 1] = o[nb][1];
     }
   }
+  if constexpr (TWO) {
+    if (warp < kCW && gid + 8 < G) {
+      if (tid == 0) {
+        m_w[warp * 16 + gid + 8] = m2;
+        l_w[warp * 16 + gid + 8] = l2;
+      }
+#pragma unroll
+      for (int nb = 0; nb < D / 8; ++nb) {
+        o_w[(warp * G + gid + 8) * D + nb * 8 + 2 * tid] = o[nb][2];
+        o_w[(warp * G + gid + 8) * D + nb * 8 + 2 * tid + 1] = o[nb][3];
+      }
+    }
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int hh = i / D, dd = i % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kCW; ++w) M = fmaxf(M, m_w[w * 8 + hh]);
+    for (int w = 0; w < kCW; ++w) M = fmaxf(M, m_w[w * 16 + hh]);
     float Ls = 0.f, Os = 0.f;
 #pragma unroll
     for (int w = 0; w < kCW; ++w) {
-      const float mw = m_w[w * 8 + hh];
+      const float mw = m_w[w * 16 + hh];
       const float e = mw > -INFINITY ? exp2f(mw - M) : 0.f;
-      Ls += e * l_w[w * 8 + hh];
+      Ls += e * l_w[w * 16 + hh];
       Os += e * o_w[(w * G + hh) * D + dd];
     }
     if (Ls > 0.f) {
@@ -657,6 +705,14 @@ cudaError_t launch_mma_g(const DecodeParams& p, int G, dim3 grid, const CUtensor
     case 6: return go(decode_mma_kernel<D, 6, F>);
     case 7: return go(decode_mma_kernel<D, 7, F>);
     case 8: return go(decode_mma_kernel<D, 8, F>);
+    case 9: return go(decode_mma_kernel<D, 9, F>);
+    case 10: return go(decode_mma_kernel<D, 10, F>);
+    case 11: return go(decode_mma_kernel<D, 11, F>);
+    case 12: return go(decode_mma_kernel<D, 12, F>);
+    case 13: return go(decode_mma_kernel<D, 13, F>);
+    case 14: return go(decode_mma_kernel<D, 14, F>);
+    case 15: return go(decode_mma_kernel<D, 15, F>);
+    case 16: return go(decode_mma_kernel<D, 16, F>);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -262,7 +262,7 @@ cp_status cp_attn_prefill_fused(const cp_prefill_args* args, void* out, float* o
 typedef struct cp_decode_args {
   int32_t dtype;                /* cp_dtype of q and caches                             */
   int32_t num_seqs;             /* B                                                    */
-  int32_t num_q_heads;          /* Hq = G * Hkv with G (q heads per kv head) in 1 .. 8  */
+  int32_t num_q_heads;          /* Hq = G * Hkv, G in 1 .. 16 (bf16) or 1 .. 8 (f32)    */
   int32_t num_kv_heads;         /* Hkv                                                  */
   int32_t head_dim;             /* d in {64, 128}                                       */
   int32_t cp;                   /* logical ranks                                        */

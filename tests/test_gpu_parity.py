@@ -231,6 +231,8 @@ DECODE_CASES = [
     (4, (100, 2500), 28, 4, 128, torch.bfloat16, 2, 8),   # G = 7
     (3, (50, 700), 15, 5, 64, torch.bfloat16, 3, 16),     # G = 3
     (2, (200, 900), 10, 2, 128, torch.float32, 2, 8),     # G = 5, CUDA-core kernel
+    (3, (100, 1500), 32, 2, 128, torch.bfloat16, 2, 8),   # G = 16: both MMA row halves
+    (2, (30, 600), 11, 1, 64, torch.bfloat16, 3, 4),      # G = 11
 ]
 
 
