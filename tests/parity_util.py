@@ -1,8 +1,10 @@
 """Shared helpers of the GPU parity tests: tolerance checks against the float64 oracle.
 
 Tolerances (bf16 inputs, fp32 accumulation):
-  * outputs: max |O_gpu - O_oracle| <= 1e-2 (also for bf16-rounded merged outputs: |O| is at
-    most a few units here and bf16 rounding adds <= 2^-9 |O|);
+  * outputs: max |O_gpu - O_oracle| <= 1e-2.  Outputs the library rounds to bf16 (the merged
+    output of bf16 inputs, round to nearest even) additionally get the rounding bound of that
+    format, half an ulp <= 2^-8 |O| per element (8 significant bits): with few visible keys O is
+    close to a single N(0,1) value row and |O| reaches ~4.5, where rounding alone is ~0.018;
   * LSE: |LSE_gpu - LSE_oracle| <= 1e-3 |LSE_oracle| + 1e-5.  The absolute floor covers rows
     whose LSE is near 0: fp32 dot products of 128 bf16 products of unit scale carry ~1e-6
     absolute error, far inside 1e-5;
@@ -43,11 +45,17 @@ def check_partials(out, lse, O_ref, L_ref, rows=None, what=""):
     return float(do.max(initial=0)), float(dl.max(initial=0))
 
 
+BF16_HALF_ULP_REL = 2.0 ** -8
+
+
 def check_merged(out, lse, O_ref, L_ref, what=""):
+    rounded = out.dtype == torch.bfloat16
     out = to_np(out)
     do = np.abs(out - O_ref)
     assert np.isfinite(out).all(), f"{what}: non-finite output"
-    assert do.max(initial=0) <= ATOL_O, f"{what}: merged out max err {do.max():.3e}"
+    tol = ATOL_O + (BF16_HALF_ULP_REL * np.abs(O_ref) if rounded else 0.0)
+    assert (do <= tol).all(), f"{what}: merged out max err {do.max():.3e} " \
+        f"(worst ratio {(do / tol).max():.2f})"
     if lse is not None:
         lse = to_np(lse)
         fin = np.isfinite(L_ref)
@@ -56,3 +64,13 @@ def check_merged(out, lse, O_ref, L_ref, what=""):
         assert (dl <= RTOL_LSE * np.abs(L_ref[fin]) + ATOL_LSE).all(), \
             f"{what}: merged lse max err {dl.max():.3e}"
     return float(do.max(initial=0))
+
+
+def check_same_rounded(a, b, what=""):
+    """Two bf16 outputs of the same exact attention computed along different paths: each is
+    within the f32 error of the truth before rounding, and the two roundings may land one ulp
+    apart (<= 2^-7 |x|)."""
+    a, b = to_np(a), to_np(b)
+    tol = ATOL_O + 2 * BF16_HALF_ULP_REL * np.abs(b)
+    d = np.abs(a - b)
+    assert (d <= tol).all(), f"{what}: max diff {d.max():.3e} (worst ratio {(d / tol).max():.2f})"
