@@ -125,7 +125,8 @@ CP_DEV void page_rows(const int (&id)[NP], int t, int n_local, long long pool, i
 
 // blockIdx.x -> (q tile slot, sequence, kv shard, head group of `hpc` consecutive q heads).
 // Slots run heaviest first (last chunk, last tile) so long items start early.
-CP_DEV Work decode_work(const TcParams& p, int hpc) {
+// `span` query rows per item: BM (one tile; head pairs) or 2 BM (two tiles of one head).
+CP_DEV Work decode_work(const TcParams& p, int hpc, int span = BM) {
   Work w;
   w.valid = 0;
   unsigned lin = blockIdx.x;  // 32-bit divisions: the grid is below 2^31 blocks
@@ -147,9 +148,9 @@ CP_DEV Work decode_work(const TcParams& p, int hpc) {
   const int Tq = p.cu_q[w.b + 1] - q0;
   if (Tq <= 0) return w;
   const int cs = chunk_bound(c, Tq, p.cp), ce = chunk_bound(c + 1, Tq, p.cp);
-  w.q_lo = cs + j * BM;
+  w.q_lo = cs + j * span;
   if (w.q_lo >= ce) return w;
-  w.q_hi = min(w.q_lo + BM, ce);
+  w.q_hi = min(w.q_lo + span, ce);
   if (p.q_shard >= 0 && shard_of_chunk(c, p.cp) != p.q_shard) return w;
   w.valid = 1;
   w.g = w.h / (p.Hq / p.Hkv);
@@ -774,7 +775,9 @@ struct Layout2 {
   static_assert(kAlloc <= 232448, "dynamic shared memory beyond the 227 KB per-CTA limit");
 };
 
-template <int D, bool PT, bool PG>  // PG: paged K/V as whole-page boxes (pass-Q, d = 128)
+// PG: paged K/V as whole-page boxes (pass-Q, d = 128).  TT: the two "tiles" of the CTA are two
+// consecutive 128-row query tiles of one head (any G) instead of two heads of a kv group (even G).
+template <int D, bool PT, bool PG, bool TT>
 __global__ void __launch_bounds__(kThreads2, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -785,15 +788,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
   constexpr int KB = D / 64;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Work w = decode_work(p, 2);
+  const Work w = TT ? decode_work(p, 1, 2 * BM) : decode_work(p, 2);
   if (!w.valid) return;
 
   if (w.ntiles == 0) {  // empty pair
     if (warp >= 2) {
       const int tile = (warp - 2) >> 2;
-      const int row = (warp & 3) * 32 + lane;
+      const int row = (warp & 3) * 32 + lane + (TT ? tile * BM : 0);  // within the item
       if (w.q_lo + row < w.q_hi)
-        p.lse[((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile] = -INFINITY;
+        p.lse[((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + (TT ? 0 : tile)] = -INFINITY;
     }
     return;
   }
@@ -825,11 +828,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
     tma_prefetch_desc(&map_q);
     mbar_expect_tx(bar(Ly::bQ), 2 * Ly::kQ);
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < 2; ++i)  // two heads at the tile's rows, or one head's two row tiles
 #pragma unroll
       for (int kb = 0; kb < KB; ++kb)
-        tma_load_2d(sQ + i * Ly::kQ + kb * BM * 128, &map_q, (w.h + i) * D + kb * 64, w.q_row0,
-                    bar(Ly::bQ));
+        tma_load_2d(sQ + i * Ly::kQ + kb * BM * 128, &map_q, (w.h + (TT ? 0 : i)) * D + kb * 64,
+                    w.q_row0 + (TT ? i * BM : 0), bar(Ly::bQ));
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(misc), 512);
@@ -983,11 +986,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const int tile = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
+    const int rofs = TT ? tile * BM : 0;   // this tile's first row within the item
+    const int hcol = w.h + (TT ? 0 : tile);  // this tile's query head
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)(tile * BN);
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(tile * D);
-    const bool row_valid = w.q_lo + row < w.q_hi;
-    const long long qpos = w.qpos0 + row;
+    const bool row_valid = w.q_lo + rofs + row < w.q_hi;
+    const long long qpos = w.qpos0 + rofs + row;
     int nvis = 0;
     if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
     float m = -INFINITY, l = 0.f;
@@ -1032,9 +1037,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
                                              abort_flag, p.budget));
     if (ok) {
       tc_fence_after();
-      const long long frow = (long long)(w.q_row0 + row) * p.Hq + w.h + tile;
-      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + tile;
-      if (p.tma_out && w.q_lo + q4 * 32 + 32 <= w.q_hi) {
+      const long long frow = (long long)(w.q_row0 + rofs + row) * p.Hq + hcol;
+      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + rofs + row) * p.Hq + hcol;
+      if (p.tma_out && w.q_lo + rofs + q4 * 32 + 32 <= w.q_hi) {
         // all 32 rows of this warp are real: stage them and store by TMA.  Head 0 stages in
         // the Q tiles (free: its last PV completed after the other head's last QK), head 1 in
         // the K/V ring (free: its last PV is the CTA's last MMA).
@@ -1045,9 +1050,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          const int z = (p.fused ? 0 : w.p * p.Nq) + w.q_row0 + q4 * 32;
+          const int z = (p.fused ? 0 : w.p * p.Nq) + w.q_row0 + rofs + q4 * 32;
           const int nbox = p.fused ? D / 64 : D / 32, bw = p.fused ? 64 : 32;
-          for (int bx = 0; bx < nbox; ++bx) tma_store_3d(&map_o, sb + bx * 4096, bx * bw, w.h + tile, z);
+          for (int bx = 0; bx < nbox; ++bx) tma_store_3d(&map_o, sb + bx * 4096, bx * bw, hcol, z);
           bulk_commit();
           bulk_wait_read_all();  // the staging buffer is released at kernel exit
         }
@@ -1135,9 +1140,11 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
     if (!make_map(&mk, a.k, hd, Nq, hd, BN) || !make_map(&mv, a.v, hd, Nq, hd, BN))
       return cudaErrorInvalidValue;
   }
-  // two heads per CTA when the heads of a kv group pair up, unless one head per CTA is forced
+  // the two-tile kernel unless one head per CTA is forced: two heads of a kv group when they
+  // pair up (even G), else two consecutive row tiles of one head (`tiles`)
   const int G = a.num_q_heads / a.num_kv_heads;
-  const bool pair = (G % 2 == 0) && a.impl != CP_IMPL_TCGEN05_SINGLE;
+  const bool pair = a.impl != CP_IMPL_TCGEN05_SINGLE;
+  const bool tiles = pair && (G % 2 != 0);
   int page_kv = 0;
   if (a.mode != CP_PASS_KV) {
     const unsigned long long rows = (unsigned long long)a.cp * a.pool_pages * a.num_kv_heads * 16;
@@ -1165,7 +1172,8 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   p.debug = a.debug;
   p.budget = (a.debug & 1) ? (1ll << 21) : kBudget;
   const int chunk_max = (a.max_seqlen_q + 2 * a.cp - 1) / (2 * a.cp);
-  p.TPC = (chunk_max + BM - 1) / BM;
+  const int span = tiles ? 2 * BM : BM;  // query rows per work item
+  p.TPC = (chunk_max + span - 1) / span;
   p.Nq = a.total_q;
   p.pool = a.pool_pages;
   p.scale_log2 = scale * kLog2e;
@@ -1183,7 +1191,8 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   p.tma_out = p.fused ? make_out_map(&mo, fused_out, true, D, a.num_q_heads, Nq)
                       : make_out_map(&mo, a.out, false, D, a.num_q_heads, (unsigned long long)a.cp * Nq);
   const long long grid = (long long)2 * a.cp * p.TPC * a.num_seqs *
-                         ((a.kv_shard >= 0 || p.fused) ? 1 : a.cp) * (a.num_q_heads / (pair ? 2 : 1));
+                         ((a.kv_shard >= 0 || p.fused) ? 1 : a.cp) *
+                         (a.num_q_heads / (pair && !tiles ? 2 : 1));
   if (grid == 0) return cudaSuccess;
   if (grid >= (1ll << 31)) return cudaErrorInvalidConfiguration;
   cudaError_t e;
@@ -1191,8 +1200,10 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
     const int smem = Layout2<D, kPInTmem>::kAlloc;
     // pass-Q at d = 128 (page_kv): K and V pages arrive as whole-page boxes laid out
     // [page][row group][half][8 rows][128 B] in the slot
-    auto kern = page_kv ? prefill_tc2_kernel<D, kPInTmem, (D == 128)>
-                        : prefill_tc2_kernel<D, kPInTmem, false>;
+    auto kern = tiles ? (page_kv ? prefill_tc2_kernel<D, kPInTmem, (D == 128), true>
+                                 : prefill_tc2_kernel<D, kPInTmem, false, true>)
+                      : (page_kv ? prefill_tc2_kernel<D, kPInTmem, (D == 128), false>
+                                 : prefill_tc2_kernel<D, kPInTmem, false, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, mo, p);
