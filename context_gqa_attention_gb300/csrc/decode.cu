@@ -46,19 +46,7 @@ struct DecodeParams {
   int page_box;
 };
 
-template <typename T> struct Vec;
-template <> struct Vec<__nv_bfloat16> {
-  static constexpr int N = 8;
-  static CP_DEV void unpack(const uint4& u, float* f) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 x = __bfloat1622float2(h[i]);
-      f[2 * i] = x.x;
-      f[2 * i + 1] = x.y;
-    }
-  }
-};
+template <typename T> struct Vec;  // the CUDA-core kernel's 16-byte vector of T (f32 path)
 template <> struct Vec<float> {
   static constexpr int N = 4;
   static CP_DEV void unpack(const uint4& u, float* f) {

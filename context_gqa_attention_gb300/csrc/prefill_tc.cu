@@ -324,35 +324,6 @@ CP_DEV float row_max_update(float (&v0)[32], float (&v1)[32], float (&v2)[32], f
   return alpha;
 }
 
-// ... then exponentials streamed 32 columns at a time straight into the swizzled P tile
-// (returns the row sum of p).
-CP_DEV void exp_store_chunk(float (&a)[32], int c, uint64_t sc2, uint64_t n2, uint64_t& sum2,
-                            uint32_t prow, uint32_t sw) {
-  exp_chunk(a, sc2, n2, sum2);
-  const uint32_t blk = prow + (uint32_t)(c >> 1) * (BM * 128);
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    const uint32_t ch = (uint32_t)((c & 1) * 4 + h);
-    st_shared_v4(blk + ((ch ^ sw) << 4), pack_bf16(a[h * 8], a[h * 8 + 1]),
-                 pack_bf16(a[h * 8 + 2], a[h * 8 + 3]), pack_bf16(a[h * 8 + 4], a[h * 8 + 5]),
-                 pack_bf16(a[h * 8 + 6], a[h * 8 + 7]));
-  }
-}
-CP_DEV float row_exp_store(float (&v0)[32], float (&v1)[32], float (&v2)[32], float (&v3)[32],
-                           float sc, float m, uint32_t sP, int row) {
-  const float neg = (m == -INFINITY) ? 0.f : -m;
-  const uint64_t sc2 = f2(sc, sc), n2 = f2(neg, neg);
-  uint64_t sum2 = f2(0.f, 0.f);
-  const uint32_t prow = sP + row * 128, sw = (uint32_t)(row & 7);
-  exp_store_chunk(v0, 0, sc2, n2, sum2, prow, sw);
-  exp_store_chunk(v1, 1, sc2, n2, sum2, prow, sw);
-  exp_store_chunk(v2, 2, sc2, n2, sum2, prow, sw);
-  exp_store_chunk(v3, 3, sc2, n2, sum2, prow, sw);
-  float lo, hi;
-  f2u(sum2, lo, hi);
-  return lo + hi;
-}
-
 // Exponentials of a row packed as bf16 pairs into the first 64 columns of its S buffer in TMEM
 // (the A operand of a tensor-memory PV MMA), 16 columns per store; returns the row sum of p.
 CP_DEV void exp_pack_tmem(float (&a)[32], uint64_t sc2, uint64_t n2, uint64_t& sum2, uint32_t taddr) {
@@ -744,29 +715,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------- kernel 2
-// Two query heads of the same kv group per CTA (tiles 0 and 1: heads h, h+1, same 128 rows),
-// sharing every K/V tile.  Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2-5 softmax of
-// tile 0, 6-9 softmax of tile 1 (warp w reads TMEM lanes 32 (w % 4) ..).  TMEM: S0 [0,128), S1 [128,256),
-// O0 [256, 256+D), O1 [256+D, 256+2D).  K and V tiles stream through a 3-slot ring (load i:
-// K(t) for i = 2t, V(t) for i = 2t+1).  Tensor-core order per key tile t:
+// Two query tiles per CTA sharing every K/V tile: tiles 0 and 1 are heads h, h+1 of one kv group
+// over the same 128 rows (even G), or two consecutive 128-row tiles of one head.  Warps: 0 TMA
+// producer, 1 TMEM owner + MMA issuer, 2-5 softmax of tile 0, 6-9 softmax of tile 1 (warp w
+// reads TMEM lanes 32 (w % 4) ..).  TMEM: S0 [0,128), S1 [128,256), O0 [256, 256+D),
+// O1 [256+D, 256+2D).  The softmax writes P as packed bf16 pairs over the first 64 columns of its
+// own S buffer and the PV MMA reads A from tensor memory.  K and V tiles stream through a 4-slot
+// ring (load i: K(t) for i = 2t, V(t) for i = 2t+1; 4 slots measured ~1.5% faster than 5).
+// Tensor-core order per key tile t:
 //   PV0(t) | QK0(t+1) | PV1(t) | QK1(t+1)
 // so the softmax of each tile overlaps the other tile's two MMAs.
-// With PT (P in TMEM) the softmax writes P as packed bf16 pairs over the first 64 columns of
-// its own S buffer and the PV MMA reads A from tensor memory; the 64 KB of P tiles are given to
-// the K/V ring instead (5 slots).
 constexpr int kThreads2 = 320;
-constexpr bool kPInTmem = true;
 
-template <int D, bool PT>
+template <int D>
 struct Layout2 {
-  static constexpr int NSLOT = PT ? 4 : 3;  // 4 measured ~1.5% faster than 5 (P in TMEM)
+  static constexpr int NSLOT = 4;
   static constexpr int kQ = BM * D * 2;
   static constexpr int kKV = BN * D * 2;
-  static constexpr int kP = BM * BN * 2;
   static constexpr int oQ = 0;
   static constexpr int oKV = 2 * kQ;
-  static constexpr int oP = oKV + NSLOT * kKV;
-  static constexpr int oBar = oP + (PT ? 0 : 2 * kP);
+  static constexpr int oBar = oKV + NSLOT * kKV;
   static constexpr int bQ = 0, bFull = 1, bEmpty = bFull + NSLOT, bS = bEmpty + NSLOT, bP = bS + 2,
                        bO = bP + 2, bDone = bO + 2, nBar = bDone + 1;
   static constexpr int oMisc = oBar + nBar * 8;
@@ -777,13 +745,13 @@ struct Layout2 {
 
 // PG: paged K/V as whole-page boxes (pass-Q, d = 128).  TT: the two "tiles" of the CTA are two
 // consecutive 128-row query tiles of one head (any G) instead of two heads of a kv group (even G).
-template <int D, bool PT, bool PG, bool TT>
+template <int D, bool PG, bool TT>
 __global__ void __launch_bounds__(kThreads2, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_v,
                        const __grid_constant__ CUtensorMap map_o, const TcParams p) {
-  using Ly = Layout2<D, PT>;
+  using Ly = Layout2<D>;
   constexpr int NSLOT = Ly::NSLOT;
   constexpr int KB = D / 64;
   extern __shared__ uint8_t smem_raw[];
@@ -804,7 +772,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + Ly::oQ, sKV = base + Ly::oKV, sP = base + Ly::oP;
+  const uint32_t sQ = base + Ly::oQ, sKV = base + Ly::oKV;
   const uint32_t bars = base + Ly::oBar;
   auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
   uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Ly::oMisc);
@@ -928,13 +896,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
           // the tiled layout (halves BN x 128 B apart, groups 1 KB apart)
           const uint64_t bd = PG ? desc_sw128(v + kk * 4096, 1024, 2048)
                                  : desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
-          if constexpr (PT) {  // P: 8 packed columns per 16 keys
-            mma_ts(dO, tmem + (uint32_t)(tile * BN + kk * 8), bd, id_pv, (acc || kk > 0) ? 1u : 0u);
-          } else {
-            const uint32_t offp = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-            mma_ss(dO, desc_sw128(sP + tile * Ly::kP + offp, 16, 1024), bd, id_pv,
-                   (acc || kk > 0) ? 1u : 0u);
-          }
+          // P: 8 packed TMEM columns per 16 keys, the A operand from tensor memory
+          mma_ts(dO, tmem + (uint32_t)(tile * BN + kk * 8), bd, id_pv, (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(bar(Ly::bQ), 0u, abort_flag, p.budget);
@@ -1013,21 +976,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
         lim = nvis - 1 - t * BN;
       }
       const float alpha = row_max_update(s0, s1, s2, s3, lim, p.scale_log2, m);
-      if constexpr (PT) {
-        // S(t) complete implies PV(t-1) complete (it was issued before QK(t)): O is stable and
-        // the S columns may take P(t)
-        l = l * alpha + row_exp_tmem(s0, s1, s2, s3, p.scale_log2, m, tS);
-        if (t > 0) rescale_o<D>(tO, alpha);
-      } else {
-        if (t > 0) {  // PV(t-1) of this tile finished before QK(t) began: P free, O stable
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO + tile), (uint32_t)(t - 1) & 1u, abort_flag, p.budget));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        l = l * alpha + row_exp_store(s0, s1, s2, s3, p.scale_log2, m, sP + tile * Ly::kP, row);
-        if (t > 0) rescale_o<D>(tO, alpha);
-        fence_proxy_async_smem();
-      }
+      // S(t) complete implies PV(t-1) complete (it was issued before QK(t)): O is stable and
+      // the S columns may take P(t)
+      l = l * alpha + row_exp_tmem(s0, s1, s2, s3, p.scale_log2, m, tS);
+      if (t > 0) rescale_o<D>(tO, alpha);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Ly::bP + tile));
@@ -1197,13 +1149,13 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   if (grid >= (1ll << 31)) return cudaErrorInvalidConfiguration;
   cudaError_t e;
   if (pair) {
-    const int smem = Layout2<D, kPInTmem>::kAlloc;
+    const int smem = Layout2<D>::kAlloc;
     // pass-Q at d = 128 (page_kv): K and V pages arrive as whole-page boxes laid out
     // [page][row group][half][8 rows][128 B] in the slot
-    auto kern = tiles ? (page_kv ? prefill_tc2_kernel<D, kPInTmem, (D == 128), true>
-                                 : prefill_tc2_kernel<D, kPInTmem, false, true>)
-                      : (page_kv ? prefill_tc2_kernel<D, kPInTmem, (D == 128), false>
-                                 : prefill_tc2_kernel<D, kPInTmem, false, false>);
+    auto kern = tiles ? (page_kv ? prefill_tc2_kernel<D, (D == 128), true>
+                                 : prefill_tc2_kernel<D, false, true>)
+                      : (page_kv ? prefill_tc2_kernel<D, (D == 128), false>
+                                 : prefill_tc2_kernel<D, false, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, mo, p);
