@@ -71,7 +71,7 @@ def ncu_traffic(kind, workload):
 
 def source_sha1():
     """SHA-1 over the library's sources (kernels, host code, header): names the exact build a
-    line was measured on (the GPU machine's copy of the tree has no git metadata)."""
+    line was measured on (a copied tree need not carry git metadata)."""
     import glob
     import hashlib
     h = hashlib.sha1()
@@ -424,7 +424,7 @@ class DecodeRunner:
         self.part = torch.empty(P, w.num_seqs, Hq, d, dtype=torch.float32, device=dev)
         self.plse = torch.empty(P, w.num_seqs, Hq, dtype=torch.float32, device=dev)
         self.out = torch.empty(w.num_seqs, Hq, d, dtype=w.dtype, device=dev)
-        self.fused = False  # two launches measured faster than the fused one (see DESIGN.md)
+        self.fused = False  # two launches measured faster than the fused one
         self.ws = torch.zeros(cpa.cp_decode_workspace_size(w.num_seqs, Hq, Hkv, d, cp, self.ns),
                               dtype=torch.uint8, device=dev)
         self.local_lens = torch.empty(cp, w.num_seqs, dtype=torch.int32, device=dev)
