@@ -39,14 +39,14 @@ import workloads as wl  # noqa: E402
 # each from one ncu capture summarised under profiles/.  A figure is reported only while the
 # kernel's source file still has the SHA-1 the capture was taken on; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # profiles/prefill_tc2_full_prefill.md: dram read 42.03 MB + write 62.49 MB
+    # profiles/prefill_tc2_full_prefill.md: dram read 42.10 MB + write 62.22 MB
     "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                "sha1": "42181699a6fdc7a50284337b0f71d2c6a20ca6ea", "bytes": 104521472,
+                "sha1": "3947c9bcc27dcf9ccfb20945d0288dde1f20ea99", "bytes": 104318976,
                 "workload": "full"},
-    # profiles/decode_mma_decode.md: a 16-sequence capture (1.1187 GB read + 5.28 MB written),
+    # profiles/decode_mma_decode.md: a 16-sequence capture (1.1187 GB read + 5.36 MB written),
     # scaled to the 64-sequence workload by algorithmic bytes (4.3933e9 / 1.1181e9)
     "decode": {"file": "context_gqa_attention_gb300/csrc/decode.cu",
-               "sha1": "933f13647945ffea306dd32d47393f3451c3ae50", "bytes": 4416280000,
+               "sha1": "9b0d529eacd73ab4391495a21d18a2e537d1c074", "bytes": 4416620000,
                "workload": "decode"},
 }
 
