@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(256) prefill_simt_kernel(const SimtParams p) {
       const T* Kc = static_cast<const T*>(p.k);
       const T* Vc = static_cast<const T*>(p.v);
       const long long L = p.seq_lens_kv[b];
+      if (L < Tq) bad = true;  // fewer kv tokens than new queries: flagged, the row skipped
       const long long qpos = L - Tq + t;
       const int n = rank_local_len(qpos + 1, part, cp, p.I);
       const int32_t* trow = p.tables + ((long long)part * p.B + b) * p.max_blocks;

@@ -178,6 +178,11 @@ CP_DEV Work decode_work(const TcParams& p, int hpc, int span = BM) {
     }
   } else {
     const long long C = (long long)p.seq_lens_kv[w.b] - Tq;
+    if (C < 0) {  // fewer kv tokens than new queries: flagged, the item is skipped
+      report(p.err, CP_ERR_DEVICE_BOUNDS);
+      w.valid = 0;
+      return w;
+    }
     w.qpos0 = C + w.q_lo;
     w.n_local = rank_local_len(C + w.q_hi, w.p, p.cp, p.I);
     w.ntiles = (w.n_local + BN - 1) / BN;

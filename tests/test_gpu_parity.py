@@ -220,6 +220,21 @@ def test_pass_q_reports_bad_page(lib, impl):
     check_partials(out, lse, O, L, what=f"pass-Q {impl} after a bad table")
 
 
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
+def test_pass_q_reports_short_kv(lib, impl):
+    """seq_lens_kv below the new-query count (a negative cached context) lives on the device, so
+    the kernels flag it (CP_ERR_DEVICE_BOUNDS) and skip the rows instead of running on."""
+    x = _paged_case(2, [40, 30], [100, 60], 8, 2, 128, torch.bfloat16, 2, 8, 31)
+    sl = torch.tensor([100, 20], dtype=torch.int32, device=DEV)   # sequence 1: 20 < 30
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lib.cp_partial_attn_prefill(x["q"].to(DEV), x["cu_seqlens_q"].to(DEV), 2, mode=lib.CP_PASS_Q,
+                                k_cache=x["k_cache"].to(DEV), v_cache=x["v_cache"].to(DEV),
+                                block_tables=x["block_tables"].to(DEV), seq_lens_kv=sl,
+                                interleave=8, impl=_impl_code(lib, impl), err=err, max_seqlen_q=40)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 5
+
+
 # ------------------------------------------------------------------------------------ decode
 
 DECODE_CASES = [
