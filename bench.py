@@ -39,9 +39,9 @@ import workloads as wl  # noqa: E402
 # each from one ncu capture summarised under profiles/.  A figure is reported only while the
 # kernel's source file still has the SHA-1 the capture was taken on; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # profiles/prefill_tc2_full_prefill.md: dram read 42.10 MB + write 62.22 MB
+    # profiles/prefill_tc2_full_prefill.md: dram read 42.03 MB + write 62.41 MB
     "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                "sha1": "3947c9bcc27dcf9ccfb20945d0288dde1f20ea99", "bytes": 104318976,
+                "sha1": "d42bd18b5bf8e13a67f9c238d44014b9315d9a9d", "bytes": 104439040,
                 "workload": "full"},
     # profiles/decode_mma_decode.md: a 16-sequence capture (1.1187 GB read + 5.36 MB written),
     # scaled to the 64-sequence workload by algorithmic bytes (4.3933e9 / 1.1181e9)
