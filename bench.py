@@ -567,10 +567,24 @@ def oracle_sample(w, rows_per_step, seed):
     t = time.time()
     O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], w.cp,
                                 1 / math.sqrt(w.head_dim), rows=rows)
-    orc.lse_merge(O, L)
+    Om, Lm = orc.lse_merge(O, L)
     dt = time.time() - t
     flops = 4.0 * w.head_dim * w.num_q_heads * sum(r + 1 for r in rows)
-    return flops, dt, len(rows)
+    return flops, dt, len(rows), (rows, Om, Lm)
+
+
+def parity_line(runner, ref):
+    """Max errors of the bench's own merged output (the last device-only step) against the
+    oracle rows the CPU baseline computed (same seeded inputs)."""
+    import numpy as np
+    rows, Om, Lm = ref
+    idx = torch.as_tensor(rows, dtype=torch.long, device=runner.out.device)
+    out = runner.out.index_select(0, idx).double().cpu().numpy()
+    lse = runner.olse.index_select(0, idx).double().cpu().numpy()
+    fin = np.isfinite(Lm)
+    return {"rows": len(rows), "max_abs_out": float(np.abs(out - Om).max()),
+            "max_rel_lse": float((np.abs(lse[fin] - Lm[fin]) / np.abs(Lm[fin]).clip(1e-30)).max()),
+            "tolerance": "out 1e-2 + bf16 rounding 2^-8 |O|; lse 1e-3 relative"}
 
 
 def blas_threads():
@@ -627,7 +641,7 @@ def run_reference(args, ws, rank):
         oracle_sample(w, max(rows // 8, 8), 9000 + i)
     tot_flops, tot_t, nrows = 0.0, 0.0, 0
     for i in range(args.steps):
-        f, t, n = oracle_sample(w, rows, 9100 + i)
+        f, t, n, _ = oracle_sample(w, rows, 9100 + i)
         tot_flops += f
         tot_t += t
         nrows += n
@@ -825,7 +839,9 @@ def main():
         line["secondary"] = sec
 
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and w.kind == "pass_kv":
-        f, t, n = oracle_sample(w, args.cpu_rows, 777)
+        f, t, n, ref = oracle_sample(w, args.cpu_rows, 777)
+        if isinstance(runner, PrefillRunner) and not runner.fused:
+            line["parity"] = parity_line(runner, ref)
         line["cpu_baseline"] = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
                                 "cpu_count": os.cpu_count(), "seconds": t,
                                 "rows_per_s": n * w.num_q_heads / t,
