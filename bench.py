@@ -39,9 +39,9 @@ import workloads as wl  # noqa: E402
 # each from one ncu capture summarised under profiles/.  A figure is reported only while the
 # kernel's source file still has the SHA-1 the capture was taken on; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # profiles/prefill_tc2_full_prefill.md: dram read 42.03 MB + write 62.41 MB
+    # profiles/prefill_tc2_full_prefill.md: dram read 42.04 MB + write 62.62 MB
     "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                "sha1": "d42bd18b5bf8e13a67f9c238d44014b9315d9a9d", "bytes": 104439040,
+                "sha1": "f5e76231536f7a2d64acec456b240e4ea068bec2", "bytes": 104651264,
                 "workload": "full"},
     # profiles/decode_mma_decode.md: a 16-sequence capture (1.1187 GB read + 5.36 MB written),
     # scaled to the 64-sequence workload by algorithmic bytes (4.3933e9 / 1.1181e9)
@@ -360,8 +360,9 @@ class PassQRunner:
         ctx = w.kv_len - w.q_len
         pairs = sum(ctx + i + 1 for i in range(w.q_len)) * w.num_seqs
         self.flops = 4.0 * d * Hq * pairs
-        self.launches_per_step = 4
         self.impl = cpa.CP_IMPL_AUTO
+        self.fused = False
+        self.olse = torch.empty(self.N, Hq, dtype=torch.float32, device=dev)
 
     def step(self, ev=None):
         cpa, w = self.cpa, self.w
@@ -373,8 +374,23 @@ class PassQRunner:
 
         run_with_side_maps(self, maps, lambda: self._attention(ev))
 
+    @property
+    def launches_per_step(self):
+        return 3 if self.fused else 4
+
     def _attention(self, ev=None):
         cpa, w = self.cpa, self.w
+        if self.fused:  # every rank's resident pages walked inside one item: final output
+            if ev is not None:
+                ev[0].record()
+            cpa.cp_attn_prefill_fused(self.q, self.cu_q, w.cp, mode=cpa.CP_PASS_Q,
+                                      k_cache=self.kc, v_cache=self.vc, block_tables=self.tables,
+                                      seq_lens_kv=self.seq_lens, interleave=w.interleave,
+                                      max_seqlen_q=w.q_len, out=self.out, out_lse=self.olse,
+                                      impl=self.impl)
+            if ev is not None:
+                ev[1].record()
+            return
         if ev is not None:
             ev[0].record()
         cpa.cp_partial_attn_prefill(self.q, self.cu_q, w.cp, mode=cpa.CP_PASS_Q, k_cache=self.kc,
@@ -714,7 +730,7 @@ def main():
         runner.fused = args.decode_fused
         if args.decode_split_tokens > 0:
             runner.resplit(args.decode_split_tokens)
-    if isinstance(runner, PrefillRunner) and not isinstance(runner, PassQRunner):
+    if isinstance(runner, (PrefillRunner, PassQRunner)):
         runner.fused = args.prefill_fused
     runner.impl = {"auto": cpa.CP_IMPL_AUTO, "tcgen05": cpa.CP_IMPL_TCGEN05,
                    "simt": cpa.CP_IMPL_SIMT}[args.prefill_impl]
@@ -741,11 +757,13 @@ def main():
         e2e = None
         peak, src = pk["bf16"]
         achieved = runner.flops / dom_s / 1e12
-        roof = {"bound": "tensor", "kernel": "cp_partial_attn_prefill (pass-Q, paged)",
+        roof = {"bound": "tensor", "kernel": "cp_attn_prefill_fused (pass-Q, paged, merged in-kernel)"
+                if runner.fused else "cp_partial_attn_prefill (pass-Q, paged)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": f"{src} bf16 dense (burst)", "traffic": None,
                 "algorithmic": f"{runner.flops:.4e} causal FLOP per launch", "launch_ms": dom_s * 1e3}
-        metric = "causal GQA chunked-prefill TFLOP/s (pass-Q partial attention + LSE merge)"
+        metric = ("causal GQA chunked-prefill TFLOP/s (pass-Q, ranks merged in-kernel)" if runner.fused
+                  else "causal GQA chunked-prefill TFLOP/s (pass-Q partial attention + LSE merge)")
         unit = "TFLOP/s"
     elif isinstance(runner, PrefillRunner):
         runner.e2e_run(3, stream)

@@ -296,10 +296,13 @@ def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=N
     return out, lse
 
 
-def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k, v, *, max_seqlen_q=None, softmax_scale=0.0,
-                          impl=CP_IMPL_AUTO, out=None, out_lse=None, stream=None):
-    """Pass-KV prefill with the merge folded in (see cpattn.h): exact causal attention
-    out [Nq, Hq, d] bf16 and lse [Nq, Hq] f32 without partials."""
+def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k=None, v=None, *, mode=CP_PASS_KV, k_cache=None,
+                          v_cache=None, block_tables=None, seq_lens_kv=None, interleave=8,
+                          max_seqlen_q=None, softmax_scale=0.0, impl=CP_IMPL_AUTO, out=None,
+                          out_lse=None, stream=None):
+    """Prefill with the merge folded in (see cpattn.h): exact causal attention out [Nq, Hq, d]
+    bf16 and lse [Nq, Hq] f32 without partials.  PASS_KV: k, v [Nq, Hkv, d].  PASS_Q: the paged
+    round-robin cache as in cp_partial_attn_prefill (every rank's resident tokens in one pass)."""
     load()
     Nq, Hq, d = q.shape
     B = cu_seqlens_q.numel() - 1
@@ -307,18 +310,33 @@ def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k, v, *, max_seqlen_q=None, softm
         out = torch.empty(Nq, Hq, d, dtype=torch.bfloat16, device=q.device)
     if out_lse is None:
         out_lse = torch.empty(Nq, Hq, dtype=torch.float32, device=q.device)
-    for n, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
-                     ("cu_seqlens_q", cu_seqlens_q, torch.int32), ("out", out, torch.bfloat16),
-                     ("out_lse", out_lse, torch.float32)):
+    for n, t, dt in (("q", q, torch.bfloat16), ("cu_seqlens_q", cu_seqlens_q, torch.int32),
+                     ("out", out, torch.bfloat16), ("out_lse", out_lse, torch.float32)):
         _dev(t, n, dt)
     if max_seqlen_q is None:
         max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B else 0
     a = PrefillArgs()
-    a.mode, a.dtype, a.impl = CP_PASS_KV, CP_BF16, impl
-    a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.cp = B, Hq, k.shape[1], d, cp
+    a.mode, a.dtype, a.impl = mode, CP_BF16, impl
+    a.num_seqs, a.num_q_heads, a.head_dim, a.cp = B, Hq, d, cp
     a.softmax_scale, a.total_q, a.max_seqlen_q = softmax_scale, Nq, max_seqlen_q
     a.q_shard = a.kv_shard = -1
-    a.cu_seqlens_q, a.q, a.k, a.v = _ptr(cu_seqlens_q), _ptr(q), _ptr(k), _ptr(v)
+    a.cu_seqlens_q, a.q = _ptr(cu_seqlens_q), _ptr(q)
+    if mode == CP_PASS_KV:
+        _dev(k, "k", torch.bfloat16)
+        _dev(v, "v", torch.bfloat16)
+        a.num_kv_heads = k.shape[1]
+        a.k, a.v = _ptr(k), _ptr(v)
+    else:
+        for n, t, dt in (("k_cache", k_cache, torch.bfloat16), ("v_cache", v_cache, torch.bfloat16),
+                         ("block_tables", block_tables, torch.int32),
+                         ("seq_lens_kv", seq_lens_kv, torch.int32)):
+            _dev(t, n, dt)
+        a.num_kv_heads = k_cache.shape[2]
+        a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
+        a.pool_pages = k_cache.shape[1]
+        a.block_tables, a.max_blocks = _ptr(block_tables), block_tables.shape[-1]
+        a.block_size, a.interleave = k_cache.shape[3], interleave
+        a.seq_lens_kv = _ptr(seq_lens_kv)
     _check(_LIB.cp_attn_prefill_fused(ctypes.byref(a), _ptr(out), _ptr(out_lse), _stream(stream)))
     return out, out_lse
 

@@ -525,8 +525,10 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
 
 cp_status cp_attn_prefill_fused(const cp_prefill_args* a, void* out, float* out_lse, void* stream) {
   REQUIRE(a != nullptr, "args is null");
-  REQUIRE(a->mode == CP_PASS_KV, "the fused prefill is pass-KV");
+  REQUIRE(a->mode == CP_PASS_KV || a->mode == CP_PASS_Q, "mode must be CP_PASS_KV or CP_PASS_Q");
   if (a->dtype != CP_BF16) return fail(CP_ERR_UNSUPPORTED, "the fused prefill takes bf16 inputs");
+  if (a->mode == CP_PASS_Q && a->impl == CP_IMPL_TCGEN05_SINGLE)
+    return fail(CP_ERR_UNSUPPORTED, "the fused pass-Q prefill runs on the two-tile kernel only");
   if (a->head_dim != 64 && a->head_dim != 128)
     return fail(CP_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", a->head_dim);
   REQUIRE(a->num_seqs >= 1 && a->num_kv_heads >= 1 && a->num_q_heads % a->num_kv_heads == 0,
@@ -536,8 +538,19 @@ cp_status cp_attn_prefill_fused(const cp_prefill_args* a, void* out, float* out_
   REQUIRE(a->total_q >= 0 && a->max_seqlen_q >= 0, "bad total_q / max_seqlen_q");
   REQUIRE(a->cu_seqlens_q != nullptr, "cu_seqlens_q is null");
   REQUIRE_PTR(a->q);
-  REQUIRE_PTR(a->k);
-  REQUIRE_PTR(a->v);
+  if (a->mode == CP_PASS_KV) {
+    REQUIRE_PTR(a->k);
+    REQUIRE_PTR(a->v);
+  } else {
+    REQUIRE_PTR(a->k_cache);
+    REQUIRE_PTR(a->v_cache);
+    REQUIRE(a->block_tables != nullptr && a->seq_lens_kv != nullptr,
+            "PASS_Q needs block_tables and seq_lens_kv");
+    REQUIRE(a->max_blocks >= 1 && a->pool_pages >= 1, "PASS_Q needs max_blocks, pool_pages >= 1");
+    REQUIRE(a->interleave >= 1, "interleave must be >= 1");
+    if (a->block_size != 16)
+      return fail(CP_ERR_UNSUPPORTED, "block_size must be 16 (got %d)", a->block_size);
+  }
   REQUIRE_PTR(out);
   REQUIRE(out_lse != nullptr, "out_lse is null");
   REQUIRE(a->debug == 0, "debug must be 0");

@@ -21,6 +21,7 @@
 // MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "sm100.cuh"
@@ -123,6 +124,30 @@ CP_DEV void page_rows(const int (&id)[NP], int t, int n_local, long long pool, i
     row[j] = (int)((((long long)rank * pool + (row[j] >= 0 ? row[j] : last_good)) * Hkv + g) * 16);
 }
 
+// Fused pass-Q: key tile t of an item -> (rank r, tile tr within r's resident tokens), walked in
+// order (ranks with no visible token skipped).  n_r: r's resident tokens any row of the item
+// sees (kv_end = position after the item's last query).
+struct RankWalk {
+  int r, tr, nt_r, n_r;
+};
+CP_DEV void walk_settle(RankWalk& k, long long kv_end, int cp, int I) {
+  while (k.tr >= k.nt_r && k.r + 1 < cp) {
+    ++k.r;
+    k.n_r = rank_local_len(kv_end, k.r, cp, I);
+    k.nt_r = (k.n_r + BN - 1) / BN;
+    k.tr = 0;
+  }
+}
+CP_DEV RankWalk walk_start(long long kv_end, int cp, int I) {
+  RankWalk k{-1, 0, 0, 0};
+  walk_settle(k, kv_end, cp, I);
+  return k;
+}
+CP_DEV void walk_next(RankWalk& k, long long kv_end, int cp, int I) {
+  ++k.tr;
+  walk_settle(k, kv_end, cp, I);
+}
+
 // blockIdx.x -> (q tile slot, sequence, kv shard, head group of `hpc` consecutive q heads).
 // Slots run heaviest first (last chunk, last tile) so long items start early.
 // `span` query rows per item: BM (one tile; head pairs) or 2 BM (two tiles of one head).
@@ -184,8 +209,13 @@ CP_DEV Work decode_work(const TcParams& p, int hpc, int span = BM) {
       return w;
     }
     w.qpos0 = C + w.q_lo;
-    w.n_local = rank_local_len(C + w.q_hi, w.p, p.cp, p.I);
-    w.ntiles = (w.n_local + BN - 1) / BN;
+    if (p.fused) {  // every rank's resident tokens any row can see, rank after rank
+      w.n_local = 0;
+      for (int r = 0; r < p.cp; ++r) w.ntiles += (rank_local_len(C + w.q_hi, r, p.cp, p.I) + BN - 1) / BN;
+    } else {
+      w.n_local = rank_local_len(C + w.q_hi, w.p, p.cp, p.I);
+      w.ntiles = (w.n_local + BN - 1) / BN;
+    }
   }
   return w;
 }
@@ -750,7 +780,8 @@ struct Layout2 {
 
 // PG: paged K/V as whole-page boxes (pass-Q, d = 128).  TT: the two "tiles" of the CTA are two
 // consecutive 128-row query tiles of one head (any G) instead of two heads of a kv group (even G).
-template <int D, bool PG, bool TT>
+// FQ: fused pass-Q, the item walks every rank's resident pages (rank after rank).
+template <int D, bool PG, bool TT, bool FQ>
 __global__ void __launch_bounds__(kThreads2, 1)
     prefill_tc2_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -768,8 +799,16 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (warp >= 2) {
       const int tile = (warp - 2) >> 2;
       const int row = (warp & 3) * 32 + lane + (TT ? tile * BM : 0);  // within the item
-      if (w.q_lo + row < w.q_hi)
-        p.lse[((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + w.h + (TT ? 0 : tile)] = -INFINITY;
+      const int hcol = w.h + (TT ? 0 : tile);
+      if (w.q_lo + row < w.q_hi) {
+        if (p.fused) {  // no visible key at all: exact attention is 0 with lse -inf
+          const long long frow = (long long)(w.q_row0 + row) * p.Hq + hcol;
+          for (int c = 0; c < D; ++c) p.out_final[frow * D + c] = __float2bfloat16_rn(0.f);
+          p.lse_final[frow] = -INFINITY;
+        } else {
+          p.lse[((long long)w.p * p.Nq + w.q_row0 + row) * p.Hq + hcol] = -INFINITY;
+        }
+      }
     }
     return;
   }
@@ -824,11 +863,19 @@ __global__ void __launch_bounds__(kThreads2, 1)
       int lastph[NSLOT];  // parity of the last fill of each slot (-1: never filled)
 #pragma unroll
       for (int i = 0; i < NSLOT; ++i) lastph[i] = -1;
-      const int32_t* trow =
-          p.mode == CP_PASS_Q ? p.tables + ((long long)w.p * p.B + w.b) * p.max_blocks : nullptr;
       int prow[BN / 16];  // pass-Q: element rows of the current tile's pages (K and V alike)
       int pid[BN / 16];   // pass-Q: page ids of the next tile, loaded one tile ahead
-      if (p.mode == CP_PASS_Q) fetch_page_ids(trow, 0, w.n_local, p.max_blocks, pid);
+      auto table_of = [&](int r) { return p.tables + ((long long)r * p.B + w.b) * p.max_blocks; };
+      const int32_t* trow = p.mode == CP_PASS_Q ? table_of(w.p) : nullptr;
+      // fused pass-Q: the key tiles walk rank 0, 1, .. in turn (FQ only)
+      const long long kv_end = w.qpos0 - w.q_lo + w.q_hi;
+      RankWalk kw{0, 0, 0, 0};
+      if constexpr (FQ) {
+        kw = walk_start(kv_end, p.cp, p.I);
+        fetch_page_ids(table_of(kw.r), kw.tr, kw.n_r, p.max_blocks, pid);
+      } else {
+        if (p.mode == CP_PASS_Q) fetch_page_ids(trow, 0, w.n_local, p.max_blocks, pid);
+      }
       bool ok = true;
       for (int i = 0; i < 2 * w.ntiles; ++i) {
         const int slot = i % NSLOT;
@@ -848,8 +895,16 @@ __global__ void __launch_bounds__(kThreads2, 1)
             tma_load_2d(dst + kb * BN * 128, map, w.g * D + kb * 64, y, bar(Ly::bFull + slot));
         } else {
           if (!isV) {  // page rows of tile t (reused for its V load)
-            page_rows(pid, t, w.n_local, p.pool, p.Hkv, w.p, w.g, p.err, prow);
-            if (t + 1 < w.ntiles) fetch_page_ids(trow, t + 1, w.n_local, p.max_blocks, pid);
+            if constexpr (FQ) {
+              page_rows(pid, kw.tr, kw.n_r, p.pool, p.Hkv, kw.r, w.g, p.err, prow);
+              RankWalk kn = kw;  // the next tile
+              walk_next(kn, kv_end, p.cp, p.I);
+              if (t + 1 < w.ntiles) fetch_page_ids(table_of(kn.r), kn.tr, kn.n_r, p.max_blocks, pid);
+              kw = kn;
+            } else {
+              page_rows(pid, t, w.n_local, p.pool, p.Hkv, w.p, w.g, p.err, prow);
+              if (t + 1 < w.ntiles) fetch_page_ids(trow, t + 1, w.n_local, p.max_blocks, pid);
+            }
           }
           if constexpr (PG) {
 #pragma unroll
@@ -962,7 +1017,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const bool row_valid = w.q_lo + rofs + row < w.q_hi;
     const long long qpos = w.qpos0 + rofs + row;
     int nvis = 0;
-    if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
+    constexpr bool walk = FQ;  // fused pass-Q: rank after rank
+    const long long kv_end = w.qpos0 - w.q_lo + w.q_hi;
+    RankWalk kw{0, 0, 0, 0};
+    if constexpr (walk) {
+      kw = walk_start(kv_end, p.cp, p.I);
+      nvis = min(kw.n_r, rank_local_len(qpos + 1, kw.r, p.cp, p.I));
+    } else {
+      if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
+    }
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < w.ntiles; ++t) {
@@ -977,8 +1040,12 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const int k0 = r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN;
         const int ke = r0 ? w.ke[0] : w.ke[1];
         lim = (int)min((long long)ke - 1, qpos) - k0;
-      } else {
+      } else if constexpr (!walk) {
         lim = nvis - 1 - t * BN;
+      } else {
+        if (kw.tr == 0 && t > 0) nvis = min(kw.n_r, rank_local_len(qpos + 1, kw.r, p.cp, p.I));
+        lim = nvis - 1 - kw.tr * BN;
+        walk_next(kw, kv_end, p.cp, p.I);
       }
       const float alpha = row_max_update(s0, s1, s2, s3, lim, p.scale_log2, m);
       // S(t) complete implies PV(t-1) complete (it was issued before QK(t)): O is stable and
@@ -1157,10 +1224,17 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
     const int smem = Layout2<D>::kAlloc;
     // pass-Q at d = 128 (page_kv): K and V pages arrive as whole-page boxes laid out
     // [page][row group][half][8 rows][128 B] in the slot
-    auto kern = tiles ? (page_kv ? prefill_tc2_kernel<D, (D == 128), true>
-                                 : prefill_tc2_kernel<D, false, true>)
-                      : (page_kv ? prefill_tc2_kernel<D, (D == 128), false>
-                                 : prefill_tc2_kernel<D, false, false>);
+    // fused pass-Q walks every rank's pages (a variant of its own, so the other kernels keep
+    // their registers)
+    const bool fq = p.fused && a.mode == CP_PASS_Q;
+    auto pick = [&](auto tt) {
+      constexpr bool TTv = decltype(tt)::value;
+      return fq ? (page_kv ? prefill_tc2_kernel<D, (D == 128), TTv, true>
+                           : prefill_tc2_kernel<D, false, TTv, true>)
+                : (page_kv ? prefill_tc2_kernel<D, (D == 128), TTv, false>
+                           : prefill_tc2_kernel<D, false, TTv, false>);
+    };
+    auto kern = tiles ? pick(std::true_type{}) : pick(std::false_type{});
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, mo, p);

@@ -231,13 +231,16 @@ typedef struct cp_prefill_args {
 cp_status cp_partial_attn_prefill(const cp_prefill_args* args, void* stream);
 
 /* ------------------------------------------------------------------------------
- * cp_attn_prefill_fused -- pass-KV prefill with the merge folded in ([PKV] Purpose: the
- * partials of all KV shards of a Q row are combined; here one work item walks every shard's
- * keys -- for a query tile of chunk c the union of the shards' visible keys is the contiguous
- * range of earlier positions -- with one online softmax, so no partial is written).
+ * cp_attn_prefill_fused -- prefill with the merge folded in ([PKV] Purpose: the partials of
+ * all KV shards / ranks of a Q row are combined; here one work item walks every shard's keys
+ * with one online softmax, so no partial is written).  CP_PASS_KV: for a query tile of chunk c
+ * the union of the shards' visible keys is the contiguous range of earlier positions.
+ * CP_PASS_Q: the item walks the resident pages of rank 0, 1, .., cp-1 in turn through their
+ * block tables ([PCP] Purpose), each row seeing a rank's tokens up to its own position.
  *
- * Same arguments as cp_partial_attn_prefill with mode CP_PASS_KV, dtype CP_BF16 and
- * q_shard = kv_shard = -1 (args->out / args->lse are not used); writes
+ * Same arguments as cp_partial_attn_prefill with dtype CP_BF16 and q_shard = kv_shard = -1
+ * (args->out / args->lse are not used; CP_PASS_Q with impl CP_IMPL_TCGEN05_SINGLE is
+ * CP_ERR_UNSUPPORTED); writes
  *   out      device bf16 [Nq][Hq][d]: exact causal attention (round to nearest even)
  *   out_lse  device f32 [Nq][Hq] natural-log LSE (NULL not allowed).
  * Equals cp_lse_merge applied to cp_partial_attn_prefill's partials, up to rounding.

@@ -235,6 +235,23 @@ def test_pass_q_reports_short_kv(lib, impl):
     assert int(err.item()) == 5
 
 
+@pytest.mark.parametrize("case", [0, 1, 2, 4, 5])
+def test_fused_pass_q_parity(lib, case):
+    """cp_attn_prefill_fused over the paged round-robin cache (every rank's resident pages in
+    one online softmax) = merged pass-Q partials of the oracle."""
+    q_lens, kv_lens, Hq, Hkv, d, dt, cp, I = PASS_Q_CASES[case]
+    x = _paged_case(len(q_lens), q_lens, kv_lens, Hq, Hkv, d, dt, cp, I, 300 + case)
+    out, lse = lib.cp_attn_prefill_fused(
+        x["q"].to(DEV), x["cu_seqlens_q"].to(DEV), cp, mode=lib.CP_PASS_Q,
+        k_cache=x["k_cache"].to(DEV), v_cache=x["v_cache"].to(DEV),
+        block_tables=x["block_tables"].to(DEV), seq_lens_kv=x["seq_lens"].to(DEV), interleave=I,
+        max_seqlen_q=max(q_lens))
+    O, L = orc.pass_q_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                               x["cu_seqlens_q"], x["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
+    Om, Lm = orc.lse_merge(O, L)
+    check_merged(out, lse, Om, Lm, what="fused pass-Q")
+
+
 # ------------------------------------------------------------------------------------ decode
 
 DECODE_CASES = [

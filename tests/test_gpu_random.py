@@ -73,6 +73,11 @@ def test_random_pass_q(lib, seed):
     O, L = orc.pass_q_partials(qh, kc, vc, tables, cu, sl, cp, I, 16, 1 / math.sqrt(d))
     what = f"pass-Q q={q_lens} kv={kv_lens} cp={cp} I={I} Hq/Hkv={Hq}/{Hkv} d={d}"
     check_partials(out, lse, O, L, what=what)
+    Om, Lm = orc.lse_merge(O, L)
+    fo, fl = lib.cp_attn_prefill_fused(
+        qh.to(DEV), cu.to(DEV), cp, mode=lib.CP_PASS_Q, k_cache=kc.to(DEV), v_cache=vc.to(DEV),
+        block_tables=tables.to(DEV), seq_lens_kv=sl.to(DEV), interleave=I, max_seqlen_q=max(q_lens))
+    check_merged(fo, fl, Om, Lm, what=what + " fused")
 
 
 @pytest.mark.parametrize("seed", range(N_CASES))
