@@ -1,4 +1,5 @@
-"""Parity at the workloads' full sizes, in the launch configuration bench.py times.
+"""Parity at the workloads' full sizes, in the launch configurations bench.py times (partials +
+merge, and the fused launches).
 
 The oracle computes sampled query rows one by one (stratified: every chunk, its first and last
 rows, row 0 and the last row, 512 rows per sequence); decode is checked on every row.
@@ -37,6 +38,8 @@ def test_pass_kv_full_size(lib, name):
     Om, Lm = orc.lse_merge(O, L)
     idx = torch.as_tensor(rows, device="cuda")
     check_merged(mo.index_select(0, idx), ml.index_select(0, idx), Om, Lm, what=f"{name} merged")
+    fo, fl = lib.cp_attn_prefill_fused(q, cu, w.cp, k, v, max_seqlen_q=w.seq_len)
+    check_merged(fo.index_select(0, idx), fl.index_select(0, idx), Om, Lm, what=f"{name} fused")
 
 
 def test_pass_q_chunked_full_size(lib):
@@ -58,6 +61,11 @@ def test_pass_q_chunked_full_size(lib):
     Om, Lm = orc.lse_merge(O, L)
     idx = torch.as_tensor(rows, device="cuda")
     check_merged(mo.index_select(0, idx), ml.index_select(0, idx), Om, Lm, what="chunked merged")
+    fo, fl = lib.cp_attn_prefill_fused(
+        dev["q"], dev["cu_seqlens_q"], w.cp, mode=lib.CP_PASS_Q, k_cache=dev["k_cache"],
+        v_cache=dev["v_cache"], block_tables=dev["block_tables"], seq_lens_kv=dev["seq_lens"],
+        interleave=w.interleave, max_seqlen_q=w.q_len)
+    check_merged(fo.index_select(0, idx), fl.index_select(0, idx), Om, Lm, what="chunked fused")
 
 
 def test_decode_full_size(lib):

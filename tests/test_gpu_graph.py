@@ -102,3 +102,30 @@ def test_prefill_path_in_a_cuda_graph(lib, fused):
             lib.cp_lse_merge(part, plse, out=out, out_lse=lse)
 
     _capture_and_replay(step, [out, lse, perm])
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_pass_q_path_in_a_cuda_graph(lib, fused):
+    """Chunked prefill over the paged round-robin cache (pass-Q): partials + merge, or the fused
+    launch that walks every rank's pages."""
+    B, q_len, kv_lens, Hq, Hkv, d, cp, I = 2, 300, [1500, 900], 8, 2, 128, 2, 8
+    x = wl.paged_inputs(B, q_len, kv_lens, Hq, Hkv, d, torch.bfloat16, cp, I, 16, 75, 76)
+    dev = {n: x[n].cuda() for n in ("q", "k_cache", "v_cache", "block_tables", "seq_lens",
+                                    "cu_seqlens_q")}
+    N = B * q_len
+    part = torch.empty(cp, N, Hq, d, device="cuda")
+    plse = torch.empty(cp, N, Hq, device="cuda")
+    out = torch.empty(N, Hq, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(N, Hq, device="cuda")
+    kw = dict(mode=lib.CP_PASS_Q, k_cache=dev["k_cache"], v_cache=dev["v_cache"],
+              block_tables=dev["block_tables"], seq_lens_kv=dev["seq_lens"], interleave=I,
+              max_seqlen_q=q_len)
+
+    def step():
+        if fused:
+            lib.cp_attn_prefill_fused(dev["q"], dev["cu_seqlens_q"], cp, out=out, out_lse=lse, **kw)
+        else:
+            lib.cp_partial_attn_prefill(dev["q"], dev["cu_seqlens_q"], cp, out=part, lse=plse, **kw)
+            lib.cp_lse_merge(part, plse, out=out, out_lse=lse)
+
+    _capture_and_replay(step, [out, lse])
