@@ -6,17 +6,22 @@
 // pass-Q (Q tile against kv rank r's round-robin resident tokens in paged storage, "[Feature]
 // Prefill Context Parallel (PCP) basic support" (PR 28718), Purpose: per-rank block tables).
 //
-// One CTA = one work item (128 query rows of one head) x (one kv shard / rank):
-//   warp 0      TMA producer: Q once, then K and V tiles (128 keys) into a 2-stage ring;
-//               paged kv arrives page by page (16 rows per copy).
-//   warp 1      TMEM owner and MMA issuer (one thread): S = Q K^T into one of two TMEM S
-//               buffers, then O += P V into the TMEM O accumulator.
-//   warps 2-5   softmax warpgroup: thread i owns query row i (TMEM lane i): reads its S row
-//               with tcgen05.ld, masks by position, keeps the running max / sum, rescales
-//               O in TMEM only when the max grows by more than 2^8, writes P (bf16) to shared
-//               memory in the 128-byte-swizzled K-major layout the MMA reads, and finally
-//               normalises O and writes the partial output and its LSE.
-// QK^T of tile t+1 runs on the tensor cores while the softmax of tile t runs.
+// Two kernels.  prefill_tc2_kernel (the default) runs two "tiles" per CTA -- two query heads of
+// one kv group, or for odd G two consecutive 128-row tiles of one head -- against one kv shard
+// / rank (or, fused, against all of them):
+//   warp 0      TMA producer: both Q tiles once, then K and V tiles (128 keys) through a
+//               4-slot ring; paged kv arrives one box per page.
+//   warp 1      TMEM owner and MMA issuer (one thread): S = Q K^T into the tile's TMEM S
+//               columns, then O += P V with P read from TMEM; order per key tile
+//               PV0(t) | QK0(t+1) | PV1(t) | QK1(t+1), so each tile's softmax overlaps the
+//               other tile's two MMAs.
+//   warps 2-9   two softmax warpgroups, one per tile: thread i owns query row i (TMEM lane i),
+//               reads its S row with tcgen05.ld, masks by position, keeps the running max /
+//               sum, rescales O in TMEM only when the max grows by more than 2^8, writes P
+//               (bf16) back over its S columns, and finally normalises O and writes the output
+//               and its LSE (TMA bulk stores of staged 32-row boxes).
+// prefill_tc1_kernel (CP_IMPL_TCGEN05_SINGLE) runs one head per CTA with a 2-stage ring and P
+// in shared memory.
 // Every wait is bounded; on expiry the CTA raises CP_ERR_TIMEOUT, drains its own copies and
 // MMAs, frees TMEM and returns.
 #include <cuda.h>
