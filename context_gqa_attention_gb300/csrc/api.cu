@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(256) merge_small_kernel(const float* __restric
                                                           float* out_lse) {
   constexpr int E = D / 32, U = kMergeUnits;
   using V = typename MergeVec<D>::T;
+  griddep_wait();  // the partials' producer may still be finishing
   // U units per warp, every load of all of them issued before any arithmetic (twice the
   // bytes in flight of one unit per warp)
   const long long u0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * U;
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ po
                                                     long long units, void* out, float* out_lse) {
   constexpr int E = D / 32;
   using V = typename MergeVec<D>::T;
+  griddep_wait();
   const long long u = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (u >= units) return;
@@ -331,6 +333,26 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ po
 }  // namespace cpattn
 
 // ============================================================================ C ABI
+// The merge is launched as a programmatic dependent of whatever kernel precedes it on the
+// stream (normally the partials' producer): its CTAs may be scheduled while that kernel's last
+// CTAs finish and wait in griddep_wait() for its completion.
+template <typename... K, typename... A>
+static cudaError_t launch_after_producer(void (*kern)(K...), unsigned grid, cudaStream_t s,
+                                         A... args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 extern "C" {
 
 const char* cp_status_string(int32_t st) {
@@ -461,20 +483,22 @@ cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32
   const unsigned nbs = (unsigned)((units + 8ll * cpattn::kMergeUnits - 1) / (8ll * cpattn::kMergeUnits));
 #define CP_MERGE_SMALL(D, BF)                                                                 \
   switch (num_partials) {                                                                   \
-    case 1: cpattn::merge_small_kernel<D, BF, 1><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
-    case 2: cpattn::merge_small_kernel<D, BF, 2><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
-    case 3: cpattn::merge_small_kernel<D, BF, 3><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
-    case 4: cpattn::merge_small_kernel<D, BF, 4><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
-    case 8: cpattn::merge_small_kernel<D, BF, 8><<<nbs, 256, 0, s>>>(partial_out, partial_lse, units, out, out_lse); break; \
-    default: cpattn::merge_kernel<D, BF><<<nb, 256, 0, s>>>(partial_out, partial_lse, num_partials, units, out, out_lse); \
+    case 1: e = launch_after_producer(cpattn::merge_small_kernel<D, BF, 1>, nbs, s, partial_out, partial_lse, units, out, out_lse); break; \
+    case 2: e = launch_after_producer(cpattn::merge_small_kernel<D, BF, 2>, nbs, s, partial_out, partial_lse, units, out, out_lse); break; \
+    case 3: e = launch_after_producer(cpattn::merge_small_kernel<D, BF, 3>, nbs, s, partial_out, partial_lse, units, out, out_lse); break; \
+    case 4: e = launch_after_producer(cpattn::merge_small_kernel<D, BF, 4>, nbs, s, partial_out, partial_lse, units, out, out_lse); break; \
+    case 8: e = launch_after_producer(cpattn::merge_small_kernel<D, BF, 8>, nbs, s, partial_out, partial_lse, units, out, out_lse); break; \
+    default: e = launch_after_producer(cpattn::merge_kernel<D, BF>, nb, s, partial_out, partial_lse, (int)num_partials, units, out, out_lse); \
   }
+  cudaError_t e = cudaSuccess;
   if (head_dim == 128) {
     if (out_dtype == CP_BF16) { CP_MERGE_SMALL(128, true) } else { CP_MERGE_SMALL(128, false) }
   } else {
     if (out_dtype == CP_BF16) { CP_MERGE_SMALL(64, true) } else { CP_MERGE_SMALL(64, false) }
   }
 #undef CP_MERGE_SMALL
-  return launched(cudaGetLastError(), "cp_lse_merge launch");
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return launched(e, "cp_lse_merge launch");
 }
 
 cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {

@@ -25,6 +25,14 @@ template <> struct Elem<__nv_bfloat16> {
 };
 
 // Chunk bounds of the load-balanced partition: b_k = floor(k*T/(2cp)).
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may
+// start while the previous kernel on the stream finishes; it waits here, before reading what
+// that kernel wrote, until the previous grid has completed and its writes are visible (no-op
+// for a normal launch).  The previous kernel may let it start early (launch_dependents) once
+// its CTAs have issued their last loads.
+CP_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+CP_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 CP_DEV int chunk_bound(int k, int T, int cp) {
   // k, T >= 0; 32-bit division whenever k*T fits (64-bit division is a long software routine)
   const unsigned long long num = (unsigned long long)k * (unsigned)T;

@@ -1064,6 +1064,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (ok)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO + tile), (uint32_t)(w.ntiles - 1) & 1u,
                                              abort_flag, p.budget));
+    // every load and MMA of the item is done: a kernel launched after this one (the merge)
+    // may be scheduled once all CTAs are here
+    griddep_launch_dependents();
     if (ok) {
       tc_fence_after();
       const long long frow = (long long)(w.q_row0 + rofs + row) * p.Hq + hcol;

@@ -329,6 +329,9 @@ cp_status cp_decode_attention(const cp_decode_args* args, void* workspace, size_
  *   partial_out  device f32 [P][rows][H][d];  partial_lse device f32 [P][rows][H].
  *   out          device [rows][H][d] of out_dtype (bf16: round to nearest even).
  *   out_lse      device f32 [rows][H] or NULL.
+ * Stream-ordered like every call; the kernel is launched as a programmatic dependent of the
+ * kernel before it on the stream (its blocks may be scheduled while that kernel finishes and
+ * wait for its completion before reading anything).
  * ---------------------------------------------------------------------------- */
 cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32_t num_partials,
                        int64_t rows, int32_t num_heads, int32_t head_dim, void* out,
