@@ -39,10 +39,9 @@ import workloads as wl  # noqa: E402
 # each from one ncu capture summarised under profiles/.  A figure is reported only while the
 # kernel's source file still has the SHA-1 the capture was taken on; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # profiles/prefill_tc2_full_prefill.md: dram read 42.04 MB + write 62.62 MB (captured on
-    # f5e76231; this source differs from it only in the header comment)
+    # profiles/prefill_tc2_full_prefill.md: dram read 42.04 MB + write 62.57 MB
     "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                "sha1": "68ebc5d45952db68ccc253897a51923c6ab12b30", "bytes": 104651264,
+                "sha1": "f72141077f3eace2e0309ce3d75b4c80a82e1d37", "bytes": 104614400,
                 "workload": "full"},
     # profiles/decode_mma_decode.md: a 16-sequence capture (1.1187 GB read + 5.36 MB written),
     # scaled to the 64-sequence workload by algorithmic bytes (4.3933e9 / 1.1181e9)
