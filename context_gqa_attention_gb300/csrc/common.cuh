@@ -24,7 +24,6 @@ template <> struct Elem<__nv_bfloat16> {
   static CP_DEV float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 };
 
-// Chunk bounds of the load-balanced partition: b_k = floor(k*T/(2cp)).
 // Programmatic dependent launch: a kernel launched with programmatic stream serialization may
 // start while the previous kernel on the stream finishes; it waits here, before reading what
 // that kernel wrote, until the previous grid has completed and its writes are visible (no-op
@@ -33,6 +32,7 @@ template <> struct Elem<__nv_bfloat16> {
 CP_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 CP_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// Chunk bounds of the load-balanced partition: b_k = floor(k*T/(2cp)).
 CP_DEV int chunk_bound(int k, int T, int cp) {
   // k, T >= 0; 32-bit division whenever k*T fits (64-bit division is a long software routine)
   const unsigned long long num = (unsigned long long)k * (unsigned)T;
