@@ -79,6 +79,31 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.cp_partial_attn_decode(ctypes.byref(d), None) == 1       # split not page multiple
 
 
+def test_fused_prefill_arguments_are_checked_on_the_host(lib):
+    """cp_attn_prefill_fused: the pass-Q form needs the paged-cache arguments and the two-tile
+    kernel; bad modes and f32 inputs are refused before any launch."""
+    fake = ctypes.c_void_p(256)
+    f = cpa.PrefillArgs()
+    f.mode, f.dtype, f.num_seqs, f.num_q_heads, f.num_kv_heads, f.head_dim, f.cp = 1, 1, 1, 8, 2, 128, 2
+    f.total_q, f.max_seqlen_q, f.q_shard, f.kv_shard = 10, 10, -1, -1
+    f.cu_seqlens_q, f.q, f.k_cache, f.v_cache = 256, 256, 256, 256
+    f.impl = cpa.CP_IMPL_TCGEN05_SINGLE
+    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 2
+    assert "two-tile" in _last(lib)[1]
+    f.impl = cpa.CP_IMPL_AUTO
+    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 1   # no block tables
+    assert "block_tables" in _last(lib)[1]
+    f.block_tables, f.seq_lens_kv, f.max_blocks, f.pool_pages, f.interleave = 256, 256, 4, 8, 8
+    f.block_size = 32
+    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 2   # block size 32
+    f.block_size = 16
+    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, None, None) == 1   # no out_lse
+    f.mode = 7
+    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 1
+    f.mode, f.dtype = 0, 0
+    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 2   # f32 inputs
+
+
 def test_decode_plan_covers_every_rank_share(lib):
     for B, Hkv, cp, I, L in [(64, 8, 2, 8, 32768), (1, 1, 1, 1, 1), (3, 2, 4, 8, 1000),
                              (64, 8, 2, 8, 1024), (2, 8, 8, 16, 5)]:
