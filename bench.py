@@ -2,15 +2,18 @@
 """Throughput of the CP partial-attention hot path on one GB300 (and N replicas under torchrun).
 
 One step = one pass of the whole path over one batch of synthetic input:
-  prefill workloads (full, long, tiny): cp_partition -> cp_partial_attn_prefill (pass-KV)
+  prefill workloads (long, full, tiny): cp_partition -> cp_partial_attn_prefill (pass-KV)
       -> cp_lse_merge;
   chunked: cp_partition of the new tokens -> cp_kv_interleave_layout -> pass-Q partial
       attention -> cp_lse_merge;
   decode: cp_kv_interleave_layout -> cp_partial_attn_decode -> cp_lse_merge.
-Default workload: full prefill (1 x 8192 tokens, 16/2 heads, d=128, bf16, cp=2), metric
-causal TFLOP/s (4*d*Hq per visible (q, k) pair).  A decode measurement (GB/s of kv read) is
-added as "secondary".  Multi-GPU: every rank runs an independent replica (CP shards are logical,
-on one GPU each) -- weak scaling, no collective on the data path.
+Default workload: long prefill (2 x 32768 tokens, 16/2 heads, d=128, bf16, cp=4), metric causal
+TFLOP/s (4*d*Hq per visible (q, k) pair).  The other workloads and forms are measured as
+"secondary" entries, each with the roofline of its dominant kernel: full prefill, the fused
+prefill launches, chunked pass-Q (partials and fused, end to end, parity), decode (two launches
+and fused, end to end, parity) and the LSE merge alone.  Multi-GPU: every rank runs an
+independent replica (CP shards are logical, on one GPU each) -- weak scaling, no collective on
+the data path.
 
 --impl reference times the float64 CPU oracle on a bounded sample of the same workload.
 """
@@ -35,19 +38,17 @@ import torch  # noqa: E402
 
 import workloads as wl  # noqa: E402
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the dominant kernels,
-# each from one ncu capture summarised under profiles/.  A figure is reported only while the
-# kernel's source file still has the SHA-1 the capture was taken on; otherwise traffic is null.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a dominant kernel,
+# each from one ncu capture of the named kernel at the recorded source SHA-1.  A figure is
+# reported only while that source file still has this SHA-1; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # profiles/prefill_tc2_full_prefill.md: dram read 42.04 MB + write 62.57 MB
-    "prefill": {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                "sha1": "f72141077f3eace2e0309ce3d75b4c80a82e1d37", "bytes": 104614400,
-                "workload": "full"},
-    # profiles/decode_mma_decode.md: a 16-sequence capture (1.1187 GB read + 5.36 MB written),
-    # scaled to the 64-sequence workload by algorithmic bytes (4.3933e9 / 1.1181e9)
-    "decode": {"file": "context_gqa_attention_gb300/csrc/decode.cu",
-               "sha1": "9b0d529eacd73ab4391495a21d18a2e537d1c074", "bytes": 4416620000,
-               "workload": "decode"},
+    # prefill_tc2_kernel<128,0,0,0> on the full prefill: dram read 42.04 MB + write 62.57 MB
+    ("prefill", "full"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
+                          "sha1": "f72141077f3eace2e0309ce3d75b4c80a82e1d37", "bytes": 104614400},
+    # decode_mma_kernel<128,4,0>: a 16-sequence capture (1.1187 GB read + 5.36 MB written),
+    # scaled to the 64-sequence decode workload by algorithmic bytes (4.3933e9 / 1.1181e9)
+    ("decode", "decode"): {"file": "context_gqa_attention_gb300/csrc/decode.cu",
+                           "sha1": "9b0d529eacd73ab4391495a21d18a2e537d1c074", "bytes": 4416620000},
 }
 
 FALLBACK_HBM_GBS = 6800.0
@@ -59,8 +60,8 @@ L2_FLUSH_BYTES = 512 * 1024 * 1024
 
 def ncu_traffic(kind, workload):
     import hashlib
-    rec = NCU_TRAFFIC.get(kind)
-    if not rec or rec.get("workload") != workload:
+    rec = NCU_TRAFFIC.get((kind, workload))
+    if not rec:
         return None
     path = os.path.join(ROOT, rec["file"])
     with open(path, "rb") as f:
@@ -187,139 +188,94 @@ def run_with_side_maps(runner, maps, attention):
         main.wait_stream(side)
 
 
-class PrefillRunner:
-    """pass-KV prefill: partition -> partial attention -> merge."""
+class Runner:
+    """A step over device buffers `self.buf` (name -> tensor).  End to end, the names in
+    `e2e_in` are copied from pinned host memory (`self.host`) every step and the names in
+    `e2e_out` are read back, through two device buffer sets so that step i+1's inputs arrive
+    and step i-1's outputs leave while step i computes (event-ordered copy streams)."""
 
-    def __init__(self, w, dev, cpa):
-        self.w, self.dev, self.cpa = w, dev, cpa
-        lens = [w.seq_len] * w.num_seqs
-        x = wl.prefill_inputs(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.dtype, w.seed)
-        self.host = {k: v.pin_memory() for k, v in x.items()}
-        self.lens = lens
-        self.N = sum(lens)
-        self.q = x["q"].to(dev)
-        self.k = x["k"].to(dev)
-        self.v = x["v"].to(dev)
-        self.cu = x["cu_seqlens"].to(dev)
-        self.sets = None  # end-to-end: two device buffer sets, filled on first use
-        cp, Hq, d = w.cp, w.num_q_heads, w.head_dim
-        self.part = torch.empty(cp, self.N, Hq, d, dtype=torch.float32, device=dev)
-        self.plse = torch.empty(cp, self.N, Hq, dtype=torch.float32, device=dev)
-        self.out = torch.empty(self.N, Hq, d, dtype=w.dtype, device=dev)
-        self.olse = torch.empty(self.N, Hq, dtype=torch.float32, device=dev)
-        self.perm = torch.empty(self.N, dtype=torch.int32, device=dev)
-        self.inv = torch.empty(self.N, dtype=torch.int32, device=dev)
-        self.so = torch.empty(cp + 1, dtype=torch.int32, device=dev)
-        self.cb = torch.empty(len(lens), 2 * cp + 1, dtype=torch.int32, device=dev)
-        self.flops = 4.0 * d * Hq * causal_pairs_pass_kv(lens)
-        self.impl = cpa.CP_IMPL_AUTO
-        self.fused = False
-        self.out_host = torch.empty(self.out.shape, dtype=w.dtype).pin_memory()
+    e2e_in = ()
+    e2e_out = ("out",)
+    e2e_note = ""
 
-    def step(self, ev=None):
-        cpa, w = self.cpa, self.w
-        run_with_side_maps(
-            self, lambda: cpa.cp_partition(self.cu, w.cp, self.N, self.perm, self.inv, self.so,
-                                           self.cb),
-            lambda: self._attention(ev))
+    def __init__(self, dev, cpa):
+        self.dev, self.cpa = dev, cpa
+        self.buf = {}
+        self.host = {}
+        self._sets = None
+        self.e2e_mode = False  # a step of the end-to-end loop (e.g. also writes new kv)
 
-    def _attention(self, ev=None):
-        cpa, w = self.cpa, self.w
-        if self.fused:  # every kv shard walked inside one item: final output, no partials
-            if ev is not None:
-                ev[0].record()
-            cpa.cp_attn_prefill_fused(self.q, self.cu, w.cp, self.k, self.v,
-                                      max_seqlen_q=max(self.lens), out=self.out, out_lse=self.olse,
-                                      impl=self.impl)
-            if ev is not None:
-                ev[1].record()
-            return
-        if ev is not None:
-            ev[0].record()
-        cpa.cp_partial_attn_prefill(self.q, self.cu, w.cp, k=self.k, v=self.v,
-                                    max_seqlen_q=max(self.lens), out=self.part, lse=self.plse,
-                                    impl=self.impl)
-        if ev is not None:
-            ev[1].record()
-        cpa.cp_lse_merge(self.part, self.plse, out=self.out, out_lse=self.olse)
-
-    @property
-    def launches_per_step(self):
-        return 2 if self.fused else 3
-
-    def _use(self, st):
-        self.q, self.k, self.v, self.cu, self.out, self.olse = (
-            st["q"], st["k"], st["v"], st["cu_seqlens"], st["out"], st["olse"])
+    def e2e_prepare(self):
+        """Pinned host copies of the step inputs (called once, outside any timed region)."""
+        for n in self.e2e_in:
+            if n not in self.host:
+                self.host[n] = self.buf[n].cpu().pin_memory()
 
     def e2e_run(self, steps, stream):
-        """Host buffers in, host result out, every step: pinned host -> device copies of the
-        step's inputs on one copy stream, the step on `stream`, its output copied back on a
-        second copy stream.  Two device buffer sets let step i+1's inputs arrive and step
-        i-1's output leave while step i computes (event-ordered).  Returns seconds."""
         dev = self.dev
-        if self.sets is None:
-            base = {"q": self.q, "k": self.k, "v": self.v, "cu_seqlens": self.cu,
-                    "out": self.out, "olse": self.olse}
-            other = {k: torch.empty_like(t) for k, t in base.items()}
-            self.sets = [base, other]
-            self.outs_host = [self.out_host, torch.empty_like(self.out_host).pin_memory()]
-            self.s_in = torch.cuda.Stream(dev)
-            self.s_out = torch.cuda.Stream(dev)
+        self.e2e_prepare()
+        if self._sets is None:
+            names = list(self.e2e_in) + list(self.e2e_out)
+            base = {n: self.buf[n] for n in names}
+            other = {n: torch.empty_like(t) for n, t in base.items()}
+            self._sets = [base, other]
+            self._outs_host = [{n: torch.empty(self.buf[n].shape, dtype=self.buf[n].dtype).pin_memory()
+                                for n in self.e2e_out} for _ in range(2)]
+            self._s_in = torch.cuda.Stream(dev)
+            self._s_out = torch.cuda.Stream(dev)
         ev = lambda: torch.cuda.Event()
         in_ready = [ev(), ev()]
-        in_free = [None, None]   # compute finished reading set b
+        in_free = [None, None]
         out_ready = [ev(), ev()]
-        out_free = [None, None]  # output of set b copied to the host
+        out_free = [None, None]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.e2e_mode = True
         t0.record(stream)
-        self.s_in.wait_stream(stream)
-        self.s_out.wait_stream(stream)
+        self._s_in.wait_stream(stream)
+        self._s_out.wait_stream(stream)
         for i in range(steps):
             b = i % 2
-            st = self.sets[b]
-            with torch.cuda.stream(self.s_in):
+            st = self._sets[b]
+            with torch.cuda.stream(self._s_in):
                 if in_free[b] is not None:
-                    self.s_in.wait_event(in_free[b])
-                for name in ("q", "k", "v", "cu_seqlens"):
-                    st[name].copy_(self.host[name], non_blocking=True)
-                in_ready[b].record(self.s_in)
+                    self._s_in.wait_event(in_free[b])
+                for n in self.e2e_in:
+                    st[n].copy_(self.host[n], non_blocking=True)
+                in_ready[b].record(self._s_in)
             stream.wait_event(in_ready[b])
             if out_free[b] is not None:
                 stream.wait_event(out_free[b])
-            self._use(st)
+            self.buf.update(st)
             self.step()
             done = ev()
             done.record(stream)
             in_free[b] = done
-            with torch.cuda.stream(self.s_out):
-                self.s_out.wait_event(done)
-                self.outs_host[b].copy_(st["out"], non_blocking=True)
-                out_ready[b].record(self.s_out)
+            with torch.cuda.stream(self._s_out):
+                self._s_out.wait_event(done)
+                for n in self.e2e_out:
+                    self._outs_host[b][n].copy_(st[n], non_blocking=True)
+                out_ready[b].record(self._s_out)
             out_free[b] = out_ready[b]
             out_ready[b] = ev()
-        stream.wait_stream(self.s_in)
-        stream.wait_stream(self.s_out)
+        stream.wait_stream(self._s_in)
+        stream.wait_stream(self._s_out)
         t1.record(stream)
         torch.cuda.synchronize(dev)
-        self.e2e_last = self.outs_host[(steps - 1) % 2]
-        self._use(self.sets[0])
+        self.e2e_mode = False
+        self.e2e_last = self._outs_host[(steps - 1) % 2]
+        self.buf.update(self._sets[0])
         return t0.elapsed_time(t1) / 1e3
 
     def e2e_check(self):
         """The host copy of the last pipelined step equals a fresh device-only step."""
         self.step()
         torch.cuda.synchronize(self.dev)
-        return bool(torch.equal(self.out.cpu(), self.e2e_last))
+        return all(bool(torch.equal(self.buf[n].cpu(), self.e2e_last[n])) for n in self.e2e_out)
 
     def e2e_bytes(self):
-        h2d = sum(t.numel() * t.element_size() for t in self.host.values())
-        return h2d, self.out.numel() * self.out.element_size()
-
-    def metric(self, seconds):
-        return self.flops / seconds / 1e12
-
-    def config(self):
-        return prefill_config(self.w)
+        h2d = sum(self.host[n].numel() * self.host[n].element_size() for n in self.e2e_in)
+        d2h = sum(self.buf[n].numel() * self.buf[n].element_size() for n in self.e2e_out)
+        return h2d, d2h
 
 
 def prefill_config(w):
@@ -330,47 +286,148 @@ def prefill_config(w):
             "head_dim": w.head_dim, "mode": "pass_kv"}
 
 
-class PassQRunner:
-    """chunked prefill (pass-Q): partition of the new tokens -> round-robin layout of the kv
-    -> pass-Q partial attention over the paged cache -> merge."""
+def line_config(w, ws):
+    """The `config` of a JSON line (the same for both arms)."""
+    base = (prefill_config(w) if w.kind == "pass_kv" else
+            {"workload": w.name, "global_batch": w.num_seqs, "cp": w.cp, "mode": w.kind})
+    return dict(base, l2="flushed between timed steps (512 MB write)",
+                parallelism=f"replicas x{ws} (logical CP shards on each GPU)")
+
+
+class PrefillRunner(Runner):
+    """pass-KV prefill: partition -> partial attention -> merge (or the fused launch)."""
+
+    e2e_in = ("q", "k", "v", "cu")
+    e2e_out = ("out",)
+    e2e_note = ("throughput across steps: the inputs of step i+1 and the output of step i-1 "
+                "are copied on two copy streams while step i computes (double-buffered sets)")
 
     def __init__(self, w, dev, cpa):
-        self.w, self.dev, self.cpa = w, dev, cpa
-        x = wl.workload_inputs(w)
-        self.q = x["q"].to(dev)
-        self.kc = x["k_cache"].to(dev)
-        self.vc = x["v_cache"].to(dev)
-        self.tables = x["block_tables"].to(dev)
-        self.seq_lens = x["seq_lens"].to(dev)
-        self.cu_q = x["cu_seqlens_q"].to(dev)
+        super().__init__(dev, cpa)
+        self.w = w
+        lens = [w.seq_len] * w.num_seqs
+        self.x = wl.prefill_inputs(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.dtype, w.seed)
+        self.lens = lens
+        self.N = N = sum(lens)
+        cp, Hq, d = w.cp, w.num_q_heads, w.head_dim
+        self.buf = {
+            "q": self.x["q"].to(dev), "k": self.x["k"].to(dev), "v": self.x["v"].to(dev),
+            "cu": self.x["cu_seqlens"].to(dev),
+            "part": torch.empty(cp, N, Hq, d, dtype=torch.float32, device=dev),
+            "plse": torch.empty(cp, N, Hq, dtype=torch.float32, device=dev),
+            "out": torch.empty(N, Hq, d, dtype=w.dtype, device=dev),
+            "olse": torch.empty(N, Hq, dtype=torch.float32, device=dev),
+            "perm": torch.empty(N, dtype=torch.int32, device=dev),
+            "inv": torch.empty(N, dtype=torch.int32, device=dev),
+            "so": torch.empty(cp + 1, dtype=torch.int32, device=dev),
+            "cb": torch.empty(len(lens), 2 * cp + 1, dtype=torch.int32, device=dev),
+        }
+        self.flops = 4.0 * d * Hq * causal_pairs_pass_kv(lens)
+        self.impl = cpa.CP_IMPL_AUTO
+        self.fused = False
+
+    def step(self, ev=None):
+        cpa, w, b = self.cpa, self.w, self.buf
+        run_with_side_maps(
+            self, lambda: cpa.cp_partition(b["cu"], w.cp, self.N, b["perm"], b["inv"], b["so"], b["cb"]),
+            lambda: self._attention(ev))
+
+    def _attention(self, ev=None):
+        cpa, w, b = self.cpa, self.w, self.buf
+        if ev is not None:
+            ev[0].record()
+        if self.fused:  # every kv shard walked inside one item: final output, no partials
+            cpa.cp_attn_prefill_fused(b["q"], b["cu"], w.cp, b["k"], b["v"],
+                                      max_seqlen_q=max(self.lens), out=b["out"], out_lse=b["olse"],
+                                      impl=self.impl)
+            if ev is not None:
+                ev[1].record()
+            return
+        cpa.cp_partial_attn_prefill(b["q"], b["cu"], w.cp, k=b["k"], v=b["v"],
+                                    max_seqlen_q=max(self.lens), out=b["part"], lse=b["plse"],
+                                    impl=self.impl)
+        if ev is not None:
+            ev[1].record()
+        cpa.cp_lse_merge(b["part"], b["plse"], out=b["out"], out_lse=b["olse"])
+
+    def merge_only(self):
+        b = self.buf
+        self.cpa.cp_lse_merge(b["part"], b["plse"], out=b["out"], out_lse=b["olse"])
+
+    def merge_bytes(self):
+        """Algorithmic bytes of one merge over the current partials: every partial LSE, the out
+        rows of the non-empty partials, the merged output and its LSE."""
+        b = self.buf
+        P, R, H, d = b["part"].shape
+        live = int(torch.isfinite(b["plse"]).sum().item())
+        return P * R * H * 4 + live * d * 4 + R * H * (d * b["out"].element_size() + 4)
+
+    @property
+    def launches_per_step(self):
+        return 2 if self.fused else 3
+
+    def metric(self, seconds):
+        return self.flops / seconds / 1e12
+
+    def config(self):
+        return prefill_config(self.w)
+
+
+class PassQRunner(Runner):
+    """chunked prefill (pass-Q): partition of the new tokens -> round-robin layout of the kv
+    -> pass-Q partial attention over the paged cache -> merge.  End to end, each step also
+    stores the new tokens' K/V into the paged cache (cp_kv_cache_write)."""
+
+    e2e_in = ("q", "k_new", "v_new", "tables", "seq_lens", "cu_q", "cu_kv", "start")
+    e2e_out = ("out",)
+    e2e_note = ("throughput across steps (double-buffered sets, two copy streams); every step "
+                "also writes its new tokens' K/V into the resident paged cache")
+
+    def __init__(self, w, dev, cpa):
+        super().__init__(dev, cpa)
+        self.w = w
+        self.x = x = wl.workload_inputs(w)
+        B, cp, Hq, Hkv, d = w.num_seqs, w.cp, w.num_q_heads, w.num_kv_heads, w.head_dim
+        self.N = N = B * w.q_len
         cu = [0]
         for L in x["seq_lens"].tolist():
             cu.append(cu[-1] + L)
-        self.cu_kv = torch.tensor(cu, dtype=torch.int32, device=dev)
-        self.N = w.num_seqs * w.q_len
-        cp, Hq, d = w.cp, w.num_q_heads, w.head_dim
-        self.part = torch.empty(cp, self.N, Hq, d, dtype=torch.float32, device=dev)
-        self.plse = torch.empty(cp, self.N, Hq, dtype=torch.float32, device=dev)
-        self.out = torch.empty(self.N, Hq, d, dtype=w.dtype, device=dev)
-        self.local_lens = torch.empty(cp, w.num_seqs, dtype=torch.int32, device=dev)
-        self.perm = torch.empty(self.N, dtype=torch.int32, device=dev)
-        self.inv = torch.empty(self.N, dtype=torch.int32, device=dev)
-        self.so = torch.empty(cp + 1, dtype=torch.int32, device=dev)
-        self.cb = torch.empty(w.num_seqs, 2 * cp + 1, dtype=torch.int32, device=dev)
+        g = torch.Generator().manual_seed(w.seed + 500)
+        self.buf = {
+            "q": x["q"].to(dev), "kc": x["k_cache"].to(dev), "vc": x["v_cache"].to(dev),
+            "tables": x["block_tables"].to(dev), "seq_lens": x["seq_lens"].to(dev),
+            "cu_q": x["cu_seqlens_q"].to(dev),
+            "cu_kv": torch.tensor(cu, dtype=torch.int32, device=dev),
+            # new tokens' K/V of the end-to-end step (positions kv_len - q_len ..)
+            "k_new": wl.normal((N, Hkv, d), w.dtype, g).to(dev),
+            "v_new": wl.normal((N, Hkv, d), w.dtype, g).to(dev),
+            "start": (x["seq_lens"] - w.q_len).to(dev),
+            "part": torch.empty(cp, N, Hq, d, dtype=torch.float32, device=dev),
+            "plse": torch.empty(cp, N, Hq, dtype=torch.float32, device=dev),
+            "out": torch.empty(N, Hq, d, dtype=w.dtype, device=dev),
+            "olse": torch.empty(N, Hq, dtype=torch.float32, device=dev),
+            "local_lens": torch.empty(cp, B, dtype=torch.int32, device=dev),
+            "perm": torch.empty(N, dtype=torch.int32, device=dev),
+            "inv": torch.empty(N, dtype=torch.int32, device=dev),
+            "so": torch.empty(cp + 1, dtype=torch.int32, device=dev),
+            "cb": torch.empty(B, 2 * cp + 1, dtype=torch.int32, device=dev),
+        }
         ctx = w.kv_len - w.q_len
-        pairs = sum(ctx + i + 1 for i in range(w.q_len)) * w.num_seqs
+        pairs = sum(ctx + i + 1 for i in range(w.q_len)) * B
         self.flops = 4.0 * d * Hq * pairs
         self.impl = cpa.CP_IMPL_AUTO
         self.fused = False
-        self.olse = torch.empty(self.N, Hq, dtype=torch.float32, device=dev)
 
     def step(self, ev=None):
-        cpa, w = self.cpa, self.w
+        cpa, w, b = self.cpa, self.w, self.buf
+        if self.e2e_mode:  # the new tokens' K/V into their ranks' pages before attention
+            cpa.cp_kv_cache_write(b["k_new"], b["v_new"], b["cu_q"], b["start"], b["kc"], b["vc"],
+                                  b["tables"], w.cp, w.interleave)
 
         def maps():
-            cpa.cp_partition(self.cu_q, w.cp, self.N, self.perm, self.inv, self.so, self.cb)
-            cpa.cp_kv_interleave_layout(self.cu_kv, w.cp, w.interleave, 0, w.block_size,
-                                        local_lens=self.local_lens, want_slots=False)
+            cpa.cp_partition(b["cu_q"], w.cp, self.N, b["perm"], b["inv"], b["so"], b["cb"])
+            cpa.cp_kv_interleave_layout(b["cu_kv"], w.cp, w.interleave, 0, w.block_size,
+                                        local_lens=b["local_lens"], want_slots=False)
 
         run_with_side_maps(self, maps, lambda: self._attention(ev))
 
@@ -379,28 +436,21 @@ class PassQRunner:
         return 3 if self.fused else 4
 
     def _attention(self, ev=None):
-        cpa, w = self.cpa, self.w
+        cpa, w, b = self.cpa, self.w, self.buf
+        kw = dict(mode=cpa.CP_PASS_Q, k_cache=b["kc"], v_cache=b["vc"], block_tables=b["tables"],
+                  seq_lens_kv=b["seq_lens"], interleave=w.interleave, max_seqlen_q=w.q_len,
+                  impl=self.impl)
+        if ev is not None:
+            ev[0].record()
         if self.fused:  # every rank's resident pages walked inside one item: final output
-            if ev is not None:
-                ev[0].record()
-            cpa.cp_attn_prefill_fused(self.q, self.cu_q, w.cp, mode=cpa.CP_PASS_Q,
-                                      k_cache=self.kc, v_cache=self.vc, block_tables=self.tables,
-                                      seq_lens_kv=self.seq_lens, interleave=w.interleave,
-                                      max_seqlen_q=w.q_len, out=self.out, out_lse=self.olse,
-                                      impl=self.impl)
+            cpa.cp_attn_prefill_fused(b["q"], b["cu_q"], w.cp, out=b["out"], out_lse=b["olse"], **kw)
             if ev is not None:
                 ev[1].record()
             return
-        if ev is not None:
-            ev[0].record()
-        cpa.cp_partial_attn_prefill(self.q, self.cu_q, w.cp, mode=cpa.CP_PASS_Q, k_cache=self.kc,
-                                    v_cache=self.vc, block_tables=self.tables,
-                                    seq_lens_kv=self.seq_lens, interleave=w.interleave,
-                                    max_seqlen_q=w.q_len, out=self.part, lse=self.plse,
-                                    impl=self.impl)
+        cpa.cp_partial_attn_prefill(b["q"], b["cu_q"], w.cp, out=b["part"], lse=b["plse"], **kw)
         if ev is not None:
             ev[1].record()
-        cpa.cp_lse_merge(self.part, self.plse, out=self.out, want_lse=False)
+        cpa.cp_lse_merge(b["part"], b["plse"], out=b["out"], out_lse=b["olse"])
 
     def metric(self, seconds):
         return self.flops / seconds / 1e12
@@ -413,117 +463,102 @@ class PassQRunner:
                 "mode": "pass_q"}
 
 
-class DecodeRunner:
-    """decode: interleave layout -> per-rank split partials -> merge."""
+class DecodeRunner(Runner):
+    """decode: interleave layout -> per-rank split partials -> merge.  End to end, each step
+    also stores the new token's K/V (position L-1) into the paged cache."""
 
-    def __init__(self, w, dev, cpa, on_device_values=True):
-        self.w, self.dev, self.cpa = w, dev, cpa
+    e2e_in = ("q", "k_new", "v_new", "seq_lens", "tables", "cu", "start", "cu_new")
+    e2e_out = ("out",)
+    e2e_note = ("throughput across steps (double-buffered sets, two copy streams); the paged "
+                "cache stays resident, every step writes its new token's K/V into it")
+
+    def __init__(self, w, dev, cpa):
+        super().__init__(dev, cpa)
+        self.w = w
         lens = wl.decode_lengths(w.num_seqs, w.min_len, w.max_len, w.len_seed).tolist()
         self.lens = lens
         caps = [wl.block_capacity(L, w.cp, w.interleave, w.block_size) for L in lens]
         tables, pool = wl.shuffled_block_tables(caps, w.cp, torch.Generator().manual_seed(w.table_seed))
-        Hq, Hkv, d, cp = w.num_q_heads, w.num_kv_heads, w.head_dim, w.cp
+        B, Hq, Hkv, d, cp = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.cp
         g = torch.Generator(device=dev).manual_seed(w.seed)
         shape = (cp, pool, Hkv, w.block_size, d)
-        # kv values drawn on the device (same N(0,1) recipe; the bench checks no parity)
-        self.kc = torch.randn(shape, generator=g, device=dev, dtype=w.dtype)
-        self.vc = torch.randn(shape, generator=g, device=dev, dtype=w.dtype)
-        self.q = torch.randn(w.num_seqs, Hq, d, generator=g, device=dev, dtype=w.dtype)
-        self.tables = tables.to(dev)
-        self.seq_lens = torch.tensor(lens, dtype=torch.int32, device=dev)
         cu = [0]
         for L in lens:
             cu.append(cu[-1] + L)
-        self.cu = torch.tensor(cu, dtype=torch.int32, device=dev)
-        self.ns, self.st = cpa.cp_decode_plan(w.num_seqs, Hkv, cp, w.interleave, w.block_size, max(lens))
-        P = cp * self.ns
-        self.part = torch.empty(P, w.num_seqs, Hq, d, dtype=torch.float32, device=dev)
-        self.plse = torch.empty(P, w.num_seqs, Hq, dtype=torch.float32, device=dev)
-        self.out = torch.empty(w.num_seqs, Hq, d, dtype=w.dtype, device=dev)
+        self.buf = {
+            # kv values drawn on the device (same N(0,1) recipe; ~4.4 GB would take minutes on
+            # the host), parity is checked on sampled sequences copied back
+            "kc": torch.randn(shape, generator=g, device=dev, dtype=w.dtype),
+            "vc": torch.randn(shape, generator=g, device=dev, dtype=w.dtype),
+            "q": torch.randn(B, Hq, d, generator=g, device=dev, dtype=w.dtype),
+            "k_new": torch.randn(B, Hkv, d, generator=g, device=dev, dtype=w.dtype),
+            "v_new": torch.randn(B, Hkv, d, generator=g, device=dev, dtype=w.dtype),
+            "tables": tables.to(dev),
+            "seq_lens": torch.tensor(lens, dtype=torch.int32, device=dev),
+            "start": torch.tensor([L - 1 for L in lens], dtype=torch.int32, device=dev),
+            "cu_new": torch.arange(B + 1, dtype=torch.int32, device=dev),
+            "cu": torch.tensor(cu, dtype=torch.int32, device=dev),
+            "out": torch.empty(B, Hq, d, dtype=w.dtype, device=dev),
+            "olse": torch.empty(B, Hq, dtype=torch.float32, device=dev),
+            "local_lens": torch.empty(cp, B, dtype=torch.int32, device=dev),
+        }
+        self.ns, self.st = cpa.cp_decode_plan(B, Hkv, cp, w.interleave, w.block_size, max(lens))
+        self._alloc_partials()
         self.fused = False  # two launches measured faster than the fused one
-        self.ws = torch.zeros(cpa.cp_decode_workspace_size(w.num_seqs, Hq, Hkv, d, cp, self.ns),
-                              dtype=torch.uint8, device=dev)
-        self.local_lens = torch.empty(cp, w.num_seqs, dtype=torch.int32, device=dev)
         el = torch.tensor([], dtype=w.dtype).element_size()
         pages = sum(-(-n // w.block_size) for L in lens
                     for n in [(L // (w.interleave * cp)) * w.interleave
                               + min(max(L % (w.interleave * cp) - r * w.interleave, 0), w.interleave)
                               for r in range(cp)])
-        self.bytes = (sum(lens) * Hkv * d * 2 * el + 2 * w.num_seqs * Hq * d * el + pages * 4)
-        self.kv_bytes = sum(lens) * Hkv * d * 2 * el
+        self.bytes = (sum(lens) * Hkv * d * 2 * el + 2 * B * Hq * d * el + pages * 4)
         self.pool = pool
 
+    def _alloc_partials(self):
+        w, dev = self.w, self.dev
+        P = w.cp * self.ns
+        B, Hq, Hkv, d = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
+        self.buf["part"] = torch.empty(P, B, Hq, d, dtype=torch.float32, device=dev)
+        self.buf["plse"] = torch.empty(P, B, Hq, dtype=torch.float32, device=dev)
+        self.buf["ws"] = torch.zeros(self.cpa.cp_decode_workspace_size(B, Hq, Hkv, d, w.cp, self.ns),
+                                     dtype=torch.uint8, device=dev)
+
     def resplit(self, split_tokens):
-        w = self.w
         share = self.ns * self.st  # the planned split covers the largest rank share
         self.st = split_tokens
         self.ns = -(-share // split_tokens)
-        P = w.cp * self.ns
-        Hq, d = w.num_q_heads, w.head_dim
-        self.part = torch.empty(P, w.num_seqs, Hq, d, dtype=torch.float32, device=self.dev)
-        self.plse = torch.empty(P, w.num_seqs, Hq, dtype=torch.float32, device=self.dev)
-        self.ws = torch.zeros(self.cpa.cp_decode_workspace_size(w.num_seqs, Hq, w.num_kv_heads, d,
-                                                                w.cp, self.ns),
-                              dtype=torch.uint8, device=self.dev)
+        self._alloc_partials()
 
     @property
     def launches_per_step(self):
         return 2 if self.fused else 3
 
     def step(self, ev=None):
-        cpa, w = self.cpa, self.w
+        cpa, w, b = self.cpa, self.w, self.buf
+        if self.e2e_mode:  # the new token's K/V into its rank's page before attention
+            cpa.cp_kv_cache_write(b["k_new"], b["v_new"], b["cu_new"], b["start"], b["kc"], b["vc"],
+                                  b["tables"], w.cp, w.interleave)
         run_with_side_maps(
-            self, lambda: cpa.cp_kv_interleave_layout(self.cu, w.cp, w.interleave, 0, w.block_size,
-                                                      local_lens=self.local_lens, want_slots=False),
+            self, lambda: cpa.cp_kv_interleave_layout(b["cu"], w.cp, w.interleave, 0, w.block_size,
+                                                      local_lens=b["local_lens"], want_slots=False),
             lambda: self._attention(ev))
 
     def _attention(self, ev=None):
-        cpa, w = self.cpa, self.w
+        cpa, w, b = self.cpa, self.w, self.buf
         if ev is not None:
             ev[0].record()
         if self.fused:  # partials + merge in one launch
-            cpa.cp_decode_attention(self.q, self.kc, self.vc, self.tables, self.seq_lens, w.cp,
+            cpa.cp_decode_attention(b["q"], b["kc"], b["vc"], b["tables"], b["seq_lens"], w.cp,
                                     w.interleave, num_splits=self.ns, split_tokens=self.st,
-                                    workspace=self.ws, out=self.out, want_lse=False)
+                                    workspace=b["ws"], out=b["out"], out_lse=b["olse"])
             if ev is not None:
                 ev[1].record()
             return
-        cpa.cp_partial_attn_decode(self.q, self.kc, self.vc, self.tables, self.seq_lens, w.cp,
+        cpa.cp_partial_attn_decode(b["q"], b["kc"], b["vc"], b["tables"], b["seq_lens"], w.cp,
                                    w.interleave, num_splits=self.ns, split_tokens=self.st,
-                                   out=self.part, lse=self.plse)
+                                   out=b["part"], lse=b["plse"])
         if ev is not None:
             ev[1].record()
-        cpa.cp_lse_merge(self.part, self.plse, out=self.out, want_lse=False)
-
-    def e2e_run(self, steps, stream):
-        """Every step copies its per-step inputs from pinned host memory (new query tokens,
-        sequence lengths, block tables, cumulative lengths; the paged kv cache stays resident,
-        as it would in serving) and reads the merged output back.  Returns seconds."""
-        if not hasattr(self, "host"):
-            self.host = {n: t.cpu().pin_memory() for n, t in
-                         (("q", self.q), ("seq_lens", self.seq_lens), ("tables", self.tables),
-                          ("cu", self.cu))}
-            self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(steps):
-            for n in ("q", "seq_lens", "tables", "cu"):
-                getattr(self, n).copy_(self.host[n], non_blocking=True)
-            self.step()
-            self.out_host.copy_(self.out, non_blocking=True)
-        t1.record(stream)
-        torch.cuda.synchronize(self.dev)
-        return t0.elapsed_time(t1) / 1e3
-
-    def e2e_bytes(self):
-        h2d = sum(t.numel() * t.element_size() for t in self.host.values())
-        return h2d, self.out.numel() * self.out.element_size()
-
-    def e2e_check(self):
-        last = self.out_host.clone()
-        self.step()
-        torch.cuda.synchronize(self.dev)
-        return bool(torch.equal(self.out.cpu(), last))
+        cpa.cp_lse_merge(b["part"], b["plse"], out=b["out"], out_lse=b["olse"])
 
     def metric(self, seconds):
         return self.bytes / seconds / 1e9
@@ -536,11 +571,13 @@ class DecodeRunner:
                 "splits": self.ns, "split_tokens": self.st}
 
 
-def time_steps(runner, steps, warmup, flush, dev, stream, dominant=True, stretch_s=0.0):
-    """Per-step device time (CUDA events on the launching stream), L2 flushed between steps."""
+def time_steps(runner, steps, warmup, flush, dev, stream, dominant=True, stretch_s=0.0, fn=None):
+    """Per-step device time (CUDA events on the launching stream), L2 flushed between steps.
+    `fn` (default runner.step) is the timed call; it records the dominant kernel's events."""
+    fn = fn or runner.step
     for _ in range(warmup):
         flush.zero_()
-        runner.step()
+        fn()
     torch.cuda.synchronize(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -561,7 +598,10 @@ def time_steps(runner, steps, warmup, flush, dev, stream, dominant=True, stretch
             flush.zero_()
         torch.cuda.nvtx.range_push(f"{type(runner).__name__} step {i}")  # profiler timelines
         starts[i].record(stream)
-        runner.step(dom[i])
+        if dominant:
+            fn(dom[i])
+        else:
+            fn()
         ends[i].record(stream)
         torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
@@ -573,34 +613,97 @@ def time_steps(runner, steps, warmup, flush, dev, stream, dominant=True, stretch
 
 # ------------------------------------------------------------------------------------- oracle
 
-def oracle_sample(w, rows_per_step, seed):
-    """Time the float64 oracle on a bounded, stratified sample of query rows of the workload."""
+_INPUTS = {}
+
+
+def _prefill_host_inputs(w):
+    key = (w.name, w.num_seqs, w.seq_len, w.seed)
+    if key not in _INPUTS:
+        _INPUTS[key] = wl.prefill_inputs([w.seq_len] * w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                         w.head_dim, w.dtype, w.seed)
+    return _INPUTS[key]
+
+
+def sampled_rows(w, per_seq, seed, T):
+    """Stratified query rows (global token rows) of every sequence: per_seq rows each."""
     from oracle import cp_oracle as orc
-    lens = [w.seq_len] * w.num_seqs
-    x = wl.prefill_inputs(lens, w.num_q_heads, w.num_kv_heads, w.head_dim, w.dtype, w.seed)
-    bnd = orc.chunk_bounds(w.seq_len, w.cp).tolist()
-    rows = wl.sample_rows(w.seq_len, bnd, rows_per_step, seed)
+    bnd = orc.chunk_bounds(T, w.cp).tolist()
+    rows = []
+    for b in range(w.num_seqs):
+        rows += [b * T + r for r in wl.sample_rows(T, bnd, per_seq, seed + b)]
+    return rows
+
+
+def oracle_pass_kv(w, per_seq, seed, x=None):
+    """The float64 oracle (pass-KV partials + merge) on stratified query rows of the workload.
+    Returns (causal flops of those rows, seconds, rows, (rows, O, LSE))."""
+    from oracle import cp_oracle as orc
+    x = x if x is not None else _prefill_host_inputs(w)
+    rows = sampled_rows(w, per_seq, seed, w.seq_len)
     t = time.time()
     O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], w.cp,
                                 1 / math.sqrt(w.head_dim), rows=rows)
     Om, Lm = orc.lse_merge(O, L)
     dt = time.time() - t
-    flops = 4.0 * w.head_dim * w.num_q_heads * sum(r + 1 for r in rows)
+    flops = 4.0 * w.head_dim * w.num_q_heads * sum(r % w.seq_len + 1 for r in rows)
     return flops, dt, len(rows), (rows, Om, Lm)
 
 
-def parity_line(runner, ref):
-    """Max errors of the bench's own merged output (the last device-only step) against the
-    oracle rows the CPU baseline computed (same seeded inputs)."""
+def oracle_pass_q(w, x, per_seq, seed):
+    """The float64 oracle (pass-Q partials + merge) on stratified new-query rows."""
+    from oracle import cp_oracle as orc
+    rows = sampled_rows(w, per_seq, seed, w.q_len)
+    O, L = orc.pass_q_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                               x["cu_seqlens_q"], x["seq_lens"], w.cp, w.interleave,
+                               w.block_size, 1 / math.sqrt(w.head_dim), rows=rows)
+    Om, Lm = orc.lse_merge(O, L)
+    return rows, Om, Lm
+
+
+def oracle_decode(runner, seqs):
+    """The float64 oracle (decode partials + merge) for the sampled sequences: their pages are
+    copied back to the host into a compact pool (tables renumbered) first."""
+    from oracle import cp_oracle as orc
+    w, b = runner.w, runner.buf
+    tables = b["tables"].cpu()
+    cp = w.cp
+    ids = [[int(p) for s in seqs for p in tables[r, s].tolist() if p >= 0] for r in range(cp)]
+    n = max(len(x) for x in ids)
+    shape = (cp, n) + tuple(b["kc"].shape[2:])
+    kc = torch.zeros(shape, dtype=b["kc"].dtype)
+    vc = torch.zeros(shape, dtype=b["vc"].dtype)
+    new_tables = torch.full((cp, len(seqs), tables.shape[-1]), -1, dtype=torch.int32)
+    for r in range(cp):
+        idx = torch.tensor(ids[r], dtype=torch.long, device=b["kc"].device)
+        kc[r, :len(ids[r])] = b["kc"][r].index_select(0, idx).cpu()
+        vc[r, :len(ids[r])] = b["vc"][r].index_select(0, idx).cpu()
+        remap = {p: i for i, p in enumerate(ids[r])}
+        for j, s in enumerate(seqs):
+            row = [remap[int(p)] for p in tables[r, s].tolist() if p >= 0]
+            new_tables[r, j, :len(row)] = torch.tensor(row, dtype=torch.int32)
+    q = b["q"].index_select(0, torch.tensor(seqs, device=b["q"].device)).cpu()
+    lens = torch.tensor([runner.lens[s] for s in seqs], dtype=torch.int32)
+    O, L = orc.decode_partials(q, kc, vc, new_tables, lens, cp, w.interleave, w.block_size,
+                               1 / math.sqrt(w.head_dim))
+    return orc.lse_merge(O, L)
+
+
+def parity_block(out, lse, rows, Om, Lm, what):
+    """Max errors of the GPU's merged output rows against the oracle's (same seeded inputs)."""
     import numpy as np
-    rows, Om, Lm = ref
-    idx = torch.as_tensor(rows, dtype=torch.long, device=runner.out.device)
-    out = runner.out.index_select(0, idx).double().cpu().numpy()
-    lse = runner.olse.index_select(0, idx).double().cpu().numpy()
+    idx = torch.as_tensor(rows, dtype=torch.long, device=out.device)
+    o = out.index_select(0, idx).double().cpu().numpy()
+    l = lse.index_select(0, idx).double().cpu().numpy()
     fin = np.isfinite(Lm)
-    return {"rows": len(rows), "max_abs_out": float(np.abs(out - Om).max()),
-            "max_rel_lse": float((np.abs(lse[fin] - Lm[fin]) / np.abs(Lm[fin]).clip(1e-30)).max()),
-            "tolerance": "out 1e-2 + bf16 rounding 2^-8 |O|; lse 1e-3 relative"}
+    tol = 1e-2 + (2.0 ** -8 * np.abs(Om) if out.dtype == torch.bfloat16 else 0.0)
+    err = np.abs(o - Om)
+    lrel = np.abs(l[fin] - Lm[fin]) / np.abs(Lm[fin]).clip(1e-30)
+    return {"rows": what, "max_abs_out": float(err.max()),
+            "max_rel_lse": float(lrel.max()) if lrel.size else 0.0,
+            "within_tolerance": bool((err <= tol).all() and
+                                     (np.abs(l[fin] - Lm[fin]) <= 1e-3 * np.abs(Lm[fin]) + 1e-5).all()
+                                     and np.array_equal(np.isfinite(l), fin)),
+            "tolerance": "out 1e-2 + bf16 rounding 2^-8 |O|; lse 1e-3 relative + 1e-5"}
 
 
 def blas_threads():
@@ -644,38 +747,164 @@ def max_over_ranks(x, ws, dev):
     return float(t.item())
 
 
+PREFILL_METRIC = "causal GQA prefill TFLOP/s (pass-KV partial attention + LSE merge)"
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return 0
-    w = wl.WORKLOADS[args.workload]
+    w = select_workload(args)
     if w.kind != "pass_kv":
         print(json.dumps({"impl": "reference", "unavailable": "the oracle reference arm times "
                                                              "prefill workloads only"}))
         return 0
-    rows = args.ref_rows
+    per_seq = max(args.ref_rows // w.num_seqs, 4)
+    _prefill_host_inputs(w)
     for i in range(args.warmup):
-        oracle_sample(w, max(rows // 8, 8), 9000 + i)
+        oracle_pass_kv(w, max(per_seq // 8, 4), 9000 + i)
     tot_flops, tot_t, nrows = 0.0, 0.0, 0
     for i in range(args.steps):
-        f, t, n, _ = oracle_sample(w, rows, 9100 + i)
+        f, t, n, _ = oracle_pass_kv(w, per_seq, 9100 + i)
         tot_flops += f
         tot_t += t
         nrows += n
     val = tot_flops / tot_t / 1e12
     cores = blas_threads()
     line = {
-        "impl": "reference", "metric": "causal GQA prefill TFLOP/s (pass-KV partial attention + LSE merge)",
+        "impl": "reference", "metric": PREFILL_METRIC,
         "value": val, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": prefill_config(w),
+        "config": line_config(w, ws),
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows} stratified query rows x all heads per step "
-                                   f"({nrows} rows total), float64 NumPy oracle"},
+                         "sample": f"{per_seq} stratified query rows per sequence x all heads "
+                                   f"per step ({nrows} rows total), float64 NumPy oracle"},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
+
+
+def select_workload(args):
+    w = wl.WORKLOADS[args.workload]
+    if args.batch > 0:
+        w = dataclasses.replace(w, num_seqs=args.batch)
+    if args.cp > 0:
+        w = dataclasses.replace(w, cp=args.cp)
+    if args.interleave > 0:
+        w = dataclasses.replace(w, interleave=args.interleave)
+    if args.seed >= 0:
+        w = dataclasses.replace(w, seed=args.seed)
+    return w
+
+
+def roofline(bound, kernel, work, dom_s, pk, traffic=None, algorithmic=""):
+    if bound == "tensor":
+        peak, src = pk["bf16"]
+        achieved = work / dom_s / 1e12
+        unit, psrc = "TFLOP/s", f"{src} bf16 dense (burst)"
+    else:
+        peak, src = pk["hbm"]
+        achieved = work / dom_s / 1e9
+        unit, psrc = "GB/s", f"{src} HBM copy"
+    return {"bound": bound, "kernel": kernel, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "peak_source": psrc, "traffic": traffic,
+            "algorithmic": algorithmic, "launch_ms": dom_s * 1e3}
+
+
+def e2e_block(runner, steps, stream, ws, dev, unit):
+    runner.e2e_run(3, stream)
+    e2e_s = max_over_ranks(runner.e2e_run(steps, stream), ws, dev)
+    if not runner.e2e_check():
+        raise RuntimeError("end-to-end output differs from the device-only step")
+    h2d, d2h = runner.e2e_bytes()
+    return {"value": runner.metric(e2e_s / steps) * ws, "unit": unit,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelining": runner.e2e_note,
+            "checked": "last host output == device-only step (bitwise)"}
+
+
+def prefill_kernel_name(runner):
+    if isinstance(runner, PassQRunner):
+        return ("cp_attn_prefill_fused (pass-Q, paged, ranks merged in-kernel)" if runner.fused
+                else "cp_partial_attn_prefill (pass-Q, paged)")
+    return ("cp_attn_prefill_fused (pass-KV, shards merged in-kernel)" if runner.fused
+            else "cp_partial_attn_prefill (pass-KV)")
+
+
+def measure_prefill_form(runner, fused, steps, flush, dev, stream, pk, with_traffic=None):
+    """One prefill form (partials + merge, or the fused launch) of a runner: step value and the
+    dominant kernel's roofline."""
+    runner.fused = fused
+    st, dm, _ = time_steps(runner, steps, 3, flush, dev, stream)
+    d_s = statistics.mean(dm) / 1e3
+    return {"value": runner.metric(statistics.mean(st) / 1e3), "unit": "TFLOP/s",
+            "ms_per_step": statistics.mean(st),
+            "roofline": roofline("tensor", prefill_kernel_name(runner), runner.flops, d_s, pk,
+                                 traffic=with_traffic,
+                                 algorithmic=f"{runner.flops:.4e} causal FLOP per launch")}
+
+
+def secondaries(args, primary, w, dev, stream, flush, pk, ws):
+    """Every other form and workload of the path, each with its dominant kernel's roofline."""
+    sec = {}
+    n = max(10, args.steps // 2)
+    cpa = primary.cpa
+    if isinstance(primary, PrefillRunner) and w.dtype == torch.bfloat16:
+        sec[f"{w.name}_prefill_fused"] = dict(
+            measure_prefill_form(primary, True, n, flush, dev, stream, pk), config=primary.config())
+        primary.fused = False
+        # the LSE merge alone over the primary's partials
+        primary.step()
+        mb = primary.merge_bytes()
+        st, _, _ = time_steps(primary, n, 3, flush, dev, stream, dominant=False,
+                              fn=primary.merge_only)
+        m_s = statistics.mean(st) / 1e3
+        sec["lse_merge"] = {"value": mb / m_s / 1e9, "unit": "GB/s", "config": primary.config(),
+                            "roofline": roofline("hbm", "cp_lse_merge (merge_small_kernel)", mb, m_s, pk,
+                                                 algorithmic=f"{mb:.4e} B per launch (every partial "
+                                                             "LSE, non-empty partial rows, bf16 out + LSE)")}
+    if w.name != "full":
+        fr = PrefillRunner(wl.WORKLOADS["full"], dev, cpa)
+        for fused in (False, True):
+            sec["full_prefill_fused" if fused else "full_prefill"] = dict(
+                measure_prefill_form(fr, fused, n, flush, dev, stream, pk,
+                                     with_traffic=None if fused else ncu_traffic("prefill", "full")),
+                config=fr.config())
+        del fr
+    if w.name != "chunked":
+        qr = PassQRunner(wl.WORKLOADS["chunked"], dev, cpa)
+        e = measure_prefill_form(qr, False, n, flush, dev, stream, pk)
+        rows, Om, Lm = oracle_pass_q(qr.w, qr.x, 32, 4242)
+        e["parity"] = parity_block(qr.buf["out"], qr.buf["olse"], rows, Om, Lm,
+                                   f"{len(rows)} stratified new-query rows x all heads")
+        e["e2e"] = e2e_block(qr, n, stream, ws, dev, "TFLOP/s")
+        e["config"] = qr.config()
+        sec["chunked_pass_q"] = e
+        sec["chunked_pass_q_fused"] = dict(measure_prefill_form(qr, True, n, flush, dev, stream, pk),
+                                           config=qr.config())
+        del qr
+    torch.cuda.empty_cache()
+    dr = DecodeRunner(wl.WORKLOADS["decode"], dev, cpa)
+    for fused in (False, True):
+        dr.fused = fused
+        ds, dd, _ = time_steps(dr, max(10, args.steps // 5), 3, flush, dev, stream)
+        d_s = statistics.mean(dd) / 1e3
+        e = {"value": dr.metric(statistics.mean(ds) / 1e3), "unit": "GB/s", "config": dr.config(),
+             "roofline": roofline("hbm", "cp_decode_attention (partials + merge, one launch)" if fused
+                                  else "cp_partial_attn_decode", dr.bytes, d_s, pk,
+                                  traffic=None if fused else ncu_traffic("decode", "decode"),
+                                  algorithmic=f"{dr.bytes:.4e} B per launch (KV once + q + out + tables)")}
+        seqs = [0, 1, 2, 3, 4, 5]
+        Om, Lm = oracle_decode(dr, seqs)
+        e["parity"] = parity_block(dr.buf["out"], dr.buf["olse"], seqs, Om, Lm,
+                                   f"{len(seqs)} sequences x all heads")
+        if not fused:
+            e["e2e"] = e2e_block(dr, max(10, args.steps // 5), stream, ws, dev, "GB/s")
+        sec["decode_fused" if fused else "decode"] = e
+    del dr
+    torch.cuda.empty_cache()
+    return sec
 
 
 def main():
@@ -684,12 +913,15 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="full", choices=["full", "long", "tiny", "chunked", "decode"])
+    ap.add_argument("--workload", default="long", choices=["long", "full", "tiny", "chunked", "decode"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-rows", type=int, default=256)
-    # cpu baseline: every query row of the full workload (~8-10 s of float64 oracle work)
-    ap.add_argument("--cpu-rows", type=int, default=8192)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=128,
+                    help="reference arm: stratified query rows per step (over all sequences)")
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="cpu baseline: stratified query rows per sequence (0: the workload's "
+                         "sample size, all rows when it has none)")
     ap.add_argument("--prefill-impl", default="auto", choices=["auto", "tcgen05", "simt"])
     ap.add_argument("--prefill-fused", action="store_true",
                     help="prefill as one launch (cp_attn_prefill_fused) instead of partials + merge")
@@ -715,25 +947,17 @@ def main():
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     pk = peaks()
-    w = wl.WORKLOADS[args.workload]
-    if args.batch > 0:
-        w = dataclasses.replace(w, num_seqs=args.batch)
-    if args.cp > 0:
-        w = dataclasses.replace(w, cp=args.cp)
-    if args.interleave > 0:
-        w = dataclasses.replace(w, interleave=args.interleave)
-    if args.seed >= 0:
-        w = dataclasses.replace(w, seed=args.seed)
+    w = select_workload(args)
     runner = (DecodeRunner(w, dev, cpa) if w.kind == "decode" else
               PassQRunner(w, dev, cpa) if w.kind == "pass_q" else PrefillRunner(w, dev, cpa))
     if isinstance(runner, DecodeRunner):
         runner.fused = args.decode_fused
         if args.decode_split_tokens > 0:
             runner.resplit(args.decode_split_tokens)
-    if isinstance(runner, (PrefillRunner, PassQRunner)):
+    else:
         runner.fused = args.prefill_fused
-    runner.impl = {"auto": cpa.CP_IMPL_AUTO, "tcgen05": cpa.CP_IMPL_TCGEN05,
-                   "simt": cpa.CP_IMPL_SIMT}[args.prefill_impl]
+        runner.impl = {"auto": cpa.CP_IMPL_AUTO, "tcgen05": cpa.CP_IMPL_TCGEN05,
+                       "simt": cpa.CP_IMPL_SIMT}[args.prefill_impl]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     clocks = ClockSampler(local)
@@ -752,122 +976,53 @@ def main():
     value = runner.metric(total_s / args.steps) * ws
     dom_s = statistics.mean(dom_ms) / 1e3
 
-    # end to end: host buffers, copies inside the timed region
-    if isinstance(runner, PassQRunner):
-        e2e = None
-        peak, src = pk["bf16"]
-        achieved = runner.flops / dom_s / 1e12
-        roof = {"bound": "tensor", "kernel": "cp_attn_prefill_fused (pass-Q, paged, merged in-kernel)"
-                if runner.fused else "cp_partial_attn_prefill (pass-Q, paged)",
-                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{src} bf16 dense (burst)", "traffic": None,
-                "algorithmic": f"{runner.flops:.4e} causal FLOP per launch", "launch_ms": dom_s * 1e3}
-        metric = ("causal GQA chunked-prefill TFLOP/s (pass-Q, ranks merged in-kernel)" if runner.fused
-                  else "causal GQA chunked-prefill TFLOP/s (pass-Q partial attention + LSE merge)")
-        unit = "TFLOP/s"
-    elif isinstance(runner, PrefillRunner):
-        runner.e2e_run(3, stream)
-        e2e_s = max_over_ranks(runner.e2e_run(args.steps, stream), ws, dev)
-        if not runner.e2e_check():
-            raise RuntimeError("end-to-end output differs from the device-only step")
-        h2d, d2h = runner.e2e_bytes()
-        e2e = {"value": runner.metric(e2e_s / args.steps) * ws, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "pipelining": "inputs of step i+1 and output of step i-1 copied on two copy "
-                             "streams while step i computes (double-buffered device sets)",
-               "checked": "last host output == device-only step (bitwise)"}
-        peak, src = pk["bf16"]
-        achieved = runner.flops / dom_s / 1e12
-        roof = {"bound": "tensor", "kernel": "cp_attn_prefill_fused (pass-KV, merged in-kernel)"
-                if runner.fused else "cp_partial_attn_prefill (pass-KV)",
-                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{src} bf16 dense (burst)",
-                "traffic": ncu_traffic("prefill", w.name),
-                "algorithmic": f"{runner.flops:.4e} causal FLOP per launch",
-                "launch_ms": dom_s * 1e3}
-        metric = ("causal GQA prefill TFLOP/s (pass-KV, shards merged in-kernel)" if runner.fused
-                  else "causal GQA prefill TFLOP/s (pass-KV partial attention + LSE merge)")
-        unit = "TFLOP/s"
+    if isinstance(runner, DecodeRunner):
+        roof = roofline("hbm", "cp_decode_attention (partials + merge, one launch)" if runner.fused
+                        else "cp_partial_attn_decode", runner.bytes, dom_s, pk,
+                        traffic=None if runner.fused else ncu_traffic("decode", w.name),
+                        algorithmic=f"{runner.bytes:.4e} B per launch (KV once + q + out + tables)")
+        metric, unit = "decode KV-read GB/s (partial attention + LSE merge)", "GB/s"
     else:
-        runner.e2e_run(3, stream)
-        e2e_s = max_over_ranks(runner.e2e_run(args.steps, stream), ws, dev)
-        if not runner.e2e_check():
-            raise RuntimeError("end-to-end output differs from the device-only step")
-        h2d, d2h = runner.e2e_bytes()
-        e2e = {"value": runner.metric(e2e_s / args.steps) * ws, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "checked": "last host output == device-only step (bitwise)"}
-        peak, src = pk["hbm"]
-        achieved = runner.bytes / dom_s / 1e9
-        roof = {"bound": "hbm", "kernel": "cp_partial_attn_decode", "achieved": achieved,
-                "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "peak_source": f"{src} HBM copy", "traffic": ncu_traffic("decode", w.name),
-                "launch_ms": dom_s * 1e3,
-                "algorithmic": f"{runner.bytes:.4e} B per launch (KV once + q + out + tables)"}
-        metric = "decode KV-read GB/s (partial attention + LSE merge)"
-        roof["kernel"] = "cp_decode_attention (fused partials + merge)" if runner.fused else roof["kernel"]
-        unit = "GB/s"
+        roof = roofline("tensor", prefill_kernel_name(runner), runner.flops, dom_s, pk,
+                        traffic=None if runner.fused else ncu_traffic(
+                            "prefill" if isinstance(runner, PrefillRunner) else "pass_q", w.name),
+                        algorithmic=f"{runner.flops:.4e} causal FLOP per launch")
+        metric = (PREFILL_METRIC if isinstance(runner, PrefillRunner) and not runner.fused else
+                  "causal GQA prefill TFLOP/s (" + prefill_kernel_name(runner) + ")")
+        unit = "TFLOP/s"
 
     line = {"metric": metric, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
-            "config": dict(runner.config(), l2="flushed between timed steps (512 MB write)",
-                           parallelism=f"replicas x{ws} (logical CP shards on each GPU)"),
+            "config": line_config(w, ws),
             "roofline": roof, "clocks": clk,
             "gpu_launches": runner.launches_per_step * args.steps,
             "source_sha1": source_sha1()}
-    if e2e is not None:
-        line["e2e"] = e2e
 
-    if not args.no_secondary and w.kind != "decode":
-        sec = {}
-        if (isinstance(runner, PrefillRunner) and not isinstance(runner, PassQRunner)
-                and w.dtype == torch.bfloat16):  # the fused launch takes bf16
-            # the same workload as one launch (cp_attn_prefill_fused): no partial round trip
-            runner.fused = not runner.fused
-            fs, fd, _ = time_steps(runner, max(10, args.steps // 2), 3, flush, dev, stream)
-            f_s = statistics.mean(fd) / 1e3
-            bf, bsrc = pk["bf16"]
-            sec["prefill_fused" if runner.fused else "prefill_partials"] = {
-                "value": runner.metric(statistics.mean(fs) / 1e3), "unit": "TFLOP/s",
-                "roofline": {"bound": "tensor",
-                             "kernel": "cp_attn_prefill_fused" if runner.fused else
-                             "cp_partial_attn_prefill (pass-KV)",
-                             "achieved": runner.flops / f_s / 1e12, "peak": bf, "unit": "TFLOP/s",
-                             "frac": runner.flops / f_s / 1e12 / bf,
-                             "peak_source": f"{bsrc} bf16 dense (burst)", "launch_ms": f_s * 1e3}}
-            runner.fused = not runner.fused
-        hbm, hsrc = pk["hbm"]
-        for fused in (False, True):
-            dr = DecodeRunner(wl.WORKLOADS["decode"], dev, cpa)
-            dr.fused = fused
-            ds, dd, _ = time_steps(dr, max(10, args.steps // 5), 3, flush, dev, stream)
-            d_s = statistics.mean(dd) / 1e3
-            sec["decode_fused" if fused else "decode"] = {
-                "value": dr.metric(statistics.mean(ds) / 1e3), "unit": "GB/s",
-                "config": dr.config(),
-                "roofline": {"bound": "hbm",
-                             "kernel": "cp_decode_attention (partials + merge, one launch)" if fused
-                             else "cp_partial_attn_decode (+ cp_lse_merge)",
-                             "achieved": dr.bytes / d_s / 1e9, "peak": hbm,
-                             "unit": "GB/s", "frac": dr.bytes / d_s / 1e9 / hbm,
-                             "peak_source": f"{hsrc} HBM copy", "launch_ms": d_s * 1e3}}
-            del dr
-        line["secondary"] = sec
-
+    # parity and the CPU baseline come from one oracle run over sampled rows of the workload
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and w.kind == "pass_kv":
-        f, t, n, ref = oracle_sample(w, args.cpu_rows, 777)
-        if isinstance(runner, PrefillRunner) and not runner.fused:
-            line["parity"] = parity_line(runner, ref)
+        per_seq = args.cpu_rows or w.sample_rows or w.seq_len
+        f, t, n, (rows, Om, Lm) = oracle_pass_kv(w, per_seq, 777, x=runner.x)
+        if not runner.fused:
+            runner.step()
+            torch.cuda.synchronize(dev)
+        line["parity"] = parity_block(runner.buf["out"], runner.buf["olse"], rows, Om, Lm,
+                                      f"{n} stratified query rows x all heads" if n < runner.N
+                                      else f"all {n} query rows x all heads")
         line["cpu_baseline"] = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(),
                                 "cpu_count": os.cpu_count(), "seconds": t,
-                                "rows_per_s": n * w.num_q_heads / t,
-                                "kind": "oracle",
-                                "sample": (f"all {n} query rows" if n >= w.seq_len * w.num_seqs
-                                           else f"{n} stratified query rows")
+                                "rows_per_s": n * w.num_q_heads / t, "kind": "oracle",
+                                "sample": (f"all {n} query rows" if n >= runner.N
+                                           else f"{n} stratified query rows ({per_seq} per sequence)")
                                           + f" x {w.num_q_heads} heads of the {w.name} workload, "
                                           f"float64 NumPy oracle, {t:.1f} s"}
+    if not args.no_e2e and not (isinstance(runner, PrefillRunner) and runner.fused):
+        line["e2e"] = e2e_block(runner, args.steps, stream, ws, dev, unit)
+
+    if not args.no_secondary and w.kind != "decode":
+        line["secondary"] = secondaries(args, runner, w, dev, stream, flush, pk, ws)
+
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:

@@ -12,8 +12,10 @@ never allocates); when omitted they are allocated here with ``torch.empty``.
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 import os
+import threading
 
 import torch
 
@@ -150,11 +152,36 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_CALL = threading.local()
+
+
+def _on_first_tensors_device(fn):
+    """Runs an entry point with its first tensor argument's device current (so the launch, the
+    stream and any tensor allocated here belong to that device) and makes every other tensor
+    argument check that it lives on the same device."""
+    @functools.wraps(fn)
+    def wrapper(first, *args, **kwargs):
+        if not isinstance(first, torch.Tensor) or not first.is_cuda:
+            raise CPError(1, f"{fn.__name__}: the first argument must be a CUDA tensor")
+        prev = getattr(_CALL, "device", None)
+        _CALL.device = first.device
+        try:
+            with torch.cuda.device(first.device):
+                return fn(first, *args, **kwargs)
+        finally:
+            _CALL.device = prev
+    return wrapper
+
+
 def _dev(t, name, dtype=None):
     if t is None:
         return
     if not t.is_cuda:
         raise CPError(1, f"{name} must be a CUDA tensor")
+    want = getattr(_CALL, "device", None)
+    if want is not None and t.device != want:
+        raise CPError(1, f"{name} is on {t.device} but the call runs on {want}: every tensor "
+                         "of one call must be on the same device")
     if not t.is_contiguous():
         raise CPError(1, f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
@@ -171,6 +198,7 @@ def _cp_dtype(t):
 
 # ------------------------------------------------------------------------------- entry points
 
+@_on_first_tensors_device
 def cp_partition(cu_seqlens, cp, total_tokens, perm=None, inv_perm=None, shard_offsets=None,
                  chunk_bounds=None, stream=None):
     """Load-balanced CP partition (see cpattn.h).  Returns (perm, inv_perm, shard_offsets,
@@ -190,6 +218,7 @@ def cp_partition(cu_seqlens, cp, total_tokens, perm=None, inv_perm=None, shard_o
     return perm, inv_perm, shard_offsets, chunk_bounds
 
 
+@_on_first_tensors_device
 def cp_kv_interleave_layout(cu_seq_lens, cp, interleave, total_tokens, block_size=16,
                             block_tables=None, local_lens=None, rank_of_token=None,
                             local_of_token=None, slot_of_token=None, want_slots=True, err=None,
@@ -217,6 +246,7 @@ def cp_kv_interleave_layout(cu_seq_lens, cp, interleave, total_tokens, block_siz
     return local_lens, rank_of_token, local_of_token, slot_of_token
 
 
+@_on_first_tensors_device
 def cp_kv_cache_write(k_new, v_new, cu_new, start_pos, k_cache, v_cache, block_tables, cp,
                       interleave, err=None, stream=None):
     """Store new K/V rows [N, Hkv, d] into the per-rank pools [cp, pool, Hkv, bs, d] at their
@@ -242,6 +272,7 @@ def cp_select_prefill_mode(q_len, kv_len, num_q_heads, num_kv_heads, head_dim, e
                                        elem_bytes)
 
 
+@_on_first_tensors_device
 def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=None,
                             k_cache=None, v_cache=None, block_tables=None, seq_lens_kv=None,
                             interleave=8, max_seqlen_q=None, softmax_scale=0.0,
@@ -296,6 +327,7 @@ def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=N
     return out, lse
 
 
+@_on_first_tensors_device
 def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k=None, v=None, *, mode=CP_PASS_KV, k_cache=None,
                           v_cache=None, block_tables=None, seq_lens_kv=None, interleave=8,
                           max_seqlen_q=None, softmax_scale=0.0, impl=CP_IMPL_AUTO, out=None,
@@ -350,6 +382,7 @@ def cp_decode_plan(num_seqs, num_kv_heads, cp, interleave, block_size, max_seq_l
     return ns.value, st.value
 
 
+@_on_first_tensors_device
 def cp_partial_attn_decode(q, k_cache, v_cache, block_tables, seq_lens, cp, interleave, *,
                            max_seq_len=None, num_splits=None, split_tokens=None, softmax_scale=0.0,
                            out=None, lse=None, err=None, stream=None):
@@ -409,6 +442,7 @@ def cp_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, cp, 
     return n.value
 
 
+@_on_first_tensors_device
 def cp_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, cp, interleave, *,
                         max_seq_len=None, num_splits=None, split_tokens=None, softmax_scale=0.0,
                         workspace=None, out=None, out_lse=None, want_lse=True, err=None,
@@ -443,6 +477,7 @@ def cp_decode_attention(q, k_cache, v_cache, block_tables, seq_lens, cp, interle
 NOALLOC_SCRATCH_BYTES = 48 * 1024 * 1024
 
 
+@_on_first_tensors_device
 def cp_decode_attention_noalloc(q, k_cache, v_cache, block_tables, seq_lens, cp, interleave,
                                 out, *, num_splits, split_tokens, softmax_scale=0.0, out_lse=None,
                                 err=None, stream=None):
@@ -466,6 +501,7 @@ def cp_decode_attention_noalloc(q, k_cache, v_cache, block_tables, seq_lens, cp,
     return out, out_lse
 
 
+@_on_first_tensors_device
 def cp_lse_merge(partial_out, partial_lse, out=None, out_dtype=torch.bfloat16, out_lse=None,
                  want_lse=True, stream=None):
     """Merge partials [P, rows, H, d] / [P, rows, H] into out [rows, H, d] (+ lse [rows, H])."""

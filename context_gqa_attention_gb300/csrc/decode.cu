@@ -11,8 +11,6 @@
 // contiguous) per warp per iteration, and all of a page's loads are issued before its math.
 #include <math.h>
 
-#include <mutex>
-
 #include <cuda.h>
 
 #include "common.cuh"
@@ -792,61 +790,4 @@ cudaError_t cp_launch_decode_fused(const cp_decode_args& a, float scale, const C
   p.final_lse = out_lse;
   dim3 grid(a.num_splits, a.num_kv_heads, a.cp * a.num_seqs);
   return launch_all<true>(p, a, grid, s);
-}
-
-// ------------------------------------------------------------------------------ no allocation
-// Scratch for cp_decode_attention_noalloc: one array per GPU that loads this library, held until
-// the process exits.  Host code must not use the symbol's host-side name as a device pointer;
-// the device address is looked up once per device with cudaGetSymbolAddress.
-static __device__ __align__(256) unsigned char g_decode_scratch[CP_NOALLOC_SCRATCH_BYTES];
-
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of this device's scratch array (the device must be current).
-cudaError_t static_scratch(void** ptr) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* addr = nullptr;
-    e = cudaGetSymbolAddress(&addr, g_decode_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = addr;
-  }
-  *ptr = g_scratch_addr[dev];
-  return cudaSuccess;
-}
-}  // namespace
-
-extern "C" cp_status cp_decode_attention_noalloc(const cp_decode_args* a, void* out,
-                                                 float* out_lse, void* stream) {
-  const cp_status st = cp_check_decode_args_for_fused(a, out);
-  if (st != CP_OK) return st;
-  size_t ol = 0, oo = 0;
-  const size_t need = cp_decode_ws_layout(a->num_seqs, a->num_q_heads, a->num_kv_heads,
-                                          a->head_dim, a->cp * a->num_splits, &ol, &oo);
-  if (need > CP_NOALLOC_SCRATCH_BYTES)
-    return cp_fail_detail(CP_ERR_INVALID_ARG,
-                          "cp_decode_attention_noalloc needs %zu bytes of scratch but its static "
-                          "array holds %zu: use fewer splits or a smaller batch",
-                          need, (size_t)CP_NOALLOC_SCRATCH_BYTES);
-  void* ws = nullptr;
-  cudaError_t e = static_scratch(&ws);
-  if (e != cudaSuccess) return cp_launch_status(e, "static scratch address");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the arrival counters must start at zero whatever an earlier call left behind
-  e = cudaMemsetAsync(ws, 0, ol, s);
-  if (e != cudaSuccess) return cp_launch_status(e, "static scratch clear");
-  CpDecodeWorkspace w;
-  w.counters = static_cast<int32_t*>(ws);
-  w.partial_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + ol);
-  w.partial_out = reinterpret_cast<float*>(static_cast<char*>(ws) + oo);
-  const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
-  return cp_launch_status(cp_launch_decode_fused(*a, scale, w, out, out_lse, s),
-                          "fused decode (static scratch) launch");
 }

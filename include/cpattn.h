@@ -346,12 +346,15 @@ cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32
  * memory pool and hands out none after start-up, or a fixed-footprint serving process that
  * must not allocate per request.  This entry point takes the same arguments as
  * cp_decode_attention minus the workspace and uses instead a scratch array built into the
- * library (CP_NOALLOC_SCRATCH_BYTES = 48 MiB per GPU, present on every GPU that loads the
- * library until the process exits).  It allocates and frees nothing.
+ * library (CP_NOALLOC_SCRATCH_BYTES = 48 MiB per GPU).  The array lives in a module of its own:
+ * a process holds it on a GPU from its first call of this entry point there until it exits;
+ * the other entry points never load it.  It allocates and frees nothing.
  *   - Sizes whose scratch (cp_decode_workspace_size) exceeds CP_NOALLOC_SCRATCH_BYTES are
  *     rejected with CP_ERR_INVALID_ARG and a message naming both sizes.
- *   - The first call on a device looks up the array's device address (once per device, with
- *     that device current); make that first call before any stream capture.
+ *   - The first call in a CUDA context looks up the array's device address (with that
+ *     context's device current) and loads the array's module; make that first call before
+ *     any stream capture.  A context that is destroyed and recreated (cudaDeviceReset) is
+ *     recognised by its context id, and its first call looks the address up again.
  *   - Every call shares the one array: calls that overlap on the GPU (other streams, other
  *     threads) race and must be serialised by the caller.  Each call clears the array's
  *     arrival counters on `stream` before its launch.

@@ -1,12 +1,19 @@
 """Hot paths captured in a CUDA graph and replayed: same results (bitwise) as the eager calls,
-over several replays.  The pages turn prefill CP off under full CUDA graphs; here the
-prefill path (partition -> partials -> merge, or the fused launch) and the decode path (layout
--> split partials -> merge, or the fused launch with its self-resetting counters) are
-capturable: every call is stream-ordered and allocates nothing when its outputs are given."""
+over several replays, and the replayed results equal the float64 oracle within the parity
+tolerances (so a fault shared by the eager and the captured call, such as a stale tensor map,
+cannot pass).  The pages turn prefill CP off under full CUDA graphs ("[Feature] Prefill Context
+Parallel (PCP) basic support", code-review summary); here the prefill path (partition ->
+partials -> merge, or the fused launch) and the decode path (layout -> split partials -> merge,
+or the fused launch with its self-resetting counters) are capturable: every call is
+stream-ordered and allocates nothing when its outputs are given."""
+import math
+
 import pytest
 import torch
 
+from oracle import cp_oracle as orc
 import workloads as wl
+from tests.parity_util import check_merged
 
 pytestmark = pytest.mark.gpu
 
@@ -38,11 +45,17 @@ def _decode_setup(lib):
     dev = {n: x[n].cuda() for n in ("q", "k_cache", "v_cache", "block_tables", "seq_lens")}
     cu = torch.tensor([0] + torch.tensor(lens).cumsum(0).tolist(), dtype=torch.int32, device="cuda")
     ns, st = lib.cp_decode_plan(B, Hkv, cp, I, 16, max(lens))
-    return B, Hq, Hkv, d, cp, I, lens, dev, cu, ns, st
+    return B, Hq, Hkv, d, cp, I, lens, dev, cu, ns, st, x
+
+
+def _decode_oracle(x, lens, cp, I, d):
+    O, L = orc.decode_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                               x["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
+    return orc.lse_merge(O, L)
 
 
 def test_decode_path_in_a_cuda_graph(lib):
-    B, Hq, Hkv, d, cp, I, lens, dev, cu, ns, st = _decode_setup(lib)
+    B, Hq, Hkv, d, cp, I, lens, dev, cu, ns, st, x = _decode_setup(lib)
     part = torch.empty(cp * ns, B, Hq, d, device="cuda")
     plse = torch.empty(cp * ns, B, Hq, device="cuda")
     out = torch.empty(B, Hq, d, dtype=torch.bfloat16, device="cuda")
@@ -57,12 +70,14 @@ def test_decode_path_in_a_cuda_graph(lib):
         lib.cp_lse_merge(part, plse, out=out, out_lse=lse)
 
     _capture_and_replay(step, [out, lse])
+    Om, Lm = _decode_oracle(x, lens, cp, I, d)
+    check_merged(out, lse, Om, Lm, "decode graph replay")
 
 
 def test_fused_decode_in_a_cuda_graph(lib):
     """The arrival counters in the workspace return to zero after every launch, so the same
     captured launch replays correctly."""
-    B, Hq, Hkv, d, cp, I, lens, dev, cu, ns, st = _decode_setup(lib)
+    B, Hq, Hkv, d, cp, I, lens, dev, cu, ns, st, x = _decode_setup(lib)
     ws = torch.zeros(lib.cp_decode_workspace_size(B, Hq, Hkv, d, cp, ns), dtype=torch.uint8,
                      device="cuda")
     out = torch.empty(B, Hq, d, dtype=torch.bfloat16, device="cuda")
@@ -74,6 +89,8 @@ def test_fused_decode_in_a_cuda_graph(lib):
                                 workspace=ws, out=out, out_lse=lse)
 
     _capture_and_replay(step, [out, lse])
+    Om, Lm = _decode_oracle(x, lens, cp, I, d)
+    check_merged(out, lse, Om, Lm, "fused decode graph replay")
 
 
 @pytest.mark.parametrize("fused", [False, True])
@@ -102,6 +119,10 @@ def test_prefill_path_in_a_cuda_graph(lib, fused):
             lib.cp_lse_merge(part, plse, out=out, out_lse=lse)
 
     _capture_and_replay(step, [out, lse, perm])
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], cp, 1 / math.sqrt(d))
+    Om, Lm = orc.lse_merge(O, L)
+    check_merged(out, lse, Om, Lm, f"prefill graph replay (fused={fused})")
+    assert perm.cpu().numpy().tolist() == orc.partition(lens, cp)["perm"].tolist()
 
 
 @pytest.mark.parametrize("fused", [False, True])
@@ -129,3 +150,7 @@ def test_pass_q_path_in_a_cuda_graph(lib, fused):
             lib.cp_lse_merge(part, plse, out=out, out_lse=lse)
 
     _capture_and_replay(step, [out, lse])
+    O, L = orc.pass_q_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                               x["cu_seqlens_q"], x["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
+    Om, Lm = orc.lse_merge(O, L)
+    check_merged(out, lse, Om, Lm, f"pass-Q graph replay (fused={fused})")

@@ -1,16 +1,20 @@
 """cp_decode_attention_noalloc: the decode entry point for callers that cannot allocate device
 memory when they call it (a framework that owns the whole memory pool, a fixed-footprint
 serving process).  It must give the same result as cp_decode_attention, which takes a caller-
-allocated workspace, and keep doing so on consecutive calls that share its built-in scratch.
+allocated workspace, and keep doing so on consecutive calls that share its built-in scratch;
+each call's output is also checked against the float64 oracle (decode partials + LSE merge).
 
 Collected last on purpose; it passes alone in a fresh process and after the other tests.
 """
 import ctypes
+import math
 
 import pytest
 import torch
 
+from oracle import cp_oracle as orc
 import workloads as wl
+from tests.parity_util import check_merged
 
 pytestmark = pytest.mark.gpu
 
@@ -24,11 +28,14 @@ def _case(seed):
     x = wl.paged_inputs(B, 1, lens, Hq, Hkv, d, torch.bfloat16, cp, I, 16, seed + 1, seed + 2,
                         q_is_decode=True)
     dev = {n: x[n].to(DEV) for n in ("q", "k_cache", "v_cache", "block_tables", "seq_lens")}
-    return dev, B, Hq, Hkv, d, cp, I, max(lens)
+    return dev, B, Hq, Hkv, d, cp, I, max(lens), x
 
 
 def test_noalloc_matches_workspace_entry_point_twice(lib):
-    dev, B, Hq, Hkv, d, cp, I, maxlen = _case(901)
+    dev, B, Hq, Hkv, d, cp, I, maxlen, x = _case(901)
+    O, L = orc.decode_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
+                               x["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
+    Om, Lm = orc.lse_merge(O, L)
     ns, st = lib.cp_decode_plan(B, Hkv, cp, I, 16, maxlen)
     assert lib.cp_decode_workspace_size(B, Hq, Hkv, d, cp, ns) <= lib.NOALLOC_SCRATCH_BYTES
     ref, ref_lse = lib.cp_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"],
@@ -45,6 +52,7 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
         fin = torch.isfinite(ref_lse)
         assert torch.equal(torch.isfinite(lse), fin)
         assert ((lse[fin] - ref_lse[fin]).abs() <= 1e-3 * ref_lse[fin].abs() + 1e-5).all(), call
+        check_merged(out, lse, Om, Lm, f"no-alloc decode, call {call}")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
