@@ -57,7 +57,8 @@ class PrefillArgs(ctypes.Structure):
         ("block_tables", _vp), ("max_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("interleave", ctypes.c_int32), ("q_shard", ctypes.c_int32), ("kv_shard", ctypes.c_int32),
         ("total_q", ctypes.c_int32), ("debug", ctypes.c_int32), ("out", _vp), ("lse", _vp),
-        ("err", _vp),
+        ("err", _vp), ("cu_seqlens_kv", _vp), ("total_kv", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -188,6 +189,19 @@ def _dev(t, name, dtype=None):
         raise CPError(1, f"{name} must be {dtype} (got {t.dtype})")
 
 
+def _kv_source(a, k, v, cu_seqlens_kv, dtype):
+    """PASS_KV operands: k, v [Nkv, Hkv, d] and, for a cached context, cu_seqlens_kv [B + 1]."""
+    _dev(k, "k", dtype)
+    _dev(v, "v", dtype)
+    if k is None or v is None or k.shape != v.shape:
+        raise CPError(1, "PASS_KV needs k and v of the same shape [Nkv, Hkv, d]")
+    a.num_kv_heads = k.shape[1]
+    a.k, a.v = _ptr(k), _ptr(v)
+    if cu_seqlens_kv is not None:
+        _dev(cu_seqlens_kv, "cu_seqlens_kv", torch.int32)
+        a.cu_seqlens_kv, a.total_kv = _ptr(cu_seqlens_kv), k.shape[0]
+
+
 def _cp_dtype(t):
     if t.dtype == torch.bfloat16:
         return CP_BF16
@@ -274,14 +288,16 @@ def cp_select_prefill_mode(q_len, kv_len, num_q_heads, num_kv_heads, head_dim, e
 
 @_on_first_tensors_device
 def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=None,
-                            k_cache=None, v_cache=None, block_tables=None, seq_lens_kv=None,
-                            interleave=8, max_seqlen_q=None, softmax_scale=0.0,
+                            cu_seqlens_kv=None, k_cache=None, v_cache=None, block_tables=None,
+                            seq_lens_kv=None, interleave=8, max_seqlen_q=None, softmax_scale=0.0,
                             impl=CP_IMPL_AUTO, q_shard=-1, kv_shard=-1, out=None, lse=None,
                             err=None, debug=0, stream=None):
     """Partial attention of every (Q shard, KV shard) pair (see cpattn.h).
 
-    q: [Nq, Hq, d].  PASS_KV: k, v [Nq, Hkv, d].  PASS_Q: k_cache/v_cache
-    [cp, pool, Hkv, 16, d], block_tables int32 [cp, B, max_blocks], seq_lens_kv int32 [B].
+    q: [Nq, Hq, d].  PASS_KV: k, v [Nkv, Hkv, d]; with cu_seqlens_kv (int32 [B + 1]) each
+    sequence's queries are the last of its kv tokens (a cached context before them), else
+    Nkv = Nq and q, k, v share cu_seqlens_q.  PASS_Q: k_cache/v_cache [cp, pool, Hkv, 16, d],
+    block_tables int32 [cp, B, max_blocks], seq_lens_kv int32 [B].
     Returns (out [cp, Nq, Hq, d] f32, lse [cp, Nq, Hq] f32).
     """
     load()
@@ -308,10 +324,7 @@ def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=N
     a.max_seqlen_q = max_seqlen_q
     a.cu_seqlens_q, a.q, a.out, a.lse, a.err = _ptr(cu_seqlens_q), _ptr(q), _ptr(out), _ptr(lse), _ptr(err)
     if mode == CP_PASS_KV:
-        _dev(k, "k", q.dtype)
-        _dev(v, "v", q.dtype)
-        a.num_kv_heads = k.shape[1]
-        a.k, a.v = _ptr(k), _ptr(v)
+        _kv_source(a, k, v, cu_seqlens_kv, q.dtype)
     else:
         _dev(k_cache, "k_cache", q.dtype)
         _dev(v_cache, "v_cache", q.dtype)
@@ -328,13 +341,14 @@ def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=N
 
 
 @_on_first_tensors_device
-def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k=None, v=None, *, mode=CP_PASS_KV, k_cache=None,
-                          v_cache=None, block_tables=None, seq_lens_kv=None, interleave=8,
-                          max_seqlen_q=None, softmax_scale=0.0, impl=CP_IMPL_AUTO, out=None,
-                          out_lse=None, stream=None):
+def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k=None, v=None, *, mode=CP_PASS_KV,
+                          cu_seqlens_kv=None, k_cache=None, v_cache=None, block_tables=None,
+                          seq_lens_kv=None, interleave=8, max_seqlen_q=None, softmax_scale=0.0,
+                          impl=CP_IMPL_AUTO, out=None, out_lse=None, stream=None):
     """Prefill with the merge folded in (see cpattn.h): exact causal attention out [Nq, Hq, d]
-    bf16 and lse [Nq, Hq] f32 without partials.  PASS_KV: k, v [Nq, Hkv, d].  PASS_Q: the paged
-    round-robin cache as in cp_partial_attn_prefill (every rank's resident tokens in one pass)."""
+    bf16 and lse [Nq, Hq] f32 without partials.  PASS_KV: k, v [Nkv, Hkv, d] (cu_seqlens_kv as
+    in cp_partial_attn_prefill).  PASS_Q: the paged round-robin cache as in
+    cp_partial_attn_prefill (every rank's resident tokens in one pass)."""
     load()
     Nq, Hq, d = q.shape
     B = cu_seqlens_q.numel() - 1
@@ -354,10 +368,7 @@ def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k=None, v=None, *, mode=CP_PASS_K
     a.q_shard = a.kv_shard = -1
     a.cu_seqlens_q, a.q = _ptr(cu_seqlens_q), _ptr(q)
     if mode == CP_PASS_KV:
-        _dev(k, "k", torch.bfloat16)
-        _dev(v, "v", torch.bfloat16)
-        a.num_kv_heads = k.shape[1]
-        a.k, a.v = _ptr(k), _ptr(v)
+        _kv_source(a, k, v, cu_seqlens_kv, torch.bfloat16)
     else:
         for n, t, dt in (("k_cache", k_cache, torch.bfloat16), ("v_cache", v_cache, torch.bfloat16),
                          ("block_tables", block_tables, torch.int32),

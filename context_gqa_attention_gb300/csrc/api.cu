@@ -501,6 +501,32 @@ cp_status cp_lse_merge(const float* partial_out, const float* partial_lse, int32
   return launched(e, "cp_lse_merge launch");
 }
 
+// The kv operands of a prefill call: contiguous k / v (PASS_KV, optionally with their own
+// per-sequence lengths) or the paged round-robin pools (PASS_Q).
+static cp_status check_kv_source(const cp_prefill_args* a) {
+  if (a->mode == CP_PASS_KV) {
+    REQUIRE_PTR(a->k);
+    REQUIRE_PTR(a->v);
+    if (a->cu_seqlens_kv != nullptr) {
+      REQUIRE(a->total_kv >= 0, "total_kv must be >= 0");
+      REQUIRE(a->total_kv > 0 || a->total_q == 0,
+              "total_kv = 0 with %d query rows: every sequence with queries needs at least as "
+              "many kv tokens", a->total_q);
+    }
+  } else {
+    REQUIRE_PTR(a->k_cache);
+    REQUIRE_PTR(a->v_cache);
+    REQUIRE(a->cu_seqlens_kv == nullptr, "cu_seqlens_kv is a PASS_KV argument (PASS_Q takes seq_lens_kv)");
+    REQUIRE(a->block_tables != nullptr && a->seq_lens_kv != nullptr,
+            "PASS_Q needs block_tables and seq_lens_kv");
+    REQUIRE(a->max_blocks >= 1 && a->pool_pages >= 1, "PASS_Q needs max_blocks, pool_pages >= 1");
+    REQUIRE(a->interleave >= 1, "interleave must be >= 1");
+    if (a->block_size != 16)
+      return fail(CP_ERR_UNSUPPORTED, "block_size must be 16 (got %d)", a->block_size);
+  }
+  return CP_OK;
+}
+
 cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   REQUIRE(a != nullptr, "args is null");
   REQUIRE(a->mode == CP_PASS_KV || a->mode == CP_PASS_Q, "mode must be CP_PASS_KV or CP_PASS_Q");
@@ -522,19 +548,8 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   REQUIRE_PTR(a->q);
   REQUIRE_PTR(a->out);
   REQUIRE(a->lse != nullptr, "lse is null");
-  if (a->mode == CP_PASS_KV) {
-    REQUIRE_PTR(a->k);
-    REQUIRE_PTR(a->v);
-  } else {
-    REQUIRE_PTR(a->k_cache);
-    REQUIRE_PTR(a->v_cache);
-    REQUIRE(a->block_tables != nullptr && a->seq_lens_kv != nullptr,
-            "PASS_Q needs block_tables and seq_lens_kv");
-    REQUIRE(a->max_blocks >= 1 && a->pool_pages >= 1, "PASS_Q needs max_blocks, pool_pages >= 1");
-    REQUIRE(a->interleave >= 1, "interleave must be >= 1");
-    if (a->block_size != 16)
-      return fail(CP_ERR_UNSUPPORTED, "block_size must be 16 (got %d)", a->block_size);
-  }
+  const cp_status st = check_kv_source(a);
+  if (st != CP_OK) return st;
   if (a->total_q == 0) return ok();
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
   int impl = a->impl;
@@ -562,19 +577,8 @@ cp_status cp_attn_prefill_fused(const cp_prefill_args* a, void* out, float* out_
   REQUIRE(a->total_q >= 0 && a->max_seqlen_q >= 0, "bad total_q / max_seqlen_q");
   REQUIRE(a->cu_seqlens_q != nullptr, "cu_seqlens_q is null");
   REQUIRE_PTR(a->q);
-  if (a->mode == CP_PASS_KV) {
-    REQUIRE_PTR(a->k);
-    REQUIRE_PTR(a->v);
-  } else {
-    REQUIRE_PTR(a->k_cache);
-    REQUIRE_PTR(a->v_cache);
-    REQUIRE(a->block_tables != nullptr && a->seq_lens_kv != nullptr,
-            "PASS_Q needs block_tables and seq_lens_kv");
-    REQUIRE(a->max_blocks >= 1 && a->pool_pages >= 1, "PASS_Q needs max_blocks, pool_pages >= 1");
-    REQUIRE(a->interleave >= 1, "interleave must be >= 1");
-    if (a->block_size != 16)
-      return fail(CP_ERR_UNSUPPORTED, "block_size must be 16 (got %d)", a->block_size);
-  }
+  const cp_status st = check_kv_source(a);
+  if (st != CP_OK) return st;
   REQUIRE_PTR(out);
   REQUIRE(out_lse != nullptr, "out_lse is null");
   REQUIRE(a->debug == 0, "debug must be 0");

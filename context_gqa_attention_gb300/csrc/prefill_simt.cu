@@ -15,6 +15,7 @@ struct SimtParams {
   long long pool;
   float scale_log2;
   const int32_t* cu_q;
+  const int32_t* cu_kv;  // pass-KV: kv rows per sequence (null: the query rows)
   const int32_t* seq_lens_kv;
   const void* q;
   const void* k;
@@ -80,13 +81,18 @@ __global__ void __launch_bounds__(256) prefill_simt_kernel(const SimtParams p) {
     if (p.mode == CP_PASS_KV) {
       const T* K = static_cast<const T*>(p.k);
       const T* V = static_cast<const T*>(p.v);
+      // kv tokens of the sequence (cached + new); this query sits at position C + t
+      const int kv0 = p.cu_kv ? p.cu_kv[b] : q0;
+      const int Tkv = p.cu_kv ? p.cu_kv[b + 1] - kv0 : Tq;
+      const int C = Tkv - Tq;
+      if (C < 0) bad = true;  // fewer kv tokens than new queries: flagged, the row skipped
       const int chunks[2] = {part, 2 * cp - 1 - part};
-      for (int ci = 0; ci < 2; ++ci) {
+      for (int ci = 0; ci < 2 && !bad; ++ci) {
         const int c = chunks[ci];
-        const int ks = chunk_bound(c, Tq, cp);
-        const int ke = min(chunk_bound(c + 1, Tq, cp), t + 1);
+        const int ks = chunk_bound(c, Tkv, cp);
+        const int ke = min(chunk_bound(c + 1, Tkv, cp), C + t + 1);
         for (int j = ks; j < ke; ++j) {
-          const long long kr = ((long long)(q0 + j) * p.Hkv + g) * D;
+          const long long kr = ((long long)(kv0 + j) * p.Hkv + g) * D;
           acc.key(K + kr, V + kr, lane);
         }
       }
@@ -141,6 +147,7 @@ cudaError_t cp_launch_prefill_simt(const cp_prefill_args& a, float scale, cudaSt
   p.pool = a.pool_pages;
   p.scale_log2 = scale * kLog2e;
   p.cu_q = a.cu_seqlens_q;
+  p.cu_kv = a.mode == CP_PASS_KV ? a.cu_seqlens_kv : nullptr;
   p.seq_lens_kv = a.seq_lens_kv;
   p.q = a.q;
   p.k = a.mode == CP_PASS_KV ? a.k : a.k_cache;

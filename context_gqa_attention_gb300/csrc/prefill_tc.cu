@@ -48,6 +48,7 @@ struct TcParams {
   long long pool, budget;
   float scale_log2;
   const int32_t* cu_q;
+  const int32_t* cu_kv;     // pass-KV: kv rows per sequence (null: the query rows)
   const int32_t* seq_lens_kv;
   const int32_t* tables;
   float* out;
@@ -85,7 +86,7 @@ struct Layout {
 struct Work {
   int valid, b, h, g, p;
   int q_row0, q_lo, q_hi;   // first token-major row; tile rows [q_lo, q_hi) of the sequence
-  long long qpos0;          // position of row q_lo
+  long long qpos0;          // position of row q_lo (cached context + q_lo)
   int kv_row0;              // pass-KV: first token-major kv row of the sequence
   int ks[2], ke[2], nt[2];  // pass-KV key ranges (positions) and their tile counts
   int n_local;              // pass-Q: resident tokens of rank p that any row can see
@@ -186,25 +187,37 @@ CP_DEV Work decode_work(const TcParams& p, int hpc, int span = BM) {
   w.g = w.h / (p.Hq / p.Hkv);
   w.q_row0 = q0 + w.q_lo;
   w.ntiles = 0;
-  if (p.mode == CP_PASS_KV && p.fused) {  // the union of all shards' keys: [0, q_hi)
-    w.qpos0 = w.q_lo;
-    w.kv_row0 = q0;
-    w.ks[0] = 0;
-    w.ke[0] = w.q_hi;
-    w.nt[0] = (w.q_hi + BN - 1) / BN;
-    w.ks[1] = w.ke[1] = w.nt[1] = 0;
-    w.ntiles = w.nt[0];
-  } else if (p.mode == CP_PASS_KV) {
-    w.qpos0 = w.q_lo;
-    w.kv_row0 = q0;
+  if (p.mode == CP_PASS_KV) {
+    // kv tokens of the sequence (cached + new); the queries are its last Tq positions
+    int kv0 = q0, Tkv = Tq;
+    if (p.cu_kv != nullptr) {
+      kv0 = p.cu_kv[w.b];
+      Tkv = p.cu_kv[w.b + 1] - kv0;
+    }
+    const int C = Tkv - Tq;
+    if (C < 0) {  // fewer kv tokens than new queries: flagged, the item is skipped
+      report(p.err, CP_ERR_DEVICE_BOUNDS);
+      w.valid = 0;
+      return w;
+    }
+    w.qpos0 = C + w.q_lo;
+    w.kv_row0 = kv0;
+    if (p.fused) {  // the union of all shards' keys: positions [0, C + q_hi)
+      w.ks[0] = 0;
+      w.ke[0] = C + w.q_hi;
+      w.nt[0] = (w.ke[0] + BN - 1) / BN;
+      w.ks[1] = w.ke[1] = w.nt[1] = 0;
+      w.ntiles = w.nt[0];
+    } else {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int ch = i == 0 ? w.p : 2 * p.cp - 1 - w.p;
-      w.ks[i] = chunk_bound(ch, Tq, p.cp);
-      w.ke[i] = min(chunk_bound(ch + 1, Tq, p.cp), w.q_hi);  // positions < q_hi
-      if (w.ke[i] < w.ks[i]) w.ke[i] = w.ks[i];
-      w.nt[i] = (w.ke[i] - w.ks[i] + BN - 1) / BN;
-      w.ntiles += w.nt[i];
+      for (int i = 0; i < 2; ++i) {  // kv chunks s and 2cp-1-s, positions < C + q_hi
+        const int ch = i == 0 ? w.p : 2 * p.cp - 1 - w.p;
+        w.ks[i] = chunk_bound(ch, Tkv, p.cp);
+        w.ke[i] = min(chunk_bound(ch + 1, Tkv, p.cp), C + w.q_hi);
+        if (w.ke[i] < w.ks[i]) w.ke[i] = w.ks[i];
+        w.nt[i] = (w.ke[i] - w.ks[i] + BN - 1) / BN;
+        w.ntiles += w.nt[i];
+      }
     }
   } else {
     const long long C = (long long)p.seq_lens_kv[w.b] - Tq;
@@ -1169,7 +1182,9 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
     return cudaErrorInvalidValue;
   if (a.mode == CP_PASS_KV) {
     const unsigned long long hd = (unsigned long long)a.num_kv_heads * D;
-    if (!make_map(&mk, a.k, hd, Nq, hd, BN) || !make_map(&mv, a.v, hd, Nq, hd, BN))
+    const unsigned long long Nkv = a.cu_seqlens_kv ? (unsigned long long)a.total_kv : Nq;
+    if (Nkv == 0) return cudaErrorInvalidValue;  // api.cu admits no empty k / v with queries
+    if (!make_map(&mk, a.k, hd, Nkv, hd, BN) || !make_map(&mv, a.v, hd, Nkv, hd, BN))
       return cudaErrorInvalidValue;
   }
   // the two-tile kernel unless one head per CTA is forced: two heads of a kv group when they
@@ -1210,6 +1225,7 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   p.pool = a.pool_pages;
   p.scale_log2 = scale * kLog2e;
   p.cu_q = a.cu_seqlens_q;
+  p.cu_kv = a.mode == CP_PASS_KV ? a.cu_seqlens_kv : nullptr;
   p.seq_lens_kv = a.seq_lens_kv;
   p.tables = a.block_tables;
   p.out = a.out;

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define CPATTN_ABI_VERSION 1
+#define CPATTN_ABI_VERSION 2
 
 typedef enum {
   CP_OK = 0,
@@ -175,10 +175,16 @@ int32_t cp_select_prefill_mode(int64_t q_len, int64_t kv_len, int32_t num_q_head
  * ([PKV] Purpose: pass-KV for full prefill, pass-Q for chunked prefill; the
  * exchange itself is logical here, so one launch covers every rotation step).
  *
- * PASS_KV (self-attention of each sequence, q = k = v tokens):
- *   partial s of query token i (position i in its sequence) is attention of i
- *   over the keys of kv shard s (chunks s and 2cp-1-s, see cp_partition) with
- *   position <= i.  Q rows of shard r are the tokens of chunks r and 2cp-1-r.
+ * PASS_KV (full prefill, or chunked prefill over a contiguous cached context):
+ *   sequence b has q_len_b = cu_seqlens_q[b+1]-cu_seqlens_q[b] new queries and
+ *   kv_len_b = cu_seqlens_kv[b+1]-cu_seqlens_kv[b] kv tokens (cached + new; NULL
+ *   cu_seqlens_kv means kv_len_b = q_len_b, plain self-attention), token-major in k / v;
+ *   query i sits at position C_b + i, C_b = kv_len_b - q_len_b (a sequence with
+ *   C_b < 0 is flagged CP_ERR_DEVICE_BOUNDS in err and skipped).  The kv tokens are cut
+ *   into 2cp chunks like cp_partition does (bounds floor(k*kv_len_b/(2cp))) and kv
+ *   shard s = kv chunks s and 2cp-1-s.  Partial s of a query is its attention over the
+ *   keys of kv shard s with position <= its own.  Q rows of shard r are chunks r and
+ *   2cp-1-r of the new queries.
  * PASS_Q (chunked prefill over a paged, round-robin cache):
  *   sequence b has q_len_b = cu_seqlens_q[b+1]-cu_seqlens_q[b] new queries at
  *   positions C_b .. C_b+q_len_b-1, C_b = seq_lens_kv[b] - q_len_b, and
@@ -208,8 +214,8 @@ typedef struct cp_prefill_args {
   const int32_t* cu_seqlens_q;  /* device [B+1] token-major query rows                  */
   const int32_t* seq_lens_kv;   /* PASS_Q: device [B] cached + new kv tokens            */
   const void* q;                /* device [Nq][Hq][d]                                   */
-  const void* k;                /* PASS_KV: device [Nq][Hkv][d]                         */
-  const void* v;                /* PASS_KV: device [Nq][Hkv][d]                         */
+  const void* k;                /* PASS_KV: device [Nkv][Hkv][d] (Nkv = total_kv or Nq) */
+  const void* v;                /* PASS_KV: device [Nkv][Hkv][d]                        */
   const void* k_cache;          /* PASS_Q: device [cp][pool_pages][Hkv][block_size][d]  */
   const void* v_cache;          /* PASS_Q: same layout as k_cache                       */
   int64_t pool_pages;           /* PASS_Q: pages in each rank's pool                    */
@@ -226,6 +232,9 @@ typedef struct cp_prefill_args {
   float* out;                   /* device [cp][Nq][Hq][d] f32                           */
   float* lse;                   /* device [cp][Nq][Hq] f32                              */
   int32_t* err;                 /* device int32 or NULL                                 */
+  const int32_t* cu_seqlens_kv; /* PASS_KV: device [B+1] kv rows of k / v, or NULL      */
+  int32_t total_kv;             /* PASS_KV with cu_seqlens_kv: host, rows of k / v      */
+  int32_t reserved;             /* 0                                                    */
 } cp_prefill_args;
 
 cp_status cp_partial_attn_prefill(const cp_prefill_args* args, void* stream);

@@ -253,15 +253,22 @@ def _rows_by_seq(cu, rows):
     return out
 
 
-def pass_kv_partials(q, k, v, cu_seqlens, cp: int, scale: float, rows=None):
+def pass_kv_partials(q, k, v, cu_seqlens, cp: int, scale: float, rows=None, cu_seqlens_kv=None):
     """Pass-KV prefill: partial of every query row against every kv shard.
 
     "Add utility functions ...", Purpose: in full prefill the KV shards circulate so every Q
     shard meets every KV shard; the order of the rotation does not change any partial.
+    Without cu_seqlens_kv, q, k and v hold the same tokens (self-attention, query i at
+    position i).  With cu_seqlens_kv, sequence b has kv_len = cu_seqlens_kv[b+1] -
+    cu_seqlens_kv[b] kv tokens (a cached context followed by the new tokens) and its q_len new
+    queries are the last q_len positions: query i sits at position kv_len - q_len + i.  The kv
+    tokens are cut into 2cp chunks exactly like the queries (chunk_bounds over kv_len) and kv
+    shard s holds kv chunks s and 2cp-1-s.
     Returns O [cp, R, Hq, d], LSE [cp, R, Hq] where partial s is kv shard s and the R rows are
-    the selected global token rows (all rows, in token order, when rows is None).
+    the selected global query rows (all rows, in token order, when rows is None).
     """
     cu = _i64(cu_seqlens)
+    cu_kv = cu if cu_seqlens_kv is None else _i64(cu_seqlens_kv)
     per_seq = _rows_by_seq(cu, rows)
     R = sum(x.size for x in per_seq)
     Hq, d = q.shape[1], q.shape[2]
@@ -270,17 +277,21 @@ def pass_kv_partials(q, k, v, cu_seqlens, cp: int, scale: float, rows=None):
     out_row = 0
     for b in range(cu.size - 1):
         lo, hi = int(cu[b]), int(cu[b + 1])
-        T = hi - lo
+        klo, khi = int(cu_kv[b]), int(cu_kv[b + 1])
+        Tq, Tkv = hi - lo, khi - klo
+        if Tkv < Tq:
+            raise ValueError(f"sequence {b}: {Tkv} kv tokens for {Tq} new queries")
+        ctx = Tkv - Tq
         sel = per_seq[b]
         if sel.size == 0:
             continue
-        bnd = chunk_bounds(T, cp)
+        bnd = chunk_bounds(Tkv, cp)
         qb = q[lo:hi][sel]
         for s in range(cp):
             keys = np.concatenate([np.arange(bnd[c], bnd[c + 1]) for c in shard_chunks(s, cp)])
-            kb = k[lo:hi][keys] if keys.size else k[lo:lo]
-            vb = v[lo:hi][keys] if keys.size else v[lo:lo]
-            o, l = partial_attention(qb, kb, vb, sel, keys, scale)
+            kb = k[klo:khi][keys] if keys.size else k[klo:klo]
+            vb = v[klo:khi][keys] if keys.size else v[klo:klo]
+            o, l = partial_attention(qb, kb, vb, ctx + sel, keys, scale)
             O[s, out_row:out_row + sel.size] = o
             LSE[s, out_row:out_row + sel.size] = l
         out_row += sel.size

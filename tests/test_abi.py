@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_struct_mirrors_match(lib):
     assert lib.cp_prefill_args_size() == ctypes.sizeof(cpa.PrefillArgs)
     assert lib.cp_decode_args_size() == ctypes.sizeof(cpa.DecodeArgs)
-    assert lib.cp_abi_version() == 1
+    assert lib.cp_abi_version() == 2
     assert lib.cp_status_string(5) == b"CP_ERR_DEVICE_BOUNDS"
 
 
@@ -102,6 +102,24 @@ def test_fused_prefill_arguments_are_checked_on_the_host(lib):
     assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 1
     f.mode, f.dtype = 0, 0
     assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 2   # f32 inputs
+
+
+def test_cached_context_arguments_are_checked_on_the_host(lib):
+    """PASS_KV with cu_seqlens_kv needs kv rows when there are queries; PASS_Q refuses the
+    PASS_KV-only kv lengths."""
+    a = cpa.PrefillArgs()
+    a.mode, a.dtype, a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.cp = 0, 1, 1, 8, 2, 128, 2
+    a.total_q, a.max_seqlen_q, a.q_shard, a.kv_shard = 10, 10, -1, -1
+    a.cu_seqlens_q, a.q, a.k, a.v, a.out, a.lse = 256, 256, 256, 256, 256, 256
+    a.cu_seqlens_kv, a.total_kv = 256, 0
+    assert lib.cp_partial_attn_prefill(ctypes.byref(a), None) == 1
+    assert "total_kv" in _last(lib)[1]
+    a.total_kv = -3
+    assert lib.cp_partial_attn_prefill(ctypes.byref(a), None) == 1
+    a.mode, a.k_cache, a.v_cache, a.block_tables, a.seq_lens_kv = 1, 256, 256, 256, 256
+    a.max_blocks, a.pool_pages, a.interleave, a.block_size = 4, 8, 8, 16
+    assert lib.cp_partial_attn_prefill(ctypes.byref(a), None) == 1
+    assert "cu_seqlens_kv" in _last(lib)[1]
 
 
 def test_decode_plan_covers_every_rank_share(lib):

@@ -149,6 +149,64 @@ def test_pass_kv_single_pair(lib, impl):
     assert (lse.cpu()[mask] == 7.0).all()
 
 
+PASS_KV_CTX_CASES = [
+    # q_lens, kv_lens (cached + new), Hq, Hkv, d, dtype, cp
+    ([300, 77], [1500, 77], 8, 2, 128, torch.bfloat16, 2),    # one cached, one plain sequence
+    ([512, 1, 130], [4096, 900, 131], 16, 2, 128, torch.bfloat16, 4),
+    ([200], [2000], 6, 2, 64, torch.bfloat16, 3),             # odd G: two row tiles per CTA
+    ([129, 0, 64], [700, 50, 64], 4, 1, 128, torch.bfloat16, 1),   # a sequence with no query
+    ([96], [1000], 8, 2, 128, torch.float32, 2),
+]
+
+
+def _ctx_case(q_lens, kv_lens, Hq, Hkv, d, dt, seed):
+    g = torch.Generator().manual_seed(seed)
+    return dict(q=wl.normal((sum(q_lens), Hq, d), dt, g), k=wl.normal((sum(kv_lens), Hkv, d), dt, g),
+                v=wl.normal((sum(kv_lens), Hkv, d), dt, g), cu_q=_cu(q_lens), cu_kv=_cu(kv_lens))
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
+@pytest.mark.parametrize("case", range(len(PASS_KV_CTX_CASES)))
+def test_pass_kv_cached_context_parity(lib, case, impl):
+    """Pass-KV with a contiguous cached context (cu_seqlens_kv): the new queries are the last
+    positions of their sequence's kv tokens, kv shards cut over the kv length."""
+    q_lens, kv_lens, Hq, Hkv, d, dt, cp = PASS_KV_CTX_CASES[case]
+    if impl.startswith("tc") and dt != torch.bfloat16:
+        pytest.skip("the tensor-core kernel takes bf16")
+    x = _ctx_case(q_lens, kv_lens, Hq, Hkv, d, dt, 500 + case)
+    out, lse = lib.cp_partial_attn_prefill(
+        x["q"].to(DEV), x["cu_q"].to(DEV), cp, k=x["k"].to(DEV), v=x["v"].to(DEV),
+        cu_seqlens_kv=x["cu_kv"].to(DEV), max_seqlen_q=max(q_lens), impl=_impl_code(lib, impl))
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_q"], cp, 1 / math.sqrt(d),
+                                cu_seqlens_kv=x["cu_kv"])
+    check_partials(out, lse, O, L, what=f"pass-KV cached context {impl} partials")
+    mo, ml = lib.cp_lse_merge(out, lse, out_dtype=dt)
+    Om, Lm = orc.lse_merge(O, L)
+    check_merged(mo, ml, Om, Lm, what=f"pass-KV cached context {impl} merged")
+    if dt == torch.bfloat16 and impl != "simt":
+        fo, fl = lib.cp_attn_prefill_fused(x["q"].to(DEV), x["cu_q"].to(DEV), cp, x["k"].to(DEV),
+                                           x["v"].to(DEV), cu_seqlens_kv=x["cu_kv"].to(DEV),
+                                           max_seqlen_q=max(q_lens), impl=_impl_code(lib, impl))
+        check_merged(fo, fl, Om, Lm, what=f"pass-KV cached context {impl} fused")
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
+def test_pass_kv_reports_short_kv(lib, impl):
+    """A sequence with fewer kv tokens than new queries is flagged (CP_ERR_DEVICE_BOUNDS) and its
+    rows skipped; the other sequences' partials still match the oracle."""
+    q_lens, kv_lens = [40, 30], [100, 20]      # sequence 1: 20 kv tokens for 30 queries
+    x = _ctx_case(q_lens, kv_lens, 8, 2, 128, torch.bfloat16, 77)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = lib.cp_partial_attn_prefill(
+        x["q"].to(DEV), x["cu_q"].to(DEV), 2, k=x["k"].to(DEV), v=x["v"].to(DEV),
+        cu_seqlens_kv=x["cu_kv"].to(DEV), max_seqlen_q=40, impl=_impl_code(lib, impl), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 5
+    O, L = orc.pass_kv_partials(x["q"][:40], x["k"][:100], x["v"][:100], _cu([40]), 2, 1 / math.sqrt(128),
+                                cu_seqlens_kv=_cu([100]))
+    check_partials(out[:, :40], lse[:, :40], O, L, what=f"pass-KV {impl} beside a flagged sequence")
+
+
 def _paged_case(B, q_lens, kv_lens, Hq, Hkv, d, dt, cp, I, seed):
     g = torch.Generator().manual_seed(seed)
     caps = [wl.block_capacity(L, cp, I, 16) for L in kv_lens]

@@ -91,7 +91,35 @@ def _deal_wrong_rank(L, cp, I):
     return rank, local
 
 
+def _pass_kv_mutant(drop_ctx=False, bounds_over_q=False):
+    """pass_kv_partials with one planted mistake in its cached-context handling."""
+    def fn(q, k, v, cu_seqlens, cp, scale, rows=None, cu_seqlens_kv=None):
+        cu = np.asarray(cu_seqlens, dtype=np.int64)
+        cu_kv = cu if cu_seqlens_kv is None else np.asarray(cu_seqlens_kv, dtype=np.int64)
+        per_seq = orc._rows_by_seq(cu, rows)
+        R = sum(x.size for x in per_seq)
+        O = np.zeros((cp, R, q.shape[1], q.shape[2]))
+        L = np.full((cp, R, q.shape[1]), -np.inf)
+        out_row = 0
+        for b in range(cu.size - 1):
+            lo, hi, klo, khi = int(cu[b]), int(cu[b + 1]), int(cu_kv[b]), int(cu_kv[b + 1])
+            ctx = 0 if drop_ctx else (khi - klo) - (hi - lo)
+            sel = per_seq[b]
+            bnd = orc.chunk_bounds((hi - lo) if bounds_over_q else (khi - klo), cp)
+            for s_ in range(cp):
+                keys = np.concatenate([np.arange(bnd[c], bnd[c + 1]) for c in orc.shard_chunks(s_, cp)])
+                o, l = orc.partial_attention(q[lo:hi][sel], k[klo:khi][keys], v[klo:khi][keys],
+                                             ctx + sel, keys, scale)
+                O[s_, out_row:out_row + sel.size] = o
+                L[s_, out_row:out_row + sel.size] = l
+            out_row += sel.size
+        return O, L
+    return fn
+
+
 MUTATIONS = {
+    "pass_kv_ctx_dropped": ("pass_kv_partials", _pass_kv_mutant(drop_ctx=True)),
+    "pass_kv_bounds_over_q_len": ("pass_kv_partials", _pass_kv_mutant(bounds_over_q=True)),
     "causal_strict": ("partial_attention", _strict_causal),
     "gqa_wrong_group": ("partial_attention", _wrong_gqa),
     "k_v_swapped": ("partial_attention", _swapped_kv),

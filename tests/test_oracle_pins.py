@@ -407,6 +407,69 @@ def pin_pass_kv_equals_attention(seed=6):
     assert np.allclose(Os, O[:, rows], atol=1e-12) and np.allclose(Ls, L[:, rows], atol=1e-12)
 
 
+def pin_pass_kv_cached_context(seed=16):
+    """Pass-KV over a cached context (queries = the last q_len of kv_len positions): merged
+    partials equal torch's scaled_dot_product_attention with an explicit bottom-right causal
+    mask (key j visible to new query i iff j <= kv_len - q_len + i) for cp in {1, 2, 4, 8};
+    with kv_len = q_len the partials equal those of plain self-attention; a brute-force loop
+    checks one tiny case end to end."""
+    r = _rng(seed)
+    q_lens, kv_lens = [5, 17, 1, 9], [37, 17, 30, 9]
+    Hq, Hkv, d = 4, 2, 8
+    q = r.standard_normal((sum(q_lens), Hq, d))
+    k = r.standard_normal((sum(kv_lens), Hkv, d))
+    v = r.standard_normal((sum(kv_lens), Hkv, d))
+    cu = np.concatenate([[0], np.cumsum(q_lens)])
+    cu_kv = np.concatenate([[0], np.cumsum(kv_lens)])
+    for cp in (1, 2, 4, 8):
+        O, L = orc.pass_kv_partials(q, k, v, cu, cp, 0.3, cu_seqlens_kv=cu_kv)
+        Om, Lm = orc.lse_merge(O, L)
+        for b in range(len(q_lens)):
+            sq, sk = slice(cu[b], cu[b + 1]), slice(cu_kv[b], cu_kv[b + 1])
+            nq, nk = q_lens[b], kv_lens[b]
+            mask = torch.from_numpy(np.arange(nk)[None, :] <= (nk - nq + np.arange(nq))[:, None])
+            qt = torch.from_numpy(q[sq]).permute(1, 0, 2)[None]
+            kt = torch.from_numpy(k[sk]).permute(1, 0, 2)[None].repeat_interleave(Hq // Hkv, 1)
+            vt = torch.from_numpy(v[sk]).permute(1, 0, 2)[None].repeat_interleave(Hq // Hkv, 1)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qt, kt, vt, attn_mask=mask, scale=0.3)[0].permute(1, 0, 2).numpy()
+            s_ = (torch.einsum("bhid,bhjd->bhij", qt, kt) * 0.3).masked_fill(~mask, float("-inf"))
+            lse = torch.logsumexp(s_, dim=-1)[0].permute(1, 0).numpy()
+            assert np.allclose(Om[sq], ref, atol=1e-12), (cp, b)
+            assert np.allclose(Lm[sq], lse, atol=1e-12), (cp, b)
+    # kv_len = q_len: the same partials as the self-attention form
+    lens = [11, 6]
+    qs = r.standard_normal((17, Hq, d))
+    ks = r.standard_normal((17, Hkv, d))
+    vs = r.standard_normal((17, Hkv, d))
+    cs = np.array([0, 11, 17])
+    O1, L1 = orc.pass_kv_partials(qs, ks, vs, cs, 2, 0.3)
+    O2, L2 = orc.pass_kv_partials(qs, ks, vs, cs, 2, 0.3, cu_seqlens_kv=cs)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+    # brute force: one sequence, 3 new queries after 6 cached tokens, cp = 2 (chunks of 2 and
+    # 3 kv tokens: bounds 0, 2, 4, 6, 9 over kv_len = 9 -> shard 0 = {0, 1, 6, 7, 8})
+    qb = r.standard_normal((3, 2, 3))
+    kb = r.standard_normal((9, 1, 3))
+    vb = r.standard_normal((9, 1, 3))
+    O, L = orc.pass_kv_partials(qb, kb, vb, np.array([0, 3]), 2, 0.7,
+                                cu_seqlens_kv=np.array([0, 9]))
+    for s_, keys in ((0, [0, 1, 6, 7, 8]), (1, [2, 3, 4, 5])):
+        Ob, Lb = brute_attention(qb.tolist(), kb[keys].tolist(), vb[keys].tolist(),
+                                 [6, 7, 8], keys, 0.7)
+        assert np.array_equal(np.isinf(L[s_]), np.isinf(Lb))
+        fin = np.isfinite(Lb)
+        assert np.allclose(L[s_][fin], Lb[fin], atol=1e-12) and np.allclose(O[s_], Ob, atol=1e-12)
+    # sampled rows give the same values as the full computation
+    rows = [0, 4, 5, 21, 22, 31]
+    O, L = orc.pass_kv_partials(q, k, v, cu, 4, 0.3, cu_seqlens_kv=cu_kv)
+    Os, Ls = orc.pass_kv_partials(q, k, v, cu, 4, 0.3, rows=rows, cu_seqlens_kv=cu_kv)
+    assert np.allclose(Os, O[:, rows], atol=1e-12) and np.allclose(Ls, L[:, rows], atol=1e-12)
+
+
+def test_pass_kv_cached_context():
+    pin_pass_kv_cached_context()
+
+
 def pin_pass_q_equals_attention(seed=7):
     r = _rng(seed)
     Hq, Hkv, d, bs = 4, 2, 8, 4
@@ -500,7 +563,7 @@ def test_kv_cache_write():
 ALL_PINS = [pin_brute_force, pin_kv_cache_write, pin_sdpa, pin_closed_forms, pin_softmax_rows, pin_merge,
             pin_partition_fixture, pin_partition_invariants, pin_load_balance, pin_interleave,
             pin_computed_tokens_fixture, pin_slot_mapping, pin_pass_kv_equals_attention,
-            pin_pass_q_equals_attention]
+            pin_pass_kv_cached_context, pin_pass_q_equals_attention]
 
 
 @pytest.mark.parametrize("T,cp", [(4, 2), (2, 4), (1, 8)])
