@@ -23,7 +23,8 @@ from . import _build
 
 __all__ = [
     "CPError", "load", "lib_path", "CP_F32", "CP_BF16", "CP_PASS_KV", "CP_PASS_Q",
-    "CP_IMPL_AUTO", "CP_IMPL_TCGEN05", "CP_IMPL_SIMT", "CP_IMPL_TCGEN05_SINGLE", "cp_partition", "cp_kv_interleave_layout",
+    "CP_IMPL_AUTO", "CP_IMPL_TCGEN05", "CP_IMPL_SIMT", "CP_IMPL_TCGEN05_SINGLE",
+    "CP_IMPL_TCGEN05_PERSISTENT", "cp_partition", "cp_kv_interleave_layout",
     "cp_partial_attn_prefill", "cp_decode_plan", "cp_partial_attn_decode", "cp_lse_merge",
     "cp_decode_workspace_size", "cp_decode_attention", "cp_decode_attention_noalloc",
     "cp_kv_cache_write", "cp_select_prefill_mode", "cp_attn_prefill_fused", "STATUS",
@@ -32,6 +33,7 @@ __all__ = [
 CP_F32, CP_BF16 = 0, 1
 CP_PASS_KV, CP_PASS_Q = 0, 1
 CP_IMPL_AUTO, CP_IMPL_TCGEN05, CP_IMPL_SIMT, CP_IMPL_TCGEN05_SINGLE = 0, 1, 2, 3
+CP_IMPL_TCGEN05_PERSISTENT = 4
 STATUS = {0: "CP_OK", 1: "CP_ERR_INVALID_ARG", 2: "CP_ERR_UNSUPPORTED", 3: "CP_ERR_CUDA",
           4: "CP_ERR_TIMEOUT", 5: "CP_ERR_DEVICE_BOUNDS"}
 
@@ -280,7 +282,8 @@ def cp_kv_cache_write(k_new, v_new, cu_new, start_pos, k_cache, v_cache, block_t
 
 
 def cp_select_prefill_mode(q_len, kv_len, num_q_heads, num_kv_heads, head_dim, elem_bytes=2):
-    """CP_PASS_KV or CP_PASS_Q by the bytes each would exchange between ranks (see cpattn.h)."""
+    """CP_PASS_KV or CP_PASS_Q: the mode measured faster on one GB300 for the nearest shape of a
+    (q_len, kv_len, q heads per kv head) grid (see cpattn.h)."""
     load()
     return _LIB.cp_select_prefill_mode(q_len, kv_len, num_q_heads, num_kv_heads, head_dim,
                                        elem_bytes)

@@ -429,10 +429,30 @@ cp_status cp_kv_interleave_layout(const int32_t* cu_seq_lens, int32_t num_seqs,
 
 int32_t cp_select_prefill_mode(int64_t q_len, int64_t kv_len, int32_t num_q_heads,
                                int32_t num_kv_heads, int32_t head_dim, int32_t elem_bytes) {
-  const double kv = (double)kv_len * 2.0 * num_kv_heads * head_dim * elem_bytes;
-  const double q = (double)q_len * num_q_heads * head_dim * elem_bytes +
-                   (double)q_len * num_q_heads * (head_dim + 1) * 4.0;
-  return q < kv ? CP_PASS_Q : CP_PASS_KV;
+  (void)head_dim;
+  (void)elem_bytes;
+  // Measured on one GB300: the partials + merge step of each mode (pass-KV over contiguous
+  // cached + new kv, pass-Q over the paged round-robin cache; cp = 4, d = 128, bf16, batch
+  // 8192 / q_len sequences, median of 8 runs with L2 flushed) over q_len in {256, 1024, 4096},
+  // kv_len / q_len in {1, 2, 4, .., 32} and G in {1, 2, 4, 8}.  Bit r of kPassQ[G][q] marks
+  // the kv_len / q_len = 2^r shapes where pass-Q was faster by more than 3%; everywhere else
+  // pass-KV was faster or within 3%.  A shape is looked up at its nearest grid point (log2).
+  static const unsigned char kPassQ[4][3] = {
+      {0x02, 0x00, 0x0F},  // G = 1: q_len 256, 1024, 4096
+      {0x02, 0x00, 0x00},  // G = 2
+      {0x02, 0x00, 0x00},  // G = 4
+      {0x02, 0x00, 0x00},  // G = 8 (and above)
+  };
+  if (q_len <= 0 || kv_len < q_len || num_kv_heads <= 0 || num_q_heads < num_kv_heads)
+    return CP_PASS_KV;
+  auto bucket = [](double x, double per_step, int top) {
+    const long i = lround(log2(x) / per_step);
+    return (int)(i < 0 ? 0 : (i > top ? top : i));
+  };
+  const int gi = bucket((double)(num_q_heads / num_kv_heads), 1.0, 3);
+  const int qi = bucket((double)q_len / 256.0, 2.0, 2);
+  const int ri = bucket((double)kv_len / (double)q_len, 1.0, 5);
+  return ((kPassQ[gi][qi] >> ri) & 1) ? CP_PASS_Q : CP_PASS_KV;
 }
 
 cp_status cp_kv_cache_write(const void* k_new, const void* v_new, const int32_t* cu_new,
@@ -531,7 +551,7 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   REQUIRE(a != nullptr, "args is null");
   REQUIRE(a->mode == CP_PASS_KV || a->mode == CP_PASS_Q, "mode must be CP_PASS_KV or CP_PASS_Q");
   REQUIRE(a->dtype == CP_F32 || a->dtype == CP_BF16, "dtype must be CP_F32 or CP_BF16");
-  REQUIRE(a->impl >= CP_IMPL_AUTO && a->impl <= CP_IMPL_TCGEN05_SINGLE, "unknown impl %d", a->impl);
+  REQUIRE(a->impl >= CP_IMPL_AUTO && a->impl <= CP_IMPL_TCGEN05_PERSISTENT, "unknown impl %d", a->impl);
   REQUIRE(a->num_seqs >= 1, "num_seqs must be >= 1");
   REQUIRE(a->num_kv_heads >= 1 && a->num_q_heads >= a->num_kv_heads &&
               a->num_q_heads % a->num_kv_heads == 0,
@@ -554,7 +574,7 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
   int impl = a->impl;
   if (impl == CP_IMPL_AUTO) impl = (a->dtype == CP_BF16 && cp_prefill_tc_supported(*a)) ? CP_IMPL_TCGEN05 : CP_IMPL_SIMT;
-  if (impl == CP_IMPL_TCGEN05 || impl == CP_IMPL_TCGEN05_SINGLE) {
+  if (impl == CP_IMPL_TCGEN05 || impl == CP_IMPL_TCGEN05_SINGLE || impl == CP_IMPL_TCGEN05_PERSISTENT) {
     if (a->dtype != CP_BF16 || !cp_prefill_tc_supported(*a))
       return fail(CP_ERR_UNSUPPORTED, "the tcgen05 kernel needs bf16 inputs and a supported shape");
     return launched(cp_launch_prefill_tc(*a, scale, as_stream(stream)), "prefill (tcgen05) launch");

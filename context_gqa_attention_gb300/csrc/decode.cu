@@ -65,10 +65,12 @@ CP_DEV uint4 ldg_stream(const void* p) {
 // Fused merge (decode): after a CTA has written its partial it counts itself in for its
 // (sequence, kv head); the CTA that arrives last merges the cp * splits partials of the G heads
 // (the LSE merge: weights 2^(lse_p - M) staged once in shared memory, empty partials weigh 0),
-// writes the final output and LSE and returns the counter to zero for the next call.  Publication follows the
-// fence-then-count pattern: each CTA fences its partial before the atomic increment, and the
-// last one fences again before reading the others' partials through L2.  No CTA waits on
-// another, so nothing can stall.
+// writes the final output and LSE and returns the counter to zero for the next call.
+// Publication: after a CTA barrier (every thread's partial writes ordered before it), one thread
+// counts the CTA in with an acquire-release atomic at GPU scope: its release side publishes the
+// CTA's partial (cumulatively, through the barrier) and its acquire side lets the last CTA see
+// every earlier CTA's partial; a second barrier passes that on to the last CTA's threads, which
+// then read the partials through L2.  No CTA waits on another, so nothing can stall.
 template <typename T, int D, int G>
 CP_DEV void fused_tail(const DecodeParams& p, int b, int g) {
   __shared__ int s_last;
@@ -77,13 +79,15 @@ CP_DEV void fused_tail(const DecodeParams& p, int b, int g) {
   __syncthreads();
   const int P = p.cp * p.S;
   if (threadIdx.x == 0) {
-    __threadfence();
-    const int prev = atomicAdd(p.counters + (long long)b * p.Hkv + g, 1);
+    int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(p.counters + (long long)b * p.Hkv + g)
+                 : "memory");
     s_last = (prev == P - 1);
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   const long long stride = (long long)p.B * p.Hq;           // between partials
   const long long unit0 = (long long)b * p.Hq + (long long)g * G;
   for (int i = threadIdx.x; i < P * G; i += blockDim.x)

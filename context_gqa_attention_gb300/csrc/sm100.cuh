@@ -232,6 +232,20 @@ SM100_DEV void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// ------------------------------------------------------------------------------ registers
+// Per-warpgroup register budget (every thread of the warpgroup executes it, same N, a multiple
+// of 8 in [24, 256]).  An increase waits until other warpgroups have released enough registers
+// of the block's launch allocation, so the budgets of all warpgroups must add up to at most
+// that allocation.
+template <int N>
+SM100_DEV void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+SM100_DEV void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 SM100_DEV float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -65,9 +65,12 @@ typedef enum {
   CP_IMPL_AUTO = 0,     /* tcgen05 tensor-core kernel for bf16, SIMT kernel for f32   */
   CP_IMPL_TCGEN05 = 1,  /* bf16 only: TMA + tcgen05.mma + TMEM                        */
   CP_IMPL_SIMT = 2,     /* plain CUDA cores, any supported dtype (cross-check path)   */
-  CP_IMPL_TCGEN05_SINGLE = 3  /* bf16: tcgen05 kernel with one q head per CTA (the     */
+  CP_IMPL_TCGEN05_SINGLE = 3, /* bf16: tcgen05 kernel with one q head per CTA (the     */
                               /* default pairs two heads, or two row tiles of one head */
                               /* when q heads per kv head is odd)                      */
+  CP_IMPL_TCGEN05_PERSISTENT = 4  /* bf16: the two-tile tcgen05 kernel as one CTA per SM */
+                                  /* walking the work items, epilogue warps overlapping  */
+                                  /* the next item                                       */
 } cp_impl;
 
 /* Human-readable name of a cp_status value (static string). */
@@ -160,12 +163,17 @@ cp_status cp_kv_cache_write(const void* k_new, const void* v_new, const int32_t*
  * suits full prefill because a KV head serves more than two query heads in most models; passing
  * Q suits chunked prefill when the cached context is much longer than the new queries).
  *
- * The rule made quantitative by the bytes one rank would exchange with the others:
- *   pass-KV  moves its KV shard:  kv_len * 2 * Hkv * d * elem_bytes
- *   pass-Q   moves its Q shard and gets its partials back:
- *            q_len * Hq * d * elem_bytes  +  q_len * Hq * (d + 1) * 4
- * (both per cp-th of the sequence).  Returns CP_PASS_Q when that is smaller, else CP_PASS_KV.
- * Host-only and pure; kv_len counts cached + new tokens, q_len the new ones.
+ * The pages' rule weighs the bytes ranks exchange; on one GPU nothing is exchanged and the
+ * choice is the faster kernel for the shape.  The answer comes from a table measured on one
+ * GB300 (partials + merge step of each mode, cp = 4, d = 128, bf16) over q_len in
+ * {256, 1024, 4096}, kv_len / q_len in {1, 2, 4, 8, 16, 32} and q heads per kv head G in
+ * {1, 2, 4, 8}; a shape takes its nearest grid point (log2 scale).  The two modes were within
+ * 5% of each other almost everywhere: CP_PASS_Q is returned only where it was more than 3%
+ * faster (q_len ~ 256 with kv_len ~ 2 q_len; G = 1 with q_len ~ 4096 and kv_len <= ~8 q_len),
+ * CP_PASS_KV elsewhere.  Both modes run for every shape the library accepts (PASS_KV takes a
+ * cached context through cu_seqlens_kv); which kv layout the caller holds decides which call
+ * applies.  Host-only and pure; kv_len counts cached + new tokens, q_len the new ones;
+ * head_dim and elem_bytes are accepted for the signature and do not change the answer.
  * ---------------------------------------------------------------------------- */
 int32_t cp_select_prefill_mode(int64_t q_len, int64_t kv_len, int32_t num_q_heads,
                                int32_t num_kv_heads, int32_t head_dim, int32_t elem_bytes);

@@ -133,16 +133,19 @@ def test_decode_plan_covers_every_rank_share(lib):
         assert (ns.value - 1) * st.value < max(share, 1)
 
 
-def test_prefill_mode_selector_follows_the_pages_rule(lib):
-    """Full prefill with more than two query heads per kv head -> pass-KV; chunked prefill with
-    a context much longer than the new queries -> pass-Q; the crossover moves with G."""
+def test_prefill_mode_selector_follows_its_measured_table(lib):
+    """The selector returns the mode measured faster on one GB300 at the nearest grid point:
+    pass-Q only where it won by more than 3% (q_len ~ 256 with kv_len ~ 2 q_len; G = 1 with
+    q_len ~ 4096 and kv_len up to ~8 q_len), pass-KV elsewhere, including full prefill."""
     sel = lib.cp_select_prefill_mode
     assert sel(8192, 8192, 16, 2, 128, 2) == 0          # full prefill, G = 8
-    assert sel(8192, 8192, 4, 2, 128, 2) == 0           # full prefill, G = 2
-    assert sel(2048, 32768, 16, 2, 128, 2) == 1         # the chunked workload: pass-Q
-    assert sel(2048, 4096, 16, 2, 128, 2) == 0          # context only 2x the chunk: pass-KV
-    # crossover: pass-Q once kv_len / q_len exceeds (G/2) (1 + 2 (d + 1) / d)
-    G, d = 8, 128
-    ratio = G / 2 * (1 + 2 * (d + 1) / d)
-    assert sel(1000, int(1000 * ratio) + 8, 8 * G, 8, d, 2) == 1
-    assert sel(1000, int(1000 * ratio) - 8, 8 * G, 8, d, 2) == 0
+    assert sel(2048, 32768, 16, 2, 128, 2) == 0         # the chunked workload: within 1%
+    for G in (1, 2, 4, 8, 16):
+        assert sel(256, 512, 2 * G, 2, 128, 2) == 1      # q_len 256, kv_len = 2 q_len
+        assert sel(256, 4096, 2 * G, 2, 128, 2) == 0
+        assert sel(1024, 2048, 2 * G, 2, 128, 2) == 0
+    assert sel(4096, 4096 * 4, 2, 2, 128, 2) == 1       # G = 1, q_len 4096, ratio 4
+    assert sel(4096, 4096 * 32, 2, 2, 128, 2) == 0
+    assert sel(4096, 4096 * 4, 4, 2, 128, 2) == 0       # G = 2
+    assert sel(300, 560, 8, 2, 128, 2) == 1             # nearest grid point (256, 2, G = 4)
+    assert sel(10, 5, 8, 2, 128, 2) == 0                # kv shorter than q: no pass-Q answer
