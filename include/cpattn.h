@@ -69,8 +69,8 @@ typedef enum {
                               /* default pairs two heads, or two row tiles of one head */
                               /* when q heads per kv head is odd)                      */
   CP_IMPL_TCGEN05_PERSISTENT = 4  /* bf16: the two-tile tcgen05 kernel as one CTA per SM */
-                                  /* walking the work items, epilogue warps overlapping  */
-                                  /* the next item                                       */
+                                  /* walking the work items; an item's loads and first   */
+                                  /* QK^T overlap the previous item's end                */
 } cp_impl;
 
 /* Human-readable name of a cp_status value (static string). */
