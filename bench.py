@@ -922,7 +922,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="cpu baseline: stratified query rows per sequence (0: the workload's "
                          "sample size, all rows when it has none)")
-    ap.add_argument("--prefill-impl", default="auto", choices=["auto", "tcgen05", "simt", "persistent"])
+    ap.add_argument("--prefill-impl", default="auto", choices=["auto", "tcgen05", "simt"])
     ap.add_argument("--prefill-fused", action="store_true",
                     help="prefill as one launch (cp_attn_prefill_fused) instead of partials + merge")
     ap.add_argument("--decode-fused", action="store_true",
@@ -957,8 +957,7 @@ def main():
     else:
         runner.fused = args.prefill_fused
         runner.impl = {"auto": cpa.CP_IMPL_AUTO, "tcgen05": cpa.CP_IMPL_TCGEN05,
-                       "simt": cpa.CP_IMPL_SIMT,
-                       "persistent": cpa.CP_IMPL_TCGEN05_PERSISTENT}[args.prefill_impl]
+                       "simt": cpa.CP_IMPL_SIMT}[args.prefill_impl]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     clocks = ClockSampler(local)

@@ -24,7 +24,7 @@ from . import _build
 __all__ = [
     "CPError", "load", "lib_path", "CP_F32", "CP_BF16", "CP_PASS_KV", "CP_PASS_Q",
     "CP_IMPL_AUTO", "CP_IMPL_TCGEN05", "CP_IMPL_SIMT", "CP_IMPL_TCGEN05_SINGLE",
-    "CP_IMPL_TCGEN05_PERSISTENT", "cp_partition", "cp_kv_interleave_layout",
+    "cp_partition", "cp_kv_interleave_layout",
     "cp_partial_attn_prefill", "cp_decode_plan", "cp_partial_attn_decode", "cp_lse_merge",
     "cp_decode_workspace_size", "cp_decode_attention", "cp_decode_attention_noalloc",
     "cp_kv_cache_write", "cp_select_prefill_mode", "cp_attn_prefill_fused", "STATUS",
@@ -33,7 +33,6 @@ __all__ = [
 CP_F32, CP_BF16 = 0, 1
 CP_PASS_KV, CP_PASS_Q = 0, 1
 CP_IMPL_AUTO, CP_IMPL_TCGEN05, CP_IMPL_SIMT, CP_IMPL_TCGEN05_SINGLE = 0, 1, 2, 3
-CP_IMPL_TCGEN05_PERSISTENT = 4
 STATUS = {0: "CP_OK", 1: "CP_ERR_INVALID_ARG", 2: "CP_ERR_UNSUPPORTED", 3: "CP_ERR_CUDA",
           4: "CP_ERR_TIMEOUT", 5: "CP_ERR_DEVICE_BOUNDS"}
 

@@ -551,7 +551,7 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   REQUIRE(a != nullptr, "args is null");
   REQUIRE(a->mode == CP_PASS_KV || a->mode == CP_PASS_Q, "mode must be CP_PASS_KV or CP_PASS_Q");
   REQUIRE(a->dtype == CP_F32 || a->dtype == CP_BF16, "dtype must be CP_F32 or CP_BF16");
-  REQUIRE(a->impl >= CP_IMPL_AUTO && a->impl <= CP_IMPL_TCGEN05_PERSISTENT, "unknown impl %d", a->impl);
+  REQUIRE(a->impl >= CP_IMPL_AUTO && a->impl <= CP_IMPL_TCGEN05_SINGLE, "unknown impl %d", a->impl);
   REQUIRE(a->num_seqs >= 1, "num_seqs must be >= 1");
   REQUIRE(a->num_kv_heads >= 1 && a->num_q_heads >= a->num_kv_heads &&
               a->num_q_heads % a->num_kv_heads == 0,
@@ -574,7 +574,7 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
   int impl = a->impl;
   if (impl == CP_IMPL_AUTO) impl = (a->dtype == CP_BF16 && cp_prefill_tc_supported(*a)) ? CP_IMPL_TCGEN05 : CP_IMPL_SIMT;
-  if (impl == CP_IMPL_TCGEN05 || impl == CP_IMPL_TCGEN05_SINGLE || impl == CP_IMPL_TCGEN05_PERSISTENT) {
+  if (impl == CP_IMPL_TCGEN05 || impl == CP_IMPL_TCGEN05_SINGLE) {
     if (a->dtype != CP_BF16 || !cp_prefill_tc_supported(*a))
       return fail(CP_ERR_UNSUPPORTED, "the tcgen05 kernel needs bf16 inputs and a supported shape");
     return launched(cp_launch_prefill_tc(*a, scale, as_stream(stream)), "prefill (tcgen05) launch");

@@ -61,8 +61,6 @@ struct TcParams {
   float* lse_final;
   // 1: the output tensor map is valid and full 32-row groups are written by TMA stores
   int tma_out;
-  // persistent kernel: work items in the whole item space (the grid strides over them)
-  int num_items;
 };
 
 template <int D>
@@ -1141,430 +1139,6 @@ __global__ void __launch_bounds__(kThreads2, 1)
   }
 }
 
-// ---------------------------------------------------------------------------------- kernel 3
-// Persistent form of the two-tile kernel: one CTA per SM walks a static snake over the work
-// items (round r takes items r*G .. r*G+G-1 in ascending CTA order for even r, descending for odd
-// r, G = grid size), so the heaviest-first item order stays balanced without a global counter.
-// Same warps and register budgets as the two-tile kernel; what changes is that an item's
-// prologue overlaps the previous item's end:
-//   warp 0     TMA producer: an item's Q tiles as soon as the previous item's last QK^T has
-//              completed (an mbarrier committed by the MMA issuer), K and V tiles through the
-//              4-slot ring with slot and phase counted over all items of the CTA.
-//   warp 1     MMA issuer: the next item's first QK^T of both tiles right after the previous
-//              item's last PV (tcgen05 ops run in issue order, so S is free by then).
-//   warps 4-11 softmax as before; at an item's end each warp writes its 32 rows through a
-//              4 KB staging buffer of its own (the Q tiles and the ring may already hold the next
-//              item) by TMA stores, then starts the next item's first tile.  Its TMEM reads of O
-//              end before it hands over that tile's P, so the next item's first PV (which
-//              overwrites O) cannot start earlier.
-template <int D>
-struct LayoutP {
-  static constexpr int NSLOT = 4;
-  static constexpr int kQ = BM * D * 2;
-  static constexpr int kKV = BN * D * 2;
-  static constexpr int oQ = 0;
-  static constexpr int oKV = 2 * kQ;
-  static constexpr int oStage = oKV + NSLOT * kKV;  // 8 softmax warps x 4 KB
-  static constexpr int oBar = oStage + 8 * 4096;
-  static constexpr int bQ = 0, bQEmpty = 1, bFull = 2, bEmpty = bFull + NSLOT, bS = bEmpty + NSLOT,
-                       bP = bS + 2, bO = bP + 2, bDone = bO + 2, nBar = bDone + 1;
-  static constexpr int oMisc = oBar + nBar * 8;
-  static constexpr int kBytes = oMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;
-  static_assert(kAlloc <= 232448, "dynamic shared memory beyond the 227 KB per-CTA limit");
-};
-
-// k-th item of this CTA in the snake order (>= num_items: no more work)
-CP_DEV unsigned snake_item(int k) {
-  const unsigned G = gridDim.x, c = blockIdx.x;
-  return (unsigned)k * G + ((k & 1) ? G - 1 - c : c);
-}
-
-template <int D, bool PG, bool TT, bool FQ, bool FU>
-__global__ void __launch_bounds__(kThreads2, 1)
-    prefill_tcp_kernel(const __grid_constant__ CUtensorMap map_q,
-                       const __grid_constant__ CUtensorMap map_k,
-                       const __grid_constant__ CUtensorMap map_v,
-                       const __grid_constant__ CUtensorMap map_o, const TcParams p) {
-  using Ly = LayoutP<D>;
-  constexpr int NSLOT = Ly::NSLOT;
-  constexpr int KB = D / 64;
-  constexpr int hpc = TT ? 1 : 2;
-  constexpr int span = TT ? 2 * BM : BM;
-  extern __shared__ uint8_t smem_raw[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* sbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + Ly::oQ, sKV = base + Ly::oKV, sStage = base + Ly::oStage;
-  const uint32_t bars = base + Ly::oBar;
-  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
-  uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Ly::oMisc);
-  volatile uint32_t* abort_flag = misc + 1;
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar(Ly::bQ), 1);
-    mbar_init(bar(Ly::bQEmpty), 1);
-    for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(bar(Ly::bFull + s), 1);
-      mbar_init(bar(Ly::bEmpty + s), 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(Ly::bS + i), 1);
-      mbar_init(bar(Ly::bP + i), 4);
-      mbar_init(bar(Ly::bO + i), 1);
-    }
-    mbar_init(bar(Ly::bDone), 1);
-    misc[1] = 0u;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(misc), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = misc[0];
-  const unsigned nitems = (unsigned)p.num_items;
-
-  if (warp < 4) {
-  regs_dec<kReg2Producer>();
-  if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------------- TMA producer
-    tma_prefetch_desc(&map_q);
-    tma_prefetch_desc(&map_k);
-    tma_prefetch_desc(&map_v);
-    int lastph[NSLOT];
-#pragma unroll
-    for (int i = 0; i < NSLOT; ++i) lastph[i] = -1;
-    int prow[BN / 16];
-    int pid[BN / 16];
-    auto table_of = [&](int r, int b) { return p.tables + ((long long)r * p.B + b) * p.max_blocks; };
-    long long tt = 0;  // key tiles of the earlier items
-    int nq = 0;        // Q loads issued
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const unsigned idx = snake_item(k);
-      if (idx >= nitems) break;
-      const Work w = decode_work_at(p, idx, hpc, span);
-      if (!w.valid || w.ntiles == 0) continue;
-      if (nq > 0 && !mbar_wait(bar(Ly::bQEmpty), (uint32_t)(nq - 1) & 1u, abort_flag, p.budget)) {
-        ok = false;
-        break;
-      }
-      mbar_expect_tx(bar(Ly::bQ), 2 * Ly::kQ);
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb)
-          tma_load_2d(sQ + i * Ly::kQ + kb * BM * 128, &map_q, (w.h + (TT ? 0 : i)) * D + kb * 64,
-                      w.q_row0 + (TT ? i * BM : 0), bar(Ly::bQ));
-      ++nq;
-      const int32_t* trow = p.mode == CP_PASS_Q ? table_of(w.p, w.b) : nullptr;
-      const long long kv_end = w.qpos0 - w.q_lo + w.q_hi;
-      RankWalk kw{0, 0, 0, 0};
-      if constexpr (FQ) {
-        kw = walk_start(kv_end, p.cp, p.I);
-        fetch_page_ids(table_of(kw.r, w.b), kw.tr, kw.n_r, p.max_blocks, pid);
-      } else {
-        if (p.mode == CP_PASS_Q) fetch_page_ids(trow, 0, w.n_local, p.max_blocks, pid);
-      }
-      for (int i = 0; i < 2 * w.ntiles; ++i) {
-        const long long li = 2 * tt + i;
-        const int slot = (int)(li & (NSLOT - 1));
-        const uint32_t ph = (uint32_t)(li / NSLOT) & 1u;
-        const int t = i >> 1;
-        const bool isV = (i & 1) != 0;
-        if (!mbar_wait(bar(Ly::bEmpty + slot), ph ^ 1u, abort_flag, p.budget)) { ok = false; break; }
-        if (isV && (p.debug & 1)) continue;  // testing: V never arrives
-        const uint32_t dst = sKV + slot * Ly::kKV;
-        const CUtensorMap* map = isV ? &map_v : &map_k;
-        mbar_expect_tx(bar(Ly::bFull + slot), Ly::kKV);
-        if (p.mode == CP_PASS_KV) {
-          const bool r0 = t < w.nt[0];
-          const int y = w.kv_row0 + (r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN);
-#pragma unroll
-          for (int kb = 0; kb < KB; ++kb)
-            tma_load_2d(dst + kb * BN * 128, map, w.g * D + kb * 64, y, bar(Ly::bFull + slot));
-        } else {
-          if (!isV) {
-            if constexpr (FQ) {
-              page_rows(pid, kw.tr, kw.n_r, p.pool, p.Hkv, kw.r, w.g, p.err, prow);
-              RankWalk kn = kw;
-              walk_next(kn, kv_end, p.cp, p.I);
-              if (t + 1 < w.ntiles) fetch_page_ids(table_of(kn.r, w.b), kn.tr, kn.n_r, p.max_blocks, pid);
-              kw = kn;
-            } else {
-              page_rows(pid, t, w.n_local, p.pool, p.Hkv, w.p, w.g, p.err, prow);
-              if (t + 1 < w.ntiles) fetch_page_ids(trow, t + 1, w.n_local, p.max_blocks, pid);
-            }
-          }
-          if constexpr (PG) {
-#pragma unroll
-            for (int j = 0; j < BN / 16; ++j)
-              tma_load_4d(dst + j * 4096, map, 0, 0, 0, prow[j] >> 3, bar(Ly::bFull + slot));
-          } else {
-#pragma unroll
-            for (int j = 0; j < BN / 16; ++j)
-#pragma unroll
-              for (int kb = 0; kb < KB; ++kb)
-                tma_load_2d(dst + kb * BN * 128 + j * 16 * 128, map, kb * 64, prow[j],
-                            bar(Ly::bFull + slot));
-          }
-        }
-#pragma unroll
-        for (int s2 = 0; s2 < NSLOT; ++s2)
-          if (s2 == slot) lastph[s2] = (int)ph;
-      }
-      tt += w.ntiles;
-    }
-    if (!ok) fail_timeout(abort_flag, p.err);
-    // drain: every copy issued into this CTA's shared memory has landed
-    if (nq > 0) mbar_wait(bar(Ly::bQ), (uint32_t)(nq - 1) & 1u, nullptr, p.budget);
-#pragma unroll
-    for (int s2 = 0; s2 < NSLOT; ++s2)
-      if (lastph[s2] >= 0) mbar_wait(bar(Ly::bFull + s2), (uint32_t)lastph[s2], nullptr, p.budget);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------------------------------------------------------- MMA issuer
-    const uint32_t id_qk = idesc_bf16_f32(BM, BN, false, false);
-    const uint32_t id_pv = idesc_bf16_f32(BM, D, false, true);
-    auto issue_qk = [&](int tile, int slot) {
-      const uint32_t q = sQ + tile * Ly::kQ, kk_ = sKV + slot * Ly::kKV;
-      const uint32_t dS = tmem + (uint32_t)(tile * BN);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t offq = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-        const uint32_t offk = (kk / 4) * (PG ? 1024u : (uint32_t)(BN * 128)) + (kk % 4) * 32;
-        mma_ss(dS, desc_sw128(q + offq, 16, 1024), desc_sw128(kk_ + offk, 16, PG ? 2048u : 1024u),
-               id_qk, kk > 0 ? 1u : 0u);
-      }
-    };
-    auto issue_pv = [&](int tile, int slot, bool acc) {
-      const uint32_t v = sKV + slot * Ly::kKV;
-      const uint32_t dO = tmem + 256u + (uint32_t)(tile * D);
-#pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk) {
-        const uint64_t bd = PG ? desc_sw128(v + kk * 4096, 1024, 2048)
-                               : desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
-        mma_ts(dO, tmem + (uint32_t)(tile * BN + kk * 8), bd, id_pv, (acc || kk > 0) ? 1u : 0u);
-      }
-    };
-    long long tt = 0;
-    int it = 0;
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const unsigned idx = snake_item(k);
-      if (idx >= nitems) break;
-      const Work w = decode_work_at(p, idx, hpc, span);
-      if (!w.valid || w.ntiles == 0) continue;
-      const long long l0 = 2 * tt;  // load index of this item's K(0)
-      const int s0 = (int)(l0 & (NSLOT - 1));
-      ok = mbar_wait(bar(Ly::bQ), (uint32_t)it & 1u, abort_flag, p.budget);
-      if (ok) ok = mbar_wait(bar(Ly::bFull + s0), (uint32_t)(l0 / NSLOT) & 1u, abort_flag, p.budget);
-      if (!ok) break;
-      tc_fence_after();
-      issue_qk(0, s0);
-      mma_commit(bar(Ly::bS + 0));
-      issue_qk(1, s0);
-      mma_commit(bar(Ly::bS + 1));
-      mma_commit(bar(Ly::bEmpty + s0));
-      if (w.ntiles == 1) mma_commit(bar(Ly::bQEmpty));  // the item's last QK^T is issued
-      for (int t = 0; ok && t < w.ntiles; ++t) {
-        const long long g = tt + t;
-        const long long iv = 2 * g + 1, ik = 2 * g + 2;
-        const int sv = (int)(iv & (NSLOT - 1)), sk = (int)(ik & (NSLOT - 1));
-        ok = mbar_wait(bar(Ly::bFull + sv), (uint32_t)(iv / NSLOT) & 1u, abort_flag, p.budget);
-        if (!ok) break;
-        ok = mbar_wait(bar(Ly::bP + 0), (uint32_t)g & 1u, abort_flag, p.budget);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(0, sv, t > 0);
-        mma_commit(bar(Ly::bO + 0));
-        const bool more = t + 1 < w.ntiles;
-        if (more) {
-          ok = mbar_wait(bar(Ly::bFull + sk), (uint32_t)(ik / NSLOT) & 1u, abort_flag, p.budget);
-          if (!ok) break;
-          tc_fence_after();
-          issue_qk(0, sk);
-          mma_commit(bar(Ly::bS + 0));
-        }
-        ok = mbar_wait(bar(Ly::bP + 1), (uint32_t)g & 1u, abort_flag, p.budget);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(1, sv, t > 0);
-        mma_commit(bar(Ly::bO + 1));
-        mma_commit(bar(Ly::bEmpty + sv));
-        if (more) {
-          issue_qk(1, sk);
-          mma_commit(bar(Ly::bS + 1));
-          mma_commit(bar(Ly::bEmpty + sk));
-          if (t + 2 == w.ntiles) mma_commit(bar(Ly::bQEmpty));
-        }
-      }
-      tt += w.ntiles;
-      ++it;
-    }
-    if (!ok) fail_timeout(abort_flag, p.err);
-    mma_commit(bar(Ly::bDone));
-    mbar_wait(bar(Ly::bDone), 0u, nullptr, p.budget);
-  }
-  } else {
-    regs_inc<kReg2Softmax>();
-    // ------------------------------------------------------------------ softmax, one WG per tile
-    const int tile = (warp - 4) >> 2;
-    const int q4 = warp & 3;
-    const int row = q4 * 32 + lane;
-    const int rofs = TT ? tile * BM : 0;
-    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const uint32_t tS = tmem + lane_off + (uint32_t)(tile * BN);
-    const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(tile * D);
-    const uint32_t sb = sStage + (uint32_t)(warp - 4) * 4096u;
-    long long tt = 0;
-    bool ok = true;
-    bool staged = false;  // a TMA store of this warp may still be reading its staging buffer
-    for (int k = 0; ok; ++k) {
-      const unsigned idx = snake_item(k);
-      if (idx >= nitems) break;
-      const Work w = decode_work_at(p, idx, hpc, span);
-      if (!w.valid) continue;
-      const int hcol = w.h + (TT ? 0 : tile);
-      const bool row_valid = w.q_lo + rofs + row < w.q_hi;
-      const long long frow = (long long)(w.q_row0 + rofs + row) * p.Hq + hcol;
-      const long long orow = ((long long)w.p * p.Nq + w.q_row0 + rofs + row) * p.Hq + hcol;
-      if (w.ntiles == 0) {  // no visible key for any row of the item
-        if (row_valid) {
-          if constexpr (FU) {
-            for (int c = 0; c < D; ++c) p.out_final[frow * D + c] = __float2bfloat16_rn(0.f);
-            p.lse_final[frow] = -INFINITY;
-          } else {
-            p.lse[orow] = -INFINITY;
-          }
-        }
-        continue;
-      }
-      const long long qpos = w.qpos0 + rofs + row;
-      const long long kv_end = w.qpos0 - w.q_lo + w.q_hi;
-      int nvis = 0;
-      RankWalk kw{0, 0, 0, 0};
-      if constexpr (FQ) {
-        kw = walk_start(kv_end, p.cp, p.I);
-        nvis = min(kw.n_r, rank_local_len(qpos + 1, kw.r, p.cp, p.I));
-      } else {
-        if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
-      }
-      float m = -INFINITY, l = 0.f;
-      for (int t = 0; t < w.ntiles; ++t) {
-        const long long g = tt + t;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bS + tile), (uint32_t)g & 1u, abort_flag, p.budget));
-        if (!ok) break;
-        tc_fence_after();
-        float s0[32], s1[32], s2[32], s3[32];
-        load_row(tS, s0, s1, s2, s3);
-        int lim;
-        if (p.mode == CP_PASS_KV) {
-          const bool r0 = t < w.nt[0];
-          const int k0 = r0 ? w.ks[0] + t * BN : w.ks[1] + (t - w.nt[0]) * BN;
-          const int ke = r0 ? w.ke[0] : w.ke[1];
-          lim = (int)min((long long)ke - 1, qpos) - k0;
-        } else if constexpr (!FQ) {
-          lim = nvis - 1 - t * BN;
-        } else {
-          if (kw.tr == 0 && t > 0) nvis = min(kw.n_r, rank_local_len(qpos + 1, kw.r, p.cp, p.I));
-          lim = nvis - 1 - kw.tr * BN;
-          walk_next(kw, kv_end, p.cp, p.I);
-        }
-        const float alpha = row_max_update(s0, s1, s2, s3, lim, p.scale_log2, m);
-        // S(t) complete implies PV(t-1) complete: O is stable and the S columns may take P(t)
-        l = l * alpha + row_exp_tmem(s0, s1, s2, s3, p.scale_log2, m, tS);
-        if (t > 0) rescale_o<D>(tO, alpha);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(Ly::bP + tile));
-      }
-      if (!ok) break;
-      // the item's last PV of this tile (the tile's own softmax finished, so one phase behind)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(Ly::bO + tile), (uint32_t)(tt + w.ntiles - 1) & 1u,
-                                             abort_flag, p.budget));
-      if (!ok) break;
-      tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const bool tma = p.tma_out && w.q_lo + rofs + q4 * 32 + 32 <= w.q_hi;
-      const int z = (FU ? 0 : w.p * p.Nq) + w.q_row0 + rofs + q4 * 32;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(tO + c * 32, o);
-        tmem_wait_ld(o);
-        if (tma) {
-          // f32: one box of 32 columns per chunk; bf16: one box of 64 columns per two chunks
-          if ((!FU || (c & 1) == 0) && staged) {
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
-          }
-          const uint32_t rb = sb + (uint32_t)(lane * 128);
-          if constexpr (FU) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              st_shared_v4(rb + ((uint32_t)(((c & 1) * 4 + j) ^ (lane & 7)) << 4),
-                           pack_bf16(o[8 * j] * inv_l, o[8 * j + 1] * inv_l),
-                           pack_bf16(o[8 * j + 2] * inv_l, o[8 * j + 3] * inv_l),
-                           pack_bf16(o[8 * j + 4] * inv_l, o[8 * j + 5] * inv_l),
-                           pack_bf16(o[8 * j + 6] * inv_l, o[8 * j + 7] * inv_l));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              st_shared_v4(rb + ((uint32_t)(j ^ (lane & 7)) << 4), __float_as_uint(o[4 * j] * inv_l),
-                           __float_as_uint(o[4 * j + 1] * inv_l), __float_as_uint(o[4 * j + 2] * inv_l),
-                           __float_as_uint(o[4 * j + 3] * inv_l));
-          }
-          if (!FU || (c & 1) == 1) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(&map_o, sb, FU ? (c - 1) * 32 : c * 32, hcol, z);
-              bulk_commit();
-            }
-            staged = true;
-          }
-        } else if (row_valid) {  // rows of a partial 32-row group: direct stores
-          if constexpr (FU) {
-            __nv_bfloat16* dst = p.out_final + frow * D + c * 32;
-#pragma unroll
-            for (int k2 = 0; k2 < 32; k2 += 8)
-              *reinterpret_cast<uint4*>(dst + k2) =
-                  make_uint4(pack_bf16(o[k2] * inv_l, o[k2 + 1] * inv_l), pack_bf16(o[k2 + 2] * inv_l, o[k2 + 3] * inv_l),
-                             pack_bf16(o[k2 + 4] * inv_l, o[k2 + 5] * inv_l), pack_bf16(o[k2 + 6] * inv_l, o[k2 + 7] * inv_l));
-          } else if (l > 0.f) {
-            float* dst = p.out + orow * D + c * 32;
-#pragma unroll
-            for (int k2 = 0; k2 < 32; k2 += 4)
-              *reinterpret_cast<float4*>(dst + k2) =
-                  make_float4(o[k2] * inv_l, o[k2 + 1] * inv_l, o[k2 + 2] * inv_l, o[k2 + 3] * inv_l);
-          }
-        }
-      }
-      if (row_valid) {
-        const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-        if constexpr (FU) p.lse_final[frow] = lse_v;
-        else p.lse[orow] = lse_v;
-      }
-      tt += w.ntiles;
-    }
-    if (!ok) fail_timeout(abort_flag, p.err);
-    if (lane == 0) bulk_wait_read_all();  // the staging buffer is released at kernel exit
-  }
-  griddep_launch_dependents();
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
 // ---------------------------------------------------------------------------------- host
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1614,10 +1188,6 @@ bool make_out_map(CUtensorMap* m, void* base, bool bf16, unsigned long long D, u
             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-// The persistent two-tile kernel on request (CP_IMPL_TCGEN05_PERSISTENT); CP_IMPL_AUTO keeps the
-// one-item-per-CTA kernel.
-bool use_persistent(const cp_prefill_args& a) { return a.impl == CP_IMPL_TCGEN05_PERSISTENT; }
 
 template <int D>
 cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* fused_out,
@@ -1690,37 +1260,7 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
                          (a.num_q_heads / (pair && !tiles ? 2 : 1));
   if (grid == 0) return cudaSuccess;
   if (grid >= (1ll << 31)) return cudaErrorInvalidConfiguration;
-  p.num_items = (int)grid;
   cudaError_t e;
-  if (pair && use_persistent(a)) {  // one CTA per SM walking every work item
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    const unsigned pgrid = (unsigned)(grid < sms ? grid : sms);
-    const int smem = LayoutP<D>::kAlloc;
-    const bool fq = p.fused && a.mode == CP_PASS_Q;
-    auto pick = [&](auto tt, auto fu) {
-      constexpr bool TTv = decltype(tt)::value, FUv = decltype(fu)::value;
-      return fq ? (page_kv ? prefill_tcp_kernel<D, (D == 128), TTv, true, FUv>
-                           : prefill_tcp_kernel<D, false, TTv, true, FUv>)
-                : (page_kv ? prefill_tcp_kernel<D, (D == 128), TTv, false, FUv>
-                           : prefill_tcp_kernel<D, false, TTv, false, FUv>);
-    };
-    auto kern = tiles ? (p.fused ? pick(std::true_type{}, std::true_type{})
-                                 : pick(std::true_type{}, std::false_type{}))
-                      : (p.fused ? pick(std::false_type{}, std::true_type{})
-                                 : pick(std::false_type{}, std::false_type{}));
-    // same register budgets as the two-tile kernel: refuse a build with another count
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    if (fa.numRegs != 168) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    kern<<<pgrid, kThreads2, smem, s>>>(mq, mk, mv, mo, p);
-    return cudaGetLastError();
-  }
   if (pair) {
     const int smem = Layout2<D>::kAlloc;
     // pass-Q at d = 128 (page_kv): K and V pages arrive as whole-page boxes laid out

@@ -65,12 +65,9 @@ typedef enum {
   CP_IMPL_AUTO = 0,     /* tcgen05 tensor-core kernel for bf16, SIMT kernel for f32   */
   CP_IMPL_TCGEN05 = 1,  /* bf16 only: TMA + tcgen05.mma + TMEM                        */
   CP_IMPL_SIMT = 2,     /* plain CUDA cores, any supported dtype (cross-check path)   */
-  CP_IMPL_TCGEN05_SINGLE = 3, /* bf16: tcgen05 kernel with one q head per CTA (the     */
+  CP_IMPL_TCGEN05_SINGLE = 3  /* bf16: tcgen05 kernel with one q head per CTA (the     */
                               /* default pairs two heads, or two row tiles of one head */
                               /* when q heads per kv head is odd)                      */
-  CP_IMPL_TCGEN05_PERSISTENT = 4  /* bf16: the two-tile tcgen05 kernel as one CTA per SM */
-                                  /* walking the work items; an item's loads and first   */
-                                  /* QK^T overlap the previous item's end                */
 } cp_impl;
 
 /* Human-readable name of a cp_status value (static string). */

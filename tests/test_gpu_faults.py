@@ -17,14 +17,13 @@ from tests.parity_util import check_partials
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("impl", ["tc", "tc1", "tcp"])
+@pytest.mark.parametrize("impl", ["tc", "tc1"])
 def test_wait_timeout_is_reported_and_context_survives(lib, impl):
     lens, Hq, Hkv, d, cp = [640], 8, 2, 128, 2
     x = wl.prefill_inputs(lens, Hq, Hkv, d, torch.bfloat16, seed=77)
     q, k, v, cu = (x[n].cuda() for n in ("q", "k", "v", "cu_seqlens"))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    code = {"tc": lib.CP_IMPL_TCGEN05, "tc1": lib.CP_IMPL_TCGEN05_SINGLE,
-            "tcp": lib.CP_IMPL_TCGEN05_PERSISTENT}[impl]
+    code = {"tc": lib.CP_IMPL_TCGEN05, "tc1": lib.CP_IMPL_TCGEN05_SINGLE}[impl]
     lib.cp_partial_attn_prefill(q, cu, cp, k=k, v=v, max_seqlen_q=640, impl=code, err=err,
                                 debug=1)
     torch.cuda.synchronize()

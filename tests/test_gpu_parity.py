@@ -94,7 +94,7 @@ def test_merge_parity(lib, P, rows, H, d, dt):
 
 def _impl_code(lib, name):
     return {"simt": lib.CP_IMPL_SIMT, "tc": lib.CP_IMPL_TCGEN05,
-            "tc1": lib.CP_IMPL_TCGEN05_SINGLE, "tcp": lib.CP_IMPL_TCGEN05_PERSISTENT}[name]
+            "tc1": lib.CP_IMPL_TCGEN05_SINGLE}[name]
 
 
 PASS_KV_CASES = [
@@ -110,7 +110,7 @@ PASS_KV_CASES = [
 ]
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc", "tc1", "tcp"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 @pytest.mark.parametrize("case", range(len(PASS_KV_CASES)))
 def test_pass_kv_parity(lib, case, impl):
     lens, Hq, Hkv, d, dt, cp = PASS_KV_CASES[case]
@@ -128,7 +128,7 @@ def test_pass_kv_parity(lib, case, impl):
     check_merged(mo, ml, Om, Lm, what=f"pass-KV {impl} merged")
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc", "tc1", "tcp"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 def test_pass_kv_single_pair(lib, impl):
     """q_shard / kv_shard restrict the launch to one rotation step; other pairs untouched."""
     lens, Hq, Hkv, d, cp = [900], 8, 2, 128, 4
@@ -165,7 +165,7 @@ def _ctx_case(q_lens, kv_lens, Hq, Hkv, d, dt, seed):
                 v=wl.normal((sum(kv_lens), Hkv, d), dt, g), cu_q=_cu(q_lens), cu_kv=_cu(kv_lens))
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc", "tc1", "tcp"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 @pytest.mark.parametrize("case", range(len(PASS_KV_CTX_CASES)))
 def test_pass_kv_cached_context_parity(lib, case, impl):
     """Pass-KV with a contiguous cached context (cu_seqlens_kv): the new queries are the last
@@ -190,7 +190,7 @@ def test_pass_kv_cached_context_parity(lib, case, impl):
         check_merged(fo, fl, Om, Lm, what=f"pass-KV cached context {impl} fused")
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc", "tc1", "tcp"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 def test_pass_kv_reports_short_kv(lib, impl):
     """A sequence with fewer kv tokens than new queries is flagged (CP_ERR_DEVICE_BOUNDS) and its
     rows skipped; the other sequences' partials still match the oracle."""
@@ -229,7 +229,7 @@ PASS_Q_CASES = [
 ]
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc", "tc1", "tcp"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 @pytest.mark.parametrize("case", range(len(PASS_Q_CASES)))
 def test_pass_q_parity(lib, case, impl):
     q_lens, kv_lens, Hq, Hkv, d, dt, cp, I = PASS_Q_CASES[case]
@@ -249,7 +249,7 @@ def test_pass_q_parity(lib, case, impl):
     check_merged(mo, ml, Om, Lm, what=f"pass-Q {impl} merged")
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc", "tc1", "tcp"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 def test_pass_q_reports_bad_page(lib, impl):
     """Block-table entries outside the pool (too large, negative) are checked before any read:
     the kernel flags CP_ERR_DEVICE_BOUNDS and the next valid call still matches the oracle."""
@@ -278,7 +278,7 @@ def test_pass_q_reports_bad_page(lib, impl):
     check_partials(out, lse, O, L, what=f"pass-Q {impl} after a bad table")
 
 
-@pytest.mark.parametrize("impl", ["simt", "tc", "tc1", "tcp"])
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 def test_pass_q_reports_short_kv(lib, impl):
     """seq_lens_kv below the new-query count (a negative cached context) lives on the device, so
     the kernels flag it (CP_ERR_DEVICE_BOUNDS) and skip the rows instead of running on."""
@@ -293,9 +293,8 @@ def test_pass_q_reports_short_kv(lib, impl):
     assert int(err.item()) == 5
 
 
-@pytest.mark.parametrize("impl", ["auto", "tcp"])
 @pytest.mark.parametrize("case", [0, 1, 2, 4, 5])
-def test_fused_pass_q_parity(lib, case, impl):
+def test_fused_pass_q_parity(lib, case):
     """cp_attn_prefill_fused over the paged round-robin cache (every rank's resident pages in
     one online softmax) = merged pass-Q partials of the oracle."""
     q_lens, kv_lens, Hq, Hkv, d, dt, cp, I = PASS_Q_CASES[case]
@@ -304,8 +303,7 @@ def test_fused_pass_q_parity(lib, case, impl):
         x["q"].to(DEV), x["cu_seqlens_q"].to(DEV), cp, mode=lib.CP_PASS_Q,
         k_cache=x["k_cache"].to(DEV), v_cache=x["v_cache"].to(DEV),
         block_tables=x["block_tables"].to(DEV), seq_lens_kv=x["seq_lens"].to(DEV), interleave=I,
-        max_seqlen_q=max(q_lens),
-        impl=lib.CP_IMPL_AUTO if impl == "auto" else lib.CP_IMPL_TCGEN05_PERSISTENT)
+        max_seqlen_q=max(q_lens))
     O, L = orc.pass_q_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
                                x["cu_seqlens_q"], x["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
     Om, Lm = orc.lse_merge(O, L)
@@ -482,16 +480,13 @@ def test_kv_cache_write_reports_missing_page(lib):
 
 # ------------------------------------------------------------------------------------ fused prefill
 
-@pytest.mark.parametrize("impl", ["auto", "tcp"])
 @pytest.mark.parametrize("case", [1, 2, 3, 4, 6, 7])
-def test_fused_prefill_parity(lib, case, impl):
+def test_fused_prefill_parity(lib, case):
     """cp_attn_prefill_fused = merged pass-KV partials = plain causal attention."""
     lens, Hq, Hkv, d, dt, cp = PASS_KV_CASES[case]
     x = wl.prefill_inputs(lens, Hq, Hkv, d, dt, seed=100 + case)
     out, lse = lib.cp_attn_prefill_fused(x["q"].to(DEV), x["cu_seqlens"].to(DEV), cp,
-                                         x["k"].to(DEV), x["v"].to(DEV), max_seqlen_q=max(lens),
-                                         impl=lib.CP_IMPL_AUTO if impl == "auto"
-                                         else lib.CP_IMPL_TCGEN05_PERSISTENT)
+                                         x["k"].to(DEV), x["v"].to(DEV), max_seqlen_q=max(lens))
     O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], cp, 1 / math.sqrt(d))
     Om, Lm = orc.lse_merge(O, L)
     check_merged(out, lse, Om, Lm, what="fused prefill")
