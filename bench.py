@@ -42,13 +42,15 @@ import workloads as wl  # noqa: E402
 # each from one ncu capture of the named kernel at the recorded source SHA-1.  A figure is
 # reported only while that source file still has this SHA-1; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # prefill_tc2_kernel<128,0,0,0> on the full prefill: dram read 42.04 MB + write 62.57 MB
+    # prefill_tc2_kernel<128,0,0,0>, 12-warp build, full prefill: dram read 42.11 MB + write 59.34 MB
     ("prefill", "full"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                          "sha1": "f72141077f3eace2e0309ce3d75b4c80a82e1d37", "bytes": 104614400},
-    # decode_mma_kernel<128,4,0>: a 16-sequence capture (1.1187 GB read + 5.36 MB written),
-    # scaled to the 64-sequence decode workload by algorithmic bytes (4.3933e9 / 1.1181e9)
+                          "sha1": "14702212c0b8a58968b6a97d2d69140f334579b9", "bytes": 101450000},
+    # the same kernel on the long prefill: dram read 1.43 GB + write 1.75 GB
+    ("prefill", "long"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
+                          "sha1": "14702212c0b8a58968b6a97d2d69140f334579b9", "bytes": 3180000000},
+    # decode_mma_kernel<128,4,0>, 64-sequence decode: dram read 4.40 GB + write 8.38 MB
     ("decode", "decode"): {"file": "context_gqa_attention_gb300/csrc/decode.cu",
-                           "sha1": "9b0d529eacd73ab4391495a21d18a2e537d1c074", "bytes": 4416620000},
+                           "sha1": "6ac2ef88b7a62cb153e08f4e82625259b1afe4f6", "bytes": 4408380000},
 }
 
 FALLBACK_HBM_GBS = 6800.0
