@@ -191,6 +191,30 @@ def test_pass_kv_cached_context_parity(lib, case, impl):
 
 
 @pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
+def test_pass_kv_cached_context_single_pair(lib, impl):
+    """One rotation step over a cached context: q_shard / kv_shard select one (Q shard, KV shard)
+    pair, the KV shard cut over the kv length; the other pairs' outputs stay untouched."""
+    q_lens, kv_lens, Hq, Hkv, d, cp = [300], [1700], 8, 2, 128, 3
+    x = _ctx_case(q_lens, kv_lens, Hq, Hkv, d, torch.bfloat16, 91)
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_q"], cp, 1 / math.sqrt(d),
+                                cu_seqlens_kv=x["cu_kv"])
+    part = orc.partition(q_lens, cp)
+    out = torch.full((cp, 300, Hq, d), 7.0, device=DEV)
+    lse = torch.full((cp, 300, Hq), 7.0, device=DEV)
+    qs, ks = 2, 1
+    lib.cp_partial_attn_prefill(x["q"].to(DEV), x["cu_q"].to(DEV), cp, k=x["k"].to(DEV),
+                                v=x["v"].to(DEV), cu_seqlens_kv=x["cu_kv"].to(DEV), q_shard=qs,
+                                kv_shard=ks, out=out, lse=lse, impl=_impl_code(lib, impl),
+                                max_seqlen_q=300)
+    rows = part["perm"][part["shard_offsets"][qs]:part["shard_offsets"][qs + 1]]
+    check_partials(out[ks:ks + 1], lse[ks:ks + 1], O[ks:ks + 1][:, rows], L[ks:ks + 1][:, rows],
+                   rows=rows.tolist(), what=f"cached-context single pair {impl}")
+    mask = torch.ones(cp, 300, dtype=torch.bool)
+    mask[ks, torch.as_tensor(rows)] = False
+    assert (lse.cpu()[mask] == 7.0).all()
+
+
+@pytest.mark.parametrize("impl", ["simt", "tc", "tc1"])
 def test_pass_kv_reports_short_kv(lib, impl):
     """A sequence with fewer kv tokens than new queries is flagged (CP_ERR_DEVICE_BOUNDS) and its
     rows skipped; the other sequences' partials still match the oracle."""

@@ -1,7 +1,8 @@
 """Seeded random sweep of small shapes against the float64 oracle: varlen batches with ragged
 lengths (including 1 and lengths below 2cp), cp in 1..8, query heads per kv head in 1..16,
-head_dim 64 / 128, interleave sizes 1..16, for pass-KV (partials, merged and fused), pass-Q
-over paged round-robin caches, and decode (partials and fused).  Each case is small enough for
+head_dim 64 / 128, interleave sizes 1..16, for pass-KV (partials, merged and fused; plain and
+over a contiguous cached context), pass-Q over paged round-robin caches, and decode (partials
+and fused).  Each case is small enough for
 the oracle; the sweep looks for edge cases the hand-picked cases miss."""
 import math
 import random
@@ -46,6 +47,35 @@ def test_random_pass_kv(lib, seed):
     mo, ml = lib.cp_lse_merge(out, lse, out_dtype=torch.bfloat16)
     check_merged(mo, ml, Om, Lm, what=what + " merged")
     fo, fl = lib.cp_attn_prefill_fused(q, cu, cp, k, v, max_seqlen_q=max(lens))
+    check_merged(fo, fl, Om, Lm, what=what + " fused")
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_pass_kv_cached_context(lib, seed):
+    r = random.Random(4000 + seed)
+    B = r.randint(1, 3)
+    cp = r.randint(1, 8)
+    q_lens = [r.choice([0, 1, r.randint(2, 2 * cp), r.randint(2, 400)]) for _ in range(B)]
+    kv_lens = [ql + r.choice([0, r.randint(1, 2 * cp), r.randint(1, 1200)]) for ql in q_lens]
+    Hq, Hkv = _rand_heads(r, 8)
+    d = r.choice([64, 128])
+    g = torch.Generator().manual_seed(9000 + seed)
+    qh = wl.normal((sum(q_lens), Hq, d), torch.bfloat16, g)
+    kh = wl.normal((sum(kv_lens), Hkv, d), torch.bfloat16, g)
+    vh = wl.normal((sum(kv_lens), Hkv, d), torch.bfloat16, g)
+    cu, cu_kv = _cu(q_lens), _cu(kv_lens)
+    what = f"pass-KV cached q={q_lens} kv={kv_lens} cp={cp} Hq/Hkv={Hq}/{Hkv} d={d}"
+    if sum(q_lens) == 0:
+        pytest.skip(what + ": no query rows")
+    args = (qh.to(DEV), cu.to(DEV), cp)
+    kw = dict(k=kh.to(DEV), v=vh.to(DEV), cu_seqlens_kv=cu_kv.to(DEV), max_seqlen_q=max(q_lens))
+    out, lse = lib.cp_partial_attn_prefill(*args, **kw)
+    O, L = orc.pass_kv_partials(qh, kh, vh, cu, cp, 1 / math.sqrt(d), cu_seqlens_kv=cu_kv)
+    check_partials(out, lse, O, L, what=what)
+    Om, Lm = orc.lse_merge(O, L)
+    mo, ml = lib.cp_lse_merge(out, lse, out_dtype=torch.bfloat16)
+    check_merged(mo, ml, Om, Lm, what=what + " merged")
+    fo, fl = lib.cp_attn_prefill_fused(*args, **kw)
     check_merged(fo, fl, Om, Lm, what=what + " fused")
 
 
