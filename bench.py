@@ -288,9 +288,10 @@ def prefill_config(w):
             "head_dim": w.head_dim, "mode": "pass_kv"}
 
 
-def line_config(w, ws):
+def line_config(w, ws, runner=None):
     """The `config` of a JSON line (the same for both arms)."""
     base = (prefill_config(w) if w.kind == "pass_kv" else
+            runner.config() if runner is not None else
             {"workload": w.name, "global_batch": w.num_seqs, "cp": w.cp, "mode": w.kind})
     return dict(base, l2="flushed between timed steps (512 MB write)",
                 parallelism=f"replicas x{ws} (logical CP shards on each GPU)")
@@ -997,7 +998,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32", "data": "synthetic",
-            "config": line_config(w, ws),
+            "config": line_config(w, ws, runner),
             "roofline": roof, "clocks": clk,
             "gpu_launches": runner.launches_per_step * args.steps,
             "source_sha1": source_sha1()}

@@ -162,17 +162,35 @@ CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = 
   w.valid = 0;
   // 32-bit divisions: the item space is below 2^31
   const unsigned groups = (unsigned)(p.Hq / hpc);
+  const unsigned nslot = 2u * (unsigned)p.cp * (unsigned)p.TPC;
   w.h = (int)(lin % groups) * hpc;
   lin /= groups;
-  if (p.kv_shard >= 0 || p.fused) {
-    w.p = p.fused ? 0 : p.kv_shard;
+  int slot;
+  if (p.mode == CP_PASS_Q) {
+    // pass-Q items cost about the same (every query sees its rank's whole cached context), so
+    // they run sequence by sequence and rank by rank: the CTAs resident at one time read the
+    // pages of one or two (sequence, rank) pairs, which stay in L2
+    slot = (int)(lin % nslot);
+    lin /= nslot;
+    if (p.kv_shard >= 0 || p.fused) {
+      w.p = p.fused ? 0 : p.kv_shard;
+    } else {
+      w.p = (int)(lin % (unsigned)p.cp);
+      lin /= (unsigned)p.cp;
+    }
+    w.b = (int)lin;
   } else {
-    w.p = (int)(lin % (unsigned)p.cp);
-    lin /= (unsigned)p.cp;
+    // pass-KV: sequence by sequence, each heaviest tile first (last chunk, last tile), so the
+    // grid still ends on light items and the CTAs resident at one time read one sequence's K/V
+    if (p.kv_shard >= 0 || p.fused) {
+      w.p = p.fused ? 0 : p.kv_shard;
+    } else {
+      w.p = (int)(lin % (unsigned)p.cp);
+      lin /= (unsigned)p.cp;
+    }
+    slot = (int)(lin % nslot);
+    w.b = (int)(lin / nslot);
   }
-  w.b = (int)(lin % (unsigned)p.B);
-  lin /= (unsigned)p.B;
-  const int slot = (int)lin;  // heaviest tiles first: last chunk, last tile
   const int c = 2 * p.cp - 1 - slot / p.TPC;
   const int j = p.TPC - 1 - slot % p.TPC;
   const int q0 = p.cu_q[w.b];
