@@ -827,6 +827,13 @@ def e2e_block(runner, steps, stream, ws, dev, unit):
             "checked": "last host output == device-only step (bitwise)"}
 
 
+def traffic_key(runner):
+    """The NCU_TRAFFIC record of a runner's dominant kernel in its current form."""
+    kind = ("decode" if isinstance(runner, DecodeRunner) else
+            "pass_q" if isinstance(runner, PassQRunner) else "prefill")
+    return (kind + ("_fused" if runner.fused else ""), runner.w.name)
+
+
 def prefill_kernel_name(runner):
     if isinstance(runner, PassQRunner):
         return ("cp_attn_prefill_fused (pass-Q, paged, ranks merged in-kernel)" if runner.fused
@@ -835,7 +842,7 @@ def prefill_kernel_name(runner):
             else "cp_partial_attn_prefill (pass-KV)")
 
 
-def measure_prefill_form(runner, fused, steps, flush, dev, stream, pk, with_traffic=None):
+def measure_prefill_form(runner, fused, steps, flush, dev, stream, pk):
     """One prefill form (partials + merge, or the fused launch) of a runner: step value and the
     dominant kernel's roofline."""
     runner.fused = fused
@@ -844,7 +851,7 @@ def measure_prefill_form(runner, fused, steps, flush, dev, stream, pk, with_traf
     return {"value": runner.metric(statistics.mean(st) / 1e3), "unit": "TFLOP/s",
             "ms_per_step": statistics.mean(st),
             "roofline": roofline("tensor", prefill_kernel_name(runner), runner.flops, d_s, pk,
-                                 traffic=with_traffic,
+                                 traffic=ncu_traffic(*traffic_key(runner)),
                                  algorithmic=f"{runner.flops:.4e} causal FLOP per launch")}
 
 
@@ -871,8 +878,7 @@ def secondaries(args, primary, w, dev, stream, flush, pk, ws):
         fr = PrefillRunner(wl.WORKLOADS["full"], dev, cpa)
         for fused in (False, True):
             sec["full_prefill_fused" if fused else "full_prefill"] = dict(
-                measure_prefill_form(fr, fused, n, flush, dev, stream, pk,
-                                     with_traffic=None if fused else ncu_traffic("prefill", "full")),
+                measure_prefill_form(fr, fused, n, flush, dev, stream, pk),
                 config=fr.config())
         del fr
     if w.name != "chunked":
@@ -896,7 +902,7 @@ def secondaries(args, primary, w, dev, stream, flush, pk, ws):
         e = {"value": dr.metric(statistics.mean(ds) / 1e3), "unit": "GB/s", "config": dr.config(),
              "roofline": roofline("hbm", "cp_decode_attention (partials + merge, one launch)" if fused
                                   else "cp_partial_attn_decode", dr.bytes, d_s, pk,
-                                  traffic=None if fused else ncu_traffic("decode", "decode"),
+                                  traffic=ncu_traffic(*traffic_key(dr)),
                                   algorithmic=f"{dr.bytes:.4e} B per launch (KV once + q + out + tables)")}
         seqs = [0, 1, 2, 3, 4, 5]
         Om, Lm = oracle_decode(dr, seqs)
@@ -982,13 +988,12 @@ def main():
     if isinstance(runner, DecodeRunner):
         roof = roofline("hbm", "cp_decode_attention (partials + merge, one launch)" if runner.fused
                         else "cp_partial_attn_decode", runner.bytes, dom_s, pk,
-                        traffic=None if runner.fused else ncu_traffic("decode", w.name),
+                        traffic=ncu_traffic(*traffic_key(runner)),
                         algorithmic=f"{runner.bytes:.4e} B per launch (KV once + q + out + tables)")
         metric, unit = "decode KV-read GB/s (partial attention + LSE merge)", "GB/s"
     else:
         roof = roofline("tensor", prefill_kernel_name(runner), runner.flops, dom_s, pk,
-                        traffic=None if runner.fused else ncu_traffic(
-                            "prefill" if isinstance(runner, PrefillRunner) else "pass_q", w.name),
+                        traffic=ncu_traffic(*traffic_key(runner)),
                         algorithmic=f"{runner.flops:.4e} causal FLOP per launch")
         metric = (PREFILL_METRIC if isinstance(runner, PrefillRunner) and not runner.fused else
                   "causal GQA prefill TFLOP/s (" + prefill_kernel_name(runner) + ")")
