@@ -985,8 +985,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(BM, BN, false, false);
       const uint32_t id_pv = idesc_bf16_f32(BM, D, false, true);
+      // shared-memory descriptors built once (Q tiles, ring slot 0 as a K and as a V operand) and
+      // advanced by constant offsets: the issuing thread sits on the critical path between a
+      // softmax hand-off and the tensor pipe, so its instructions per MMA matter
+      const uint64_t dq0 = desc_sw128(sQ, 16, 1024);
+      const uint64_t dk0 = desc_sw128(sKV, 16, PG ? 2048u : 1024u);
+      const uint64_t dv0 = PG ? desc_sw128(sKV, 1024, 2048) : desc_sw128(sKV, BN * 128, 1024);
       auto issue_qk = [&](int tile, int slot) {
-        const uint32_t q = sQ + tile * Ly::kQ, k = sKV + slot * Ly::kKV;
+        const uint64_t dq = desc_advance(dq0, (uint32_t)(tile * Ly::kQ));
+        const uint64_t dk = desc_advance(dk0, (uint32_t)(slot * Ly::kKV));
         const uint32_t dS = tmem + (uint32_t)(tile * BN);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -994,19 +1001,17 @@ __global__ void __launch_bounds__(kThreads2, 1)
           // paged slot: 64-column block at +1 KB, 8-key groups 2 KB apart; tiled: block at
           // +BN x 128 B, groups 1 KB apart
           const uint32_t offk = (kk / 4) * (PG ? 1024u : (uint32_t)(BN * 128)) + (kk % 4) * 32;
-          mma_ss(dS, desc_sw128(q + offq, 16, 1024), desc_sw128(k + offk, 16, PG ? 2048u : 1024u),
-                 id_qk, kk > 0 ? 1u : 0u);
+          mma_ss(dS, desc_advance(dq, offq), desc_advance(dk, offk), id_qk, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int tile, int slot, bool acc) {
-        const uint32_t v = sKV + slot * Ly::kKV;
+        const uint64_t dv = desc_advance(dv0, (uint32_t)(slot * Ly::kKV));
         const uint32_t dO = tmem + 256u + (uint32_t)(tile * D);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           // 16 keys = one page: paged slot (halves 1 KB apart, 8-key groups 2 KB apart) or
           // the tiled layout (halves BN x 128 B apart, groups 1 KB apart)
-          const uint64_t bd = PG ? desc_sw128(v + kk * 4096, 1024, 2048)
-                                 : desc_sw128(v + kk * 16 * 128, BN * 128, 1024);
+          const uint64_t bd = desc_advance(dv, PG ? kk * 4096u : kk * 16u * 128u);
           // P: 8 packed TMEM columns per 16 keys, the A operand from tensor memory
           mma_ts(dO, tmem + (uint32_t)(tile * BN + kk * 8), bd, id_pv, (acc || kk > 0) ? 1u : 0u);
         }

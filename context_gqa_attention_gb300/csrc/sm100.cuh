@@ -194,6 +194,18 @@ SM100_DEV uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// The same descriptor for a start address `bytes` further on: the address field is the low
+// 14 bits of (address >> 4) and shared memory addresses stay below 2^18, so adding to the low
+// word never carries into the other fields.  One 32-bit add instead of rebuilding the descriptor.
+SM100_DEV uint64_t desc_advance(uint64_t d, uint32_t bytes) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(d));
+  lo += bytes >> 4;
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and f32 accumulation.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
                                                       bool b_mn_major) {
