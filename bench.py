@@ -420,6 +420,9 @@ class PassQRunner(Runner):
         self.flops = 4.0 * d * Hq * pairs
         self.impl = cpa.CP_IMPL_AUTO
         self.fused = False
+        # the fused form's tail-split workspace (0 bytes: every item runs whole)
+        self.split_bytes = cpa.cp_prefill_fused_workspace_size(B, Hq, Hkv, d, cp, w.q_len)
+        self.buf["fws"] = torch.empty(self.split_bytes, dtype=torch.uint8, device=dev)
 
     def step(self, ev=None):
         cpa, w, b = self.cpa, self.w, self.buf
@@ -436,7 +439,8 @@ class PassQRunner(Runner):
 
     @property
     def launches_per_step(self):
-        return 3 if self.fused else 4
+        # fused: attention (+ the split tail's merge) ; else attention + merge; both + 2 maps
+        return (3 + (self.split_bytes > 0)) if self.fused else 4
 
     def _attention(self, ev=None):
         cpa, w, b = self.cpa, self.w, self.buf
@@ -446,7 +450,8 @@ class PassQRunner(Runner):
         if ev is not None:
             ev[0].record()
         if self.fused:  # every rank's resident pages walked inside one item: final output
-            cpa.cp_attn_prefill_fused(b["q"], b["cu_q"], w.cp, out=b["out"], out_lse=b["olse"], **kw)
+            cpa.cp_attn_prefill_fused(b["q"], b["cu_q"], w.cp, out=b["out"], out_lse=b["olse"],
+                                      workspace=b["fws"], **kw)
             if ev is not None:
                 ev[1].record()
             return
@@ -836,8 +841,11 @@ def traffic_key(runner):
 
 def prefill_kernel_name(runner):
     if isinstance(runner, PassQRunner):
-        return ("cp_attn_prefill_fused (pass-Q, paged, ranks merged in-kernel)" if runner.fused
-                else "cp_partial_attn_prefill (pass-Q, paged)")
+        if runner.fused:
+            return ("cp_attn_prefill_fused (pass-Q, paged, ranks merged in-kernel"
+                    + ("; last wave's items split by rank range, then merged)" if runner.split_bytes
+                       else ")"))
+        return "cp_partial_attn_prefill (pass-Q, paged)"
     return ("cp_attn_prefill_fused (pass-KV, shards merged in-kernel)" if runner.fused
             else "cp_partial_attn_prefill (pass-KV)")
 

@@ -27,7 +27,8 @@ __all__ = [
     "cp_partition", "cp_kv_interleave_layout",
     "cp_partial_attn_prefill", "cp_decode_plan", "cp_partial_attn_decode", "cp_lse_merge",
     "cp_decode_workspace_size", "cp_decode_attention", "cp_decode_attention_noalloc",
-    "cp_kv_cache_write", "cp_select_prefill_mode", "cp_attn_prefill_fused", "STATUS",
+    "cp_kv_cache_write", "cp_select_prefill_mode", "cp_attn_prefill_fused",
+    "cp_prefill_fused_workspace_size", "STATUS",
 ]
 
 CP_F32, CP_BF16 = 0, 1
@@ -93,7 +94,10 @@ _SIGS = [
                                                  _vp]),
     ("cp_kv_cache_write", ctypes.c_int32, [_vp, _vp, _vp, _vp] + [ctypes.c_int32] * 8 +
      [_vp, ctypes.c_int32, ctypes.c_int64, _vp, _vp, _vp, _vp]),
-    ("cp_attn_prefill_fused", ctypes.c_int32, [ctypes.POINTER(PrefillArgs), _vp, _vp, _vp]),
+    ("cp_prefill_fused_workspace_size", ctypes.c_int32, [ctypes.POINTER(PrefillArgs),
+                                                         ctypes.POINTER(ctypes.c_size_t)]),
+    ("cp_attn_prefill_fused", ctypes.c_int32, [ctypes.POINTER(PrefillArgs), _vp, ctypes.c_size_t,
+                                               _vp, _vp, _vp]),
     ("cp_select_prefill_mode", ctypes.c_int32, [ctypes.c_int64, ctypes.c_int64] + [ctypes.c_int32] * 4),
     ("cp_partial_attn_prefill", ctypes.c_int32, [ctypes.POINTER(PrefillArgs), _vp]),
     ("cp_decode_plan", ctypes.c_int32, [ctypes.c_int32] * 6 + [ctypes.POINTER(ctypes.c_int32)] * 2),
@@ -346,11 +350,14 @@ def cp_partial_attn_prefill(q, cu_seqlens_q, cp, *, mode=CP_PASS_KV, k=None, v=N
 def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k=None, v=None, *, mode=CP_PASS_KV,
                           cu_seqlens_kv=None, k_cache=None, v_cache=None, block_tables=None,
                           seq_lens_kv=None, interleave=8, max_seqlen_q=None, softmax_scale=0.0,
-                          impl=CP_IMPL_AUTO, out=None, out_lse=None, stream=None):
+                          impl=CP_IMPL_AUTO, workspace=None, out=None, out_lse=None,
+                          stream=None):
     """Prefill with the merge folded in (see cpattn.h): exact causal attention out [Nq, Hq, d]
     bf16 and lse [Nq, Hq] f32 without partials.  PASS_KV: k, v [Nkv, Hkv, d] (cu_seqlens_kv as
     in cp_partial_attn_prefill).  PASS_Q: the paged round-robin cache as in
-    cp_partial_attn_prefill (every rank's resident tokens in one pass)."""
+    cp_partial_attn_prefill (every rank's resident tokens in one pass); `workspace` (uint8
+    CUDA tensor of cp_prefill_fused_workspace_size() bytes) lets it split the tail wave's
+    items by rank range; None allocates it, an empty tensor runs every item whole."""
     load()
     Nq, Hq, d = q.shape
     B = cu_seqlens_q.numel() - 1
@@ -382,8 +389,30 @@ def cp_attn_prefill_fused(q, cu_seqlens_q, cp, k=None, v=None, *, mode=CP_PASS_K
         a.block_tables, a.max_blocks = _ptr(block_tables), block_tables.shape[-1]
         a.block_size, a.interleave = k_cache.shape[3], interleave
         a.seq_lens_kv = _ptr(seq_lens_kv)
-    _check(_LIB.cp_attn_prefill_fused(ctypes.byref(a), _ptr(out), _ptr(out_lse), _stream(stream)))
+    if workspace is None:
+        need = ctypes.c_size_t()
+        _check(_LIB.cp_prefill_fused_workspace_size(ctypes.byref(a), ctypes.byref(need)))
+        workspace = torch.empty(need.value, dtype=torch.uint8, device=q.device)
+    _dev(workspace, "workspace")
+    ws, ws_bytes = (_ptr(workspace), workspace.numel()) if workspace.numel() else (None, 0)
+    _check(_LIB.cp_attn_prefill_fused(ctypes.byref(a), ws, ws_bytes, _ptr(out), _ptr(out_lse),
+                                      _stream(stream)))
     return out, out_lse
+
+
+def cp_prefill_fused_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, cp,
+                                    max_seqlen_q, *, mode=CP_PASS_Q, impl=CP_IMPL_AUTO):
+    """Bytes of workspace cp_attn_prefill_fused splits its tail wave with on the current device
+    (0: no split for these shapes)."""
+    load()
+    a = PrefillArgs()
+    a.mode, a.dtype, a.impl = mode, CP_BF16, impl
+    a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.cp = (
+        num_seqs, num_q_heads, num_kv_heads, head_dim, cp)
+    a.max_seqlen_q, a.q_shard, a.kv_shard = max_seqlen_q, -1, -1
+    need = ctypes.c_size_t()
+    _check(_LIB.cp_prefill_fused_workspace_size(ctypes.byref(a), ctypes.byref(need)))
+    return need.value
 
 
 def cp_decode_plan(num_seqs, num_kv_heads, cp, interleave, block_size, max_seq_len):

@@ -582,7 +582,8 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* a, void* stream) {
   return launched(cp_launch_prefill_simt(*a, scale, as_stream(stream)), "prefill (simt) launch");
 }
 
-cp_status cp_attn_prefill_fused(const cp_prefill_args* a, void* out, float* out_lse, void* stream) {
+// Shape arguments of the fused prefill (those its split plan reads too).
+static cp_status check_fused_shape(const cp_prefill_args* a) {
   REQUIRE(a != nullptr, "args is null");
   REQUIRE(a->mode == CP_PASS_KV || a->mode == CP_PASS_Q, "mode must be CP_PASS_KV or CP_PASS_Q");
   if (a->dtype != CP_BF16) return fail(CP_ERR_UNSUPPORTED, "the fused prefill takes bf16 inputs");
@@ -590,21 +591,41 @@ cp_status cp_attn_prefill_fused(const cp_prefill_args* a, void* out, float* out_
     return fail(CP_ERR_UNSUPPORTED, "the fused pass-Q prefill runs on the two-tile kernel only");
   if (a->head_dim != 64 && a->head_dim != 128)
     return fail(CP_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", a->head_dim);
-  REQUIRE(a->num_seqs >= 1 && a->num_kv_heads >= 1 && a->num_q_heads % a->num_kv_heads == 0,
+  REQUIRE(a->num_seqs >= 1 && a->num_kv_heads >= 1 && a->num_q_heads >= 1 &&
+              a->num_q_heads % a->num_kv_heads == 0,
           "bad head counts");
   REQUIRE(a->cp >= 1 && a->cp <= 64, "cp must be in [1, 64]");
   REQUIRE(a->q_shard == -1 && a->kv_shard == -1, "the fused prefill covers every pair");
   REQUIRE(a->total_q >= 0 && a->max_seqlen_q >= 0, "bad total_q / max_seqlen_q");
+  return CP_OK;
+}
+
+cp_status cp_prefill_fused_workspace_size(const cp_prefill_args* a, size_t* bytes) {
+  REQUIRE(bytes != nullptr, "bytes is null");
+  *bytes = 0;
+  const cp_status st = check_fused_shape(a);
+  if (st != CP_OK) return st;
+  *bytes = cp_prefill_fused_split_bytes(*a);
+  return ok();
+}
+
+cp_status cp_attn_prefill_fused(const cp_prefill_args* a, void* workspace, size_t workspace_bytes,
+                                void* out, float* out_lse, void* stream) {
+  cp_status st = check_fused_shape(a);
+  if (st != CP_OK) return st;
   REQUIRE(a->cu_seqlens_q != nullptr, "cu_seqlens_q is null");
   REQUIRE_PTR(a->q);
-  const cp_status st = check_kv_source(a);
+  st = check_kv_source(a);
   if (st != CP_OK) return st;
   REQUIRE_PTR(out);
   REQUIRE(out_lse != nullptr, "out_lse is null");
   REQUIRE(a->debug == 0, "debug must be 0");
+  REQUIRE(workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
+          "workspace must be 256-byte aligned");
   if (a->total_q == 0) return ok();
   const float scale = a->softmax_scale > 0.f ? a->softmax_scale : 1.f / sqrtf((float)a->head_dim);
-  return launched(cp_launch_prefill_fused(*a, scale, out, out_lse, as_stream(stream)),
+  return launched(cp_launch_prefill_fused(*a, scale, out, out_lse, workspace,
+                                          workspace ? workspace_bytes : 0, as_stream(stream)),
                   "fused prefill launch");
 }
 

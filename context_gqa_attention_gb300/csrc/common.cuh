@@ -104,8 +104,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 // argument validation.  They return the launch status.
 cudaError_t cp_launch_prefill_simt(const cp_prefill_args& a, float scale, cudaStream_t s);
 cudaError_t cp_launch_prefill_tc(const cp_prefill_args& a, float scale, cudaStream_t s);
+// ws / ws_bytes: scratch for the fused pass-Q tail split (NULL or too small: no split)
 cudaError_t cp_launch_prefill_fused(const cp_prefill_args& a, float scale, void* out, float* lse,
-                                    cudaStream_t s);
+                                    void* ws, size_t ws_bytes, cudaStream_t s);
+// Scratch bytes the fused prefill's tail split wants on the current device (0: no split).
+size_t cp_prefill_fused_split_bytes(const cp_prefill_args& a);
 bool cp_prefill_tc_supported(const cp_prefill_args& a);
 cudaError_t cp_launch_decode(const cp_decode_args& a, float scale, cudaStream_t s);
 // 2D bf16 TMA descriptor (CUtensorMap, 64-byte aligned storage of 128 bytes) over `rows` rows

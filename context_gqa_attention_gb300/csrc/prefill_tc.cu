@@ -61,6 +61,13 @@ struct TcParams {
   float* lse_final;
   // 1: the output tensor map is valid and full 32-row groups are written by TMA stores
   int tma_out;
+  // fused pass-Q, split tail: CTAs past the first n_whole run one of split_k rank ranges of
+  // item n_whole + (CTA - n_whole) / split_k and write its normalised rows and LSEs to
+  // ws_out [piece][2][BM][d] / ws_lse [piece][2][BM] (piece = CTA - n_whole; 2 = the CTA's
+  // tiles) for fq_split_merge_kernel.  split_k <= 1: every item runs whole.
+  int n_whole, split_k;
+  float* ws_out;
+  float* ws_lse;
 };
 
 template <int D>
@@ -90,6 +97,7 @@ struct Work {
   int kv_row0;              // pass-KV: first token-major kv row of the sequence
   int ks[2], ke[2], nt[2];  // pass-KV key ranges (positions) and their tile counts
   int n_local;              // pass-Q: resident tokens of rank p that any row can see
+  int r_lo, r_hi;           // fused pass-Q: the ranks the item walks
   int ntiles;
 };
 
@@ -136,30 +144,34 @@ CP_DEV void page_rows(const int (&id)[NP], int t, int n_local, long long pool, i
 struct RankWalk {
   int r, tr, nt_r, n_r;
 };
-CP_DEV void walk_settle(RankWalk& k, long long kv_end, int cp, int I) {
-  while (k.tr >= k.nt_r && k.r + 1 < cp) {
+CP_DEV void walk_settle(RankWalk& k, long long kv_end, int cp, int I, int r_end) {
+  while (k.tr >= k.nt_r && k.r + 1 < r_end) {
     ++k.r;
     k.n_r = rank_local_len(kv_end, k.r, cp, I);
     k.nt_r = (k.n_r + BN - 1) / BN;
     k.tr = 0;
   }
 }
-CP_DEV RankWalk walk_start(long long kv_end, int cp, int I) {
-  RankWalk k{-1, 0, 0, 0};
-  walk_settle(k, kv_end, cp, I);
+CP_DEV RankWalk walk_start(long long kv_end, int cp, int I, int r_lo, int r_end) {
+  RankWalk k{r_lo - 1, 0, 0, 0};
+  walk_settle(k, kv_end, cp, I, r_end);
   return k;
 }
-CP_DEV void walk_next(RankWalk& k, long long kv_end, int cp, int I) {
+CP_DEV void walk_next(RankWalk& k, long long kv_end, int cp, int I, int r_end) {
   ++k.tr;
-  walk_settle(k, kv_end, cp, I);
+  walk_settle(k, kv_end, cp, I, r_end);
 }
 
 // Work item index -> (q tile slot, sequence, kv shard, head group of `hpc` consecutive q heads).
 // Slots run heaviest first (last chunk, last tile) so long items start early.
 // `span` query rows per item: BM (one tile; head pairs) or 2 BM (two tiles of one head).
-CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = BM) {
+// Fused pass-Q items walk ranks [r_lo, r_hi) (all of them unless the item is split).
+CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = BM, int r_lo = 0,
+                           int r_hi = 1 << 30) {
   Work w;
   w.valid = 0;
+  w.r_lo = r_lo;
+  w.r_hi = min(r_hi, p.cp);
   // 32-bit divisions: the item space is below 2^31
   const unsigned groups = (unsigned)(p.Hq / hpc);
   const unsigned nslot = 2u * (unsigned)p.cp * (unsigned)p.TPC;
@@ -247,7 +259,8 @@ CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = 
     w.qpos0 = C + w.q_lo;
     if (p.fused) {  // every rank's resident tokens any row can see, rank after rank
       w.n_local = 0;
-      for (int r = 0; r < p.cp; ++r) w.ntiles += (rank_local_len(C + w.q_hi, r, p.cp, p.I) + BN - 1) / BN;
+      for (int r = w.r_lo; r < w.r_hi; ++r)
+        w.ntiles += (rank_local_len(C + w.q_hi, r, p.cp, p.I) + BN - 1) / BN;
     } else {
       w.n_local = rank_local_len(C + w.q_hi, w.p, p.cp, p.I);
       w.ntiles = (w.n_local + BN - 1) / BN;
@@ -257,6 +270,20 @@ CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = 
 }
 CP_DEV Work decode_work(const TcParams& p, int hpc, int span = BM) {
   return decode_work_at(p, blockIdx.x, hpc, span);
+}
+// Fused pass-Q: this CTA's item, or (piece >= 0) one rank range of a split item.
+CP_DEV Work decode_split_work(const TcParams& p, int hpc, int span, int& piece) {
+  unsigned lin = blockIdx.x;
+  int r_lo = 0, r_hi = p.cp;
+  piece = -1;
+  if (p.split_k > 1 && lin >= (unsigned)p.n_whole) {
+    piece = (int)(lin - (unsigned)p.n_whole);
+    const int part = piece % p.split_k;
+    lin = (unsigned)p.n_whole + (unsigned)(piece / p.split_k);
+    r_lo = part * p.cp / p.split_k;
+    r_hi = (part + 1) * p.cp / p.split_k;
+  }
+  return decode_work_at(p, lin, hpc, span, r_lo, r_hi);
 }
 
 CP_DEV uint32_t pack_bf16(float lo, float hi) {
@@ -839,7 +866,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
   constexpr int KB = D / 64;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Work w = TT ? decode_work(p, 1, 2 * BM) : decode_work(p, 2);
+  int piece = -1;  // fused pass-Q: >= 0 when this CTA runs one rank range of a split item
+  const Work w = FQ ? decode_split_work(p, TT ? 1 : 2, TT ? 2 * BM : BM, piece)
+                    : (TT ? decode_work(p, 1, 2 * BM) : decode_work(p, 2));
   if (!w.valid) return;
 
   if (w.ntiles == 0) {  // empty pair
@@ -848,7 +877,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const int row = (warp & 3) * 32 + lane + (TT ? tile * BM : 0);  // within the item
       const int hcol = w.h + (TT ? 0 : tile);
       if (w.q_lo + row < w.q_hi) {
-        if (p.fused) {  // no visible key at all: exact attention is 0 with lse -inf
+        if (piece >= 0) {  // no visible key in this rank range
+          p.ws_lse[((long long)piece * 2 + tile) * BM + (warp & 3) * 32 + lane] = -INFINITY;
+        } else if (p.fused) {  // no visible key at all: exact attention is 0 with lse -inf
           const long long frow = (long long)(w.q_row0 + row) * p.Hq + hcol;
           for (int c = 0; c < D; ++c) p.out_final[frow * D + c] = __float2bfloat16_rn(0.f);
           p.lse_final[frow] = -INFINITY;
@@ -922,7 +953,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const long long kv_end = w.qpos0 - w.q_lo + w.q_hi;
       RankWalk kw{0, 0, 0, 0};
       if constexpr (FQ) {
-        kw = walk_start(kv_end, p.cp, p.I);
+        kw = walk_start(kv_end, p.cp, p.I, w.r_lo, w.r_hi);
         fetch_page_ids(table_of(kw.r), kw.tr, kw.n_r, p.max_blocks, pid);
       } else {
         if (p.mode == CP_PASS_Q) fetch_page_ids(trow, 0, w.n_local, p.max_blocks, pid);
@@ -949,7 +980,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             if constexpr (FQ) {
               page_rows(pid, kw.tr, kw.n_r, p.pool, p.Hkv, kw.r, w.g, p.err, prow);
               RankWalk kn = kw;  // the next tile
-              walk_next(kn, kv_end, p.cp, p.I);
+              walk_next(kn, kv_end, p.cp, p.I, w.r_hi);
               if (t + 1 < w.ntiles) fetch_page_ids(table_of(kn.r), kn.tr, kn.n_r, p.max_blocks, pid);
               kw = kn;
             } else {
@@ -1079,7 +1110,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const long long kv_end = w.qpos0 - w.q_lo + w.q_hi;
     RankWalk kw{0, 0, 0, 0};
     if constexpr (walk) {
-      kw = walk_start(kv_end, p.cp, p.I);
+      kw = walk_start(kv_end, p.cp, p.I, w.r_lo, w.r_hi);
       nvis = min(kw.n_r, rank_local_len(qpos + 1, kw.r, p.cp, p.I));
     } else {
       if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
@@ -1103,7 +1134,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       } else {
         if (kw.tr == 0 && t > 0) nvis = min(kw.n_r, rank_local_len(qpos + 1, kw.r, p.cp, p.I));
         lim = nvis - 1 - kw.tr * BN;
-        walk_next(kw, kv_end, p.cp, p.I);
+        walk_next(kw, kv_end, p.cp, p.I, w.r_hi);
       }
       const float alpha = row_max_update(s0, s1, s2, s3, lim, p.scale_log2, m);
       // S(t) complete implies PV(t-1) complete (it was issued before QK(t)): O is stable and
@@ -1124,7 +1155,10 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tc_fence_after();
       const long long frow = (long long)(w.q_row0 + rofs + row) * p.Hq + hcol;
       const long long orow = ((long long)w.p * p.Nq + w.q_row0 + rofs + row) * p.Hq + hcol;
-      if (p.tma_out && w.q_lo + rofs + q4 * 32 + 32 <= w.q_hi) {
+      if (piece >= 0) {  // one rank range of a split item: its partial for the merge kernel
+        const long long wrow = ((long long)piece * 2 + tile) * BM + row;
+        write_row<D>(tO, m, l, row_valid, p.ws_out + wrow * D, p.ws_lse + wrow);
+      } else if (p.tma_out && w.q_lo + rofs + q4 * 32 + 32 <= w.q_hi) {
         // all 32 rows of this warp are real: stage them and store by TMA.  Head 0 stages in
         // the Q tiles (free: its last PV completed after the other head's last QK), head 1 in
         // the K/V ring (free: its last PV is the CTA's last MMA).
@@ -1159,6 +1193,54 @@ __global__ void __launch_bounds__(kThreads2, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// Fused pass-Q, split tail: the split_k rank-range partials of each split item (normalised rows
+// and natural-log LSEs, written by the pieces above) combined as cp_lse_merge does -- weights
+// exp(lse_k - max), a range with lse = -inf contributes nothing -- into the item's bf16 output
+// rows and LSEs.  One CTA per split item, one warp per (tile, row).  Launched as a programmatic
+// dependent of the attention kernel.
+template <int D, bool TT>
+__global__ void __launch_bounds__(256) fq_split_merge_kernel(const TcParams p) {
+  constexpr int E = D / 32;  // values per lane
+  griddep_wait();
+  const Work w = decode_work_at(p, (unsigned)p.n_whole + blockIdx.x, TT ? 1 : 2, TT ? 2 * BM : BM);
+  if (!w.valid) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int u = warp; u < 2 * BM; u += 8) {
+    const int tile = u / BM, row = u % BM;
+    const int rofs = TT ? tile * BM : 0;
+    if (w.q_lo + rofs + row >= w.q_hi) continue;
+    const int hcol = w.h + (TT ? 0 : tile);
+    float M = -INFINITY;
+    for (int k = 0; k < p.split_k; ++k) {
+      const long long wrow = (((long long)blockIdx.x * p.split_k + k) * 2 + tile) * BM + row;
+      M = fmaxf(M, p.ws_lse[wrow] * kLog2e);
+    }
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    if (M > -INFINITY) {
+      for (int k = 0; k < p.split_k; ++k) {
+        const long long wrow = (((long long)blockIdx.x * p.split_k + k) * 2 + tile) * BM + row;
+        const float lk = p.ws_lse[wrow] * kLog2e;
+        if (!(lk > -INFINITY)) continue;  // an empty range's rows were never written
+        const float wk = exp2f(lk - M);
+        wsum += wk;
+        const float* src = p.ws_out + wrow * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += wk * src[e];
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const long long frow = (long long)(w.q_row0 + rofs + row) * p.Hq + hcol;
+    __nv_bfloat16* dst = p.out_final + frow * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2)
+      *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    if (lane == 0) p.lse_final[frow] = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
   }
 }
 
@@ -1212,9 +1294,75 @@ bool make_out_map(CUtensorMap* m, void* base, bool bf16, unsigned long long D, u
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Fused pass-Q work items cost about the same (every row sees its ranks' whole cached context),
+// so a grid of n items on S SMs (one CTA each) takes ceil(n / S) item times.  When the last wave
+// is partly empty, its rem = n mod S items are each cut into k rank ranges (k <= cp; ranks hold
+// equal shares, so a piece of at most ceil(cp / k) ranks costs that many cp-ths of an item) whose
+// partials fq_split_merge_kernel combines: the tail then takes ceil(rem k / S) ceil(cp / k) / cp
+// item times.  The smallest k with the shortest tail is taken, and only when it saves at least a
+// quarter of an item (each piece repeats an item's prologue and epilogue).
+struct SplitPlan {
+  long long n_split;  // items run as pieces (the last n_split items of the grid)
+  int k;              // pieces per split item; 1 = no split
+};
+SplitPlan split_plan(long long items, int cp, int sms) {
+  SplitPlan sp{0, 1};
+  if (sms <= 0 || cp < 2 || items <= 0) return sp;
+  const long long rem = items % sms;
+  if (rem == 0) return sp;
+  double best = 1.0;
+  int bk = 1;
+  for (int k = 2; k <= cp; ++k) {
+    const double t = (double)((rem * k + sms - 1) / sms) * ((cp + k - 1) / k) / cp;
+    if (t < best - 1e-9) {
+      best = t;
+      bk = k;
+    }
+  }
+  if (best > 0.75) return sp;
+  sp.n_split = rem;
+  sp.k = bk;
+  return sp;
+}
+
+// Kernel shape of a prefill launch: two-tile kernel or not, its tiles mode, and the items.
+struct Shape {
+  bool pair, tiles;
+  int TPC;
+  long long items;
+};
+Shape shape_of(const cp_prefill_args& a, bool fused) {
+  Shape sh;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  // the two-tile kernel unless one head per CTA is forced: two heads of a kv group when they
+  // pair up (even G), else two consecutive row tiles of one head (`tiles`)
+  sh.pair = a.impl != CP_IMPL_TCGEN05_SINGLE;
+  sh.tiles = sh.pair && (G % 2 != 0);
+  const int chunk_max = (a.max_seqlen_q + 2 * a.cp - 1) / (2 * a.cp);
+  const int span = sh.tiles ? 2 * BM : BM;  // query rows per work item
+  sh.TPC = (chunk_max + span - 1) / span;
+  sh.items = (long long)2 * a.cp * sh.TPC * a.num_seqs * ((a.kv_shard >= 0 || fused) ? 1 : a.cp) *
+             (a.num_q_heads / (sh.pair && !sh.tiles ? 2 : 1));
+  return sh;
+}
+
+// Split plan of a fused pass-Q launch on the current device (no split for anything else).
+SplitPlan fused_split_plan(const cp_prefill_args& a) {
+  const Shape sh = shape_of(a, true);
+  if (a.mode != CP_PASS_Q || !sh.pair) return SplitPlan{0, 1};
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SplitPlan{0, 1};
+  return split_plan(sh.items, a.cp, sms);
+}
+size_t split_bytes(const SplitPlan& sp, int D) {
+  return sp.k > 1 ? (size_t)sp.n_split * sp.k * 2 * BM * (D + 1) * sizeof(float) : 0;
+}
+
 template <int D>
 cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* fused_out,
-                   float* fused_lse) {
+                   float* fused_lse, void* ws = nullptr, size_t ws_bytes = 0) {
   CUtensorMap mq, mk, mv;
   const unsigned long long Nq = (unsigned long long)a.total_q;
   if (!make_map(&mq, a.q, (unsigned long long)a.num_q_heads * D, Nq,
@@ -1227,11 +1375,8 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
     if (!make_map(&mk, a.k, hd, Nkv, hd, BN) || !make_map(&mv, a.v, hd, Nkv, hd, BN))
       return cudaErrorInvalidValue;
   }
-  // the two-tile kernel unless one head per CTA is forced: two heads of a kv group when they
-  // pair up (even G), else two consecutive row tiles of one head (`tiles`)
-  const int G = a.num_q_heads / a.num_kv_heads;
-  const bool pair = a.impl != CP_IMPL_TCGEN05_SINGLE;
-  const bool tiles = pair && (G % 2 != 0);
+  const Shape sh = shape_of(a, fused_out != nullptr);
+  const bool pair = sh.pair, tiles = sh.tiles;
   int page_kv = 0;
   if (a.mode != CP_PASS_KV) {
     const unsigned long long rows = (unsigned long long)a.cp * a.pool_pages * a.num_kv_heads * 16;
@@ -1258,9 +1403,7 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   p.kv_shard = a.kv_shard;
   p.debug = a.debug;
   p.budget = (a.debug & 1) ? (1ll << 21) : kBudget;
-  const int chunk_max = (a.max_seqlen_q + 2 * a.cp - 1) / (2 * a.cp);
-  const int span = tiles ? 2 * BM : BM;  // query rows per work item
-  p.TPC = (chunk_max + span - 1) / span;
+  p.TPC = sh.TPC;
   p.Nq = a.total_q;
   p.pool = a.pool_pages;
   p.scale_log2 = scale * kLog2e;
@@ -1278,10 +1421,24 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   std::memset(&mo, 0, sizeof(mo));
   p.tma_out = p.fused ? make_out_map(&mo, fused_out, true, D, a.num_q_heads, Nq)
                       : make_out_map(&mo, a.out, false, D, a.num_q_heads, (unsigned long long)a.cp * Nq);
-  const long long grid = (long long)2 * a.cp * p.TPC * a.num_seqs *
-                         ((a.kv_shard >= 0 || p.fused) ? 1 : a.cp) *
-                         (a.num_q_heads / (pair && !tiles ? 2 : 1));
+  long long grid = sh.items;
   if (grid == 0) return cudaSuccess;
+  p.n_whole = (int)(grid < (1ll << 31) ? grid : 0);
+  p.split_k = 1;
+  p.ws_out = p.ws_lse = nullptr;
+  SplitPlan sp{0, 1};
+  if (p.fused && a.mode == CP_PASS_Q && pair && ws != nullptr) {
+    sp = fused_split_plan(a);
+    if (sp.k > 1 && ws_bytes >= split_bytes(sp, D) && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0) {
+      p.n_whole = (int)(grid - sp.n_split);
+      p.split_k = sp.k;
+      p.ws_out = static_cast<float*>(ws);
+      p.ws_lse = p.ws_out + (size_t)sp.n_split * sp.k * 2 * BM * D;
+      grid = p.n_whole + sp.n_split * sp.k;
+    } else {
+      sp = SplitPlan{0, 1};
+    }
+  }
   if (grid >= (1ll << 31)) return cudaErrorInvalidConfiguration;
   cudaError_t e;
   if (pair) {
@@ -1308,6 +1465,25 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)grid, kThreads2, smem, s>>>(mq, mk, mv, mo, p);
+    if (sp.k > 1) {
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      // the pieces' partials -> the split items' output rows, scheduled while the attention
+      // kernel's last CTAs finish
+      cudaLaunchConfig_t cfg;
+      std::memset(&cfg, 0, sizeof(cfg));
+      cfg.gridDim = dim3((unsigned)sp.n_split);
+      cfg.blockDim = dim3(256);
+      cfg.stream = s;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      at[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      e = tiles ? cudaLaunchKernelEx(&cfg, fq_split_merge_kernel<D, true>, p)
+                : cudaLaunchKernelEx(&cfg, fq_split_merge_kernel<D, false>, p);
+      if (e != cudaSuccess) return e;
+    }
   } else {
     const int smem = Layout<D>::kAlloc;
     e = cudaFuncSetAttribute(prefill_tc1_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1365,7 +1541,11 @@ cudaError_t cp_launch_prefill_tc(const cp_prefill_args& a, float scale, cudaStre
 }
 
 cudaError_t cp_launch_prefill_fused(const cp_prefill_args& a, float scale, void* out, float* lse,
-                                    cudaStream_t s) {
-  return a.head_dim == 64 ? cpattn::launch<64>(a, scale, s, out, lse)
-                          : cpattn::launch<128>(a, scale, s, out, lse);
+                                    void* ws, size_t ws_bytes, cudaStream_t s) {
+  return a.head_dim == 64 ? cpattn::launch<64>(a, scale, s, out, lse, ws, ws_bytes)
+                          : cpattn::launch<128>(a, scale, s, out, lse, ws, ws_bytes);
+}
+
+size_t cp_prefill_fused_split_bytes(const cp_prefill_args& a) {
+  return cpattn::split_bytes(cpattn::fused_split_plan(a), a.head_dim);
 }

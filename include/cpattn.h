@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define CPATTN_ABI_VERSION 2
+#define CPATTN_ABI_VERSION 3
 
 typedef enum {
   CP_OK = 0,
@@ -258,9 +258,19 @@ cp_status cp_partial_attn_prefill(const cp_prefill_args* args, void* stream);
  *   out      device bf16 [Nq][Hq][d]: exact causal attention (round to nearest even)
  *   out_lse  device f32 [Nq][Hq] natural-log LSE (NULL not allowed).
  * Equals cp_lse_merge applied to cp_partial_attn_prefill's partials, up to rounding.
+ *
+ * Tail split (CP_PASS_Q): its work items cost about the same, so when the grid's last wave
+ * would leave SMs idle, the items of that wave are each cut into k rank ranges (rank
+ * subsets of the walk) whose normalised partials and LSEs go to `workspace`; a second,
+ * small kernel merges them as cp_lse_merge does.  cp_prefill_fused_workspace_size gives the
+ * bytes this takes for the shapes in args on the current device (0: no split planned).
+ * workspace: device scratch, 256-byte aligned, of at least that size; NULL, or a smaller
+ * size, runs every item whole (same results up to rounding).  No initialisation is needed;
+ * calls that use the same workspace must not overlap on the GPU.  CP_PASS_KV never splits.
  * ---------------------------------------------------------------------------- */
-cp_status cp_attn_prefill_fused(const cp_prefill_args* args, void* out, float* out_lse,
-                                void* stream);
+cp_status cp_prefill_fused_workspace_size(const cp_prefill_args* args, size_t* bytes);
+cp_status cp_attn_prefill_fused(const cp_prefill_args* args, void* workspace,
+                                size_t workspace_bytes, void* out, float* out_lse, void* stream);
 
 /* ------------------------------------------------------------------------------
  * cp_partial_attn_decode -- per-rank partial attention of one new query token per

@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_struct_mirrors_match(lib):
     assert lib.cp_prefill_args_size() == ctypes.sizeof(cpa.PrefillArgs)
     assert lib.cp_decode_args_size() == ctypes.sizeof(cpa.DecodeArgs)
-    assert lib.cp_abi_version() == 2
+    assert lib.cp_abi_version() == 3
     assert lib.cp_status_string(5) == b"CP_ERR_DEVICE_BOUNDS"
 
 
@@ -81,27 +81,50 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
 
 def test_fused_prefill_arguments_are_checked_on_the_host(lib):
     """cp_attn_prefill_fused: the pass-Q form needs the paged-cache arguments and the two-tile
-    kernel; bad modes and f32 inputs are refused before any launch."""
+    kernel; bad modes, f32 inputs and a misaligned workspace are refused before any launch."""
     fake = ctypes.c_void_p(256)
+
+    def fused(f, out_lse=fake, ws=None, ws_bytes=0):
+        return lib.cp_attn_prefill_fused(ctypes.byref(f), ws, ws_bytes, fake, out_lse, None)
+
     f = cpa.PrefillArgs()
     f.mode, f.dtype, f.num_seqs, f.num_q_heads, f.num_kv_heads, f.head_dim, f.cp = 1, 1, 1, 8, 2, 128, 2
     f.total_q, f.max_seqlen_q, f.q_shard, f.kv_shard = 10, 10, -1, -1
     f.cu_seqlens_q, f.q, f.k_cache, f.v_cache = 256, 256, 256, 256
     f.impl = cpa.CP_IMPL_TCGEN05_SINGLE
-    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 2
+    assert fused(f) == 2
     assert "two-tile" in _last(lib)[1]
     f.impl = cpa.CP_IMPL_AUTO
-    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 1   # no block tables
+    assert fused(f) == 1   # no block tables
     assert "block_tables" in _last(lib)[1]
     f.block_tables, f.seq_lens_kv, f.max_blocks, f.pool_pages, f.interleave = 256, 256, 4, 8, 8
     f.block_size = 32
-    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 2   # block size 32
+    assert fused(f) == 2   # block size 32
     f.block_size = 16
-    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, None, None) == 1   # no out_lse
+    assert fused(f, out_lse=None) == 1   # no out_lse
+    assert fused(f, ws=ctypes.c_void_p(256 + 16), ws_bytes=1 << 20) == 1   # misaligned workspace
+    assert "workspace" in _last(lib)[1]
     f.mode = 7
-    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 1
+    assert fused(f) == 1
     f.mode, f.dtype = 0, 0
-    assert lib.cp_attn_prefill_fused(ctypes.byref(f), fake, fake, None) == 2   # f32 inputs
+    assert fused(f) == 2   # f32 inputs
+
+
+def test_fused_prefill_workspace_size_on_the_host(lib):
+    """cp_prefill_fused_workspace_size: shape checks, and no split (0 bytes) for pass-KV."""
+    n = ctypes.c_size_t(123)
+    f = cpa.PrefillArgs()
+    f.mode, f.dtype, f.num_seqs, f.num_q_heads, f.num_kv_heads, f.head_dim, f.cp = 0, 1, 4, 16, 2, 128, 4
+    f.total_q, f.max_seqlen_q, f.q_shard, f.kv_shard = 8192, 2048, -1, -1
+    assert lib.cp_prefill_fused_workspace_size(ctypes.byref(f), ctypes.byref(n)) == 0
+    assert n.value == 0
+    assert lib.cp_prefill_fused_workspace_size(ctypes.byref(f), None) == 1
+    f.head_dim = 96
+    assert lib.cp_prefill_fused_workspace_size(ctypes.byref(f), ctypes.byref(n)) == 2
+    f.head_dim, f.cp = 128, 0
+    assert lib.cp_prefill_fused_workspace_size(ctypes.byref(f), ctypes.byref(n)) == 1
+    f.cp, f.kv_shard = 4, 1
+    assert lib.cp_prefill_fused_workspace_size(ctypes.byref(f), ctypes.byref(n)) == 1
 
 
 def test_cached_context_arguments_are_checked_on_the_host(lib):

@@ -142,9 +142,15 @@ def test_pass_q_path_in_a_cuda_graph(lib, fused):
               block_tables=dev["block_tables"], seq_lens_kv=dev["seq_lens"], interleave=I,
               max_seqlen_q=q_len)
 
+    # 32 equal items on 152 SMs: the fused launch splits them by rank range (+ a merge kernel)
+    ws = torch.empty(lib.cp_prefill_fused_workspace_size(B, Hq, Hkv, d, cp, q_len),
+                     dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+
     def step():
         if fused:
-            lib.cp_attn_prefill_fused(dev["q"], dev["cu_seqlens_q"], cp, out=out, out_lse=lse, **kw)
+            lib.cp_attn_prefill_fused(dev["q"], dev["cu_seqlens_q"], cp, out=out, out_lse=lse,
+                                      workspace=ws, **kw)
         else:
             lib.cp_partial_attn_prefill(dev["q"], dev["cu_seqlens_q"], cp, out=part, lse=plse, **kw)
             lib.cp_lse_merge(part, plse, out=out, out_lse=lse)

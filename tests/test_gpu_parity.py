@@ -250,6 +250,8 @@ PASS_Q_CASES = [
     ([50], [2000], 8, 8, 128, torch.float32, 2, 16),
     ([200], [1500], 8, 2, 128, torch.bfloat16, 1, 8),
     ([512, 512], [4096, 3000], 16, 2, 128, torch.bfloat16, 4, 8),   # ~512 work items
+    # fused: 192 items, so more than one wave on 152 SMs with a split tail
+    ([1024, 1024, 1024], [4096, 3500, 1100], 16, 2, 128, torch.bfloat16, 4, 8),
 ]
 
 
@@ -317,21 +319,27 @@ def test_pass_q_reports_short_kv(lib, impl):
     assert int(err.item()) == 5
 
 
-@pytest.mark.parametrize("case", [0, 1, 2, 4, 5])
-def test_fused_pass_q_parity(lib, case):
+@pytest.mark.parametrize("split", [True, False])
+@pytest.mark.parametrize("case", [0, 1, 2, 4, 5, 6])
+def test_fused_pass_q_parity(lib, case, split):
     """cp_attn_prefill_fused over the paged round-robin cache (every rank's resident pages in
-    one online softmax) = merged pass-Q partials of the oracle."""
+    one online softmax) = merged pass-Q partials of the oracle; with the tail wave split into
+    rank ranges (a workspace) and with every item whole (none)."""
     q_lens, kv_lens, Hq, Hkv, d, dt, cp, I = PASS_Q_CASES[case]
     x = _paged_case(len(q_lens), q_lens, kv_lens, Hq, Hkv, d, dt, cp, I, 300 + case)
+    need = lib.cp_prefill_fused_workspace_size(len(q_lens), Hq, Hkv, d, cp, max(q_lens))
+    if cp > 1 and case != 5:   # these grids leave most of their last wave's SMs idle
+        assert need > 0
+    ws = torch.empty(need if split else 0, dtype=torch.uint8, device=DEV)
     out, lse = lib.cp_attn_prefill_fused(
         x["q"].to(DEV), x["cu_seqlens_q"].to(DEV), cp, mode=lib.CP_PASS_Q,
         k_cache=x["k_cache"].to(DEV), v_cache=x["v_cache"].to(DEV),
         block_tables=x["block_tables"].to(DEV), seq_lens_kv=x["seq_lens"].to(DEV), interleave=I,
-        max_seqlen_q=max(q_lens))
+        max_seqlen_q=max(q_lens), workspace=ws)
     O, L = orc.pass_q_partials(x["q"], x["k_cache"], x["v_cache"], x["block_tables"],
                                x["cu_seqlens_q"], x["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
     Om, Lm = orc.lse_merge(O, L)
-    check_merged(out, lse, Om, Lm, what="fused pass-Q")
+    check_merged(out, lse, Om, Lm, what=f"fused pass-Q split={split}")
 
 
 # ------------------------------------------------------------------------------------ decode
