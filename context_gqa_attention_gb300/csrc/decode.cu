@@ -71,8 +71,19 @@ CP_DEV uint4 ldg_stream(const void* p) {
 // CTA's partial (cumulatively, through the barrier) and its acquire side lets the last CTA see
 // every earlier CTA's partial; a second barrier passes that on to the last CTA's threads, which
 // then read the partials through L2.  No CTA waits on another, so nothing can stall.
+// Only the (rank, split) CTAs that hold tokens of the sequence (split * ST < the rank's share)
+// count in and write a partial: an empty split returns at once, and the merge gives the
+// partials it did not write weight 0.
+CP_DEV bool split_live(const DecodeParams& p, int L, int part) {
+  return (part % p.S) * (long long)p.ST < rank_local_len(L, part / p.S, p.cp, p.I);
+}
+CP_DEV int live_partials(const DecodeParams& p, int L) {
+  int c = 0;
+  for (int r = 0; r < p.cp; ++r) c += min(p.S, (rank_local_len(L, r, p.cp, p.I) + p.ST - 1) / p.ST);
+  return c;
+}
 template <typename T, int D, int G>
-CP_DEV void fused_tail(const DecodeParams& p, int b, int g) {
+CP_DEV void fused_tail(const DecodeParams& p, int b, int g, int L) {
   __shared__ int s_last;
   __shared__ float s_w[kMaxFusedPartials * G];  // per (partial, head): log2 LSE, then weight
   __shared__ float s_M[G], s_L[G];
@@ -84,14 +95,15 @@ CP_DEV void fused_tail(const DecodeParams& p, int b, int g) {
                  : "=r"(prev)
                  : "l"(p.counters + (long long)b * p.Hkv + g)
                  : "memory");
-    s_last = (prev == P - 1);
+    s_last = (prev == live_partials(p, L) - 1);
   }
   __syncthreads();
   if (!s_last) return;
   const long long stride = (long long)p.B * p.Hq;           // between partials
   const long long unit0 = (long long)b * p.Hq + (long long)g * G;
   for (int i = threadIdx.x; i < P * G; i += blockDim.x)
-    s_w[i] = __ldcg(p.lse + (i / G) * stride + unit0 + i % G) * kLog2e;
+    s_w[i] = split_live(p, L, i / G) ? __ldcg(p.lse + (i / G) * stride + unit0 + i % G) * kLog2e
+                                     : -INFINITY;
   __syncthreads();
   if (threadIdx.x < G) {
     float M = -INFINITY;
@@ -143,6 +155,22 @@ CP_DEV void fused_tail(const DecodeParams& p, int b, int g) {
   if (threadIdx.x == 0) p.counters[(long long)b * p.Hkv + g] = 0;
 }
 
+// Fused decode, a CTA with no token of its sequence: it writes nothing and does not count in.
+// Only a sequence without any token (seq_lens <= 0, outside the contract) has its first CTA
+// write the exact result of no keys: zero output, LSE -inf.
+template <typename T, int D, int G>
+CP_DEV void fused_empty(const DecodeParams& p, int b, int g, int r, int split) {
+  if (r != 0 || split != 0) return;
+  const long long unit0 = (long long)b * p.Hq + (long long)g * G;
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    if constexpr (sizeof(T) == 2)
+      static_cast<__nv_bfloat16*>(p.final_out)[unit0 * D + i] = __float2bfloat16_rn(0.f);
+    else
+      static_cast<float*>(p.final_out)[unit0 * D + i] = 0.f;
+  }
+  if (threadIdx.x < G && p.final_lse) p.final_lse[unit0 + threadIdx.x] = -INFINITY;
+}
+
 template <typename T, int D, int G, bool FUSED>
 __global__ void __launch_bounds__(kWarps * 32, 4) decode_kernel(const DecodeParams p) {
   constexpr int EPV = Vec<T>::N;          // elements per 16-byte vector
@@ -170,8 +198,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_kernel(const DecodePara
   const long long obase = ((long long)part * p.B + b) * p.Hq + (long long)g * G;
 
   if (l0 >= l1) {  // nothing of this rank falls in this split
-    if (threadIdx.x < G) p.lse[obase + threadIdx.x] = -INFINITY;
-    if constexpr (FUSED) fused_tail<T, D, G>(p, b, g);
+    if constexpr (FUSED) fused_empty<T, D, G>(p, b, g, r, split);
+    else if (threadIdx.x < G) p.lse[obase + threadIdx.x] = -INFINITY;
     return;
   }
 
@@ -330,23 +358,28 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_kernel(const DecodePara
       p.lse[obase + hh] = -INFINITY;
     }
   }
-  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g);
+  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g, L);
 
 }
 
 // ------------------------------------------------------------------------------ tensor-core decode
 // bf16 decode with the kv bytes moved by TMA and the arithmetic on tensor cores.  Per CTA:
-// 4 consumer warps and 1 producer warp, two CTAs per SM.  The producer streams every page's K and V rows of one
-// kv head (16 tokens x d, two 2D TMA boxes of 64 columns each, 128-byte swizzle) into a
-// 3-stage ring per consumer warp.  A consumer computes, for its page,
+// 4 consumer warps and 1 producer warp, three CTAs per SM.  The producer streams every page's K
+// and V rows of one kv head (16 tokens x d, one whole-page box each, or two 2D boxes of 64
+// columns; 128-byte swizzle) into a 2-stage ring per consumer warp.  A consumer computes, for
+// its page,
 //   S = Q K^T   with mma.sync m16n8k16: A = the G query heads (rows >= G are zero) kept in
 //               registers for the whole CTA, B = K from shared memory via ldmatrix;
 //   P           online softmax per head, in the fragment the MMA left it in (a row = a head,
 //               so the 16 tokens of a head live in the 4 lanes of a quad: two shuffles);
 //   O += P V    A = P (that same fragment, rounded to bf16), B = V via ldmatrix.trans.
 // The swizzled layout makes every ldmatrix phase touch 8 distinct bank groups.
-constexpr int kCW = 4;  // consumer warps (two CTAs share an SM)
-constexpr int kST = 3;  // ring stages per consumer warp
+// Three CTAs of 2-stage rings per SM keep as many bytes in flight as two of 3-stage rings, and
+// one CTA's end (its partial's writes, the fused form's release and merge) then idles a third
+// of the SM's streams instead of half: measured 6.60 -> 6.68 TB/s (partials), 6.35 -> 6.64
+// (fused) on the 64-sequence decode.  It caps a thread at 128 registers (a few spilled words).
+constexpr int kCW = 4;  // consumer warps
+constexpr int kST = 2;  // ring stages per consumer warp
 constexpr long long kDecodeBudget = 4000000000ll;  // SM cycles per wait (~2 s)
 
 template <int D>
@@ -390,7 +423,7 @@ CP_DEV uint32_t page_addr(uint32_t base, int t, int d) {
 }
 
 template <int D, int G, bool FUSED>
-__global__ void __launch_bounds__((kCW + 1) * 32, 2)
+__global__ void __launch_bounds__((kCW + 1) * 32, 3)
     decode_mma_kernel(const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v, const DecodeParams p) {
   using T = __nv_bfloat16;
@@ -421,9 +454,9 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
   const int l1 = min(n, l0 + p.ST);
   const int part = r * p.S + split;
   const long long obase = ((long long)part * p.B + b) * p.Hq + (long long)g * G;
-  if (l0 >= l1) {
-    if (threadIdx.x < G) p.lse[obase + threadIdx.x] = -INFINITY;
-    if constexpr (FUSED) fused_tail<T, D, G>(p, b, g);
+  if (l0 >= l1) {  // nothing of this rank falls in this split
+    if constexpr (FUSED) fused_empty<T, D, G>(p, b, g, r, split);
+    else if (threadIdx.x < G) p.lse[obase + threadIdx.x] = -INFINITY;
     return;
   }
   if (threadIdx.x == 0) {
@@ -673,7 +706,7 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2)
       p.lse[obase + hh] = -INFINITY;
     }
   }
-  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g);
+  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g, L);
 }
 
 template <int D, bool F>
