@@ -39,18 +39,34 @@ import torch  # noqa: E402
 import workloads as wl  # noqa: E402
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a dominant kernel,
-# each from one ncu capture of the named kernel at the recorded source SHA-1.  A figure is
-# reported only while that source file still has this SHA-1; otherwise traffic is null.
+# each from one ncu capture (one pass, a warm launch: "-k regex:<kernel> -s 2 -c 1" on the bench
+# command of that form, 3 warm-up steps) at the recorded source SHA-1.  A figure is reported only
+# while that source file still has this SHA-1; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # prefill_tc2_kernel<128,0,0,0>, 12-warp build, full prefill: dram read 42.11 MB + write 59.34 MB
+    # prefill_tc2_kernel<128,0,0,0>, pass-KV partials: dram read 42.03 MB + write 59.49 MB
     ("prefill", "full"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                          "sha1": "14702212c0b8a58968b6a97d2d69140f334579b9", "bytes": 101450000},
-    # the same kernel on the long prefill: dram read 1.43 GB + write 1.75 GB
+                         "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 101520384},
+    # the same kernel, fused pass-KV: read 42.03 MB + write 1.18 MB (the bf16 output is still in L2)
+    ("prefill_fused", "full"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
+                               "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 43211520},
+    # long prefill partials: read 374.6 MB + write 1711.4 MB
     ("prefill", "long"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                          "sha1": "14702212c0b8a58968b6a97d2d69140f334579b9", "bytes": 3180000000},
-    # decode_mma_kernel<128,4,0>, 64-sequence decode: dram read 4.40 GB + write 8.38 MB
+                         "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 2086081280},
+    # long prefill fused: read 345.7 MB + write 234.4 MB
+    ("prefill_fused", "long"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
+                               "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 580104704},
+    # prefill_tc2_kernel<128,1,0,0>, pass-Q partials: read 172.2 MB + write 223.3 MB
+    ("pass_q", "chunked"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
+                           "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 395576064},
+    # prefill_tc2_kernel<128,1,0,1>, fused pass-Q (split tail): read 225.5 MB + write 25.5 MB
+    ("pass_q_fused", "chunked"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
+                                 "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 251002624},
+    # decode_mma_kernel<128,4,0>, 64-sequence decode: read 4.402 GB + write 23.5 MB
     ("decode", "decode"): {"file": "context_gqa_attention_gb300/csrc/decode.cu",
-                           "sha1": "6ac2ef88b7a62cb153e08f4e82625259b1afe4f6", "bytes": 4408380000},
+                          "sha1": "b5c01eaf5355f8808871d81349446501c2511cb0", "bytes": 4425172736},
+    # decode_mma_kernel<128,4,1> (fused merge): read 4.403 GB + write 18.1 MB
+    ("decode_fused", "decode"): {"file": "context_gqa_attention_gb300/csrc/decode.cu",
+                                "sha1": "b5c01eaf5355f8808871d81349446501c2511cb0", "bytes": 4420925696},
 }
 
 FALLBACK_HBM_GBS = 6800.0
