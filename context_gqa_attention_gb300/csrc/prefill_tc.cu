@@ -43,8 +43,36 @@ constexpr int kThreads = 192;
 constexpr long long kBudget = 4000000000ll;  // SM cycles per wait (~2 s)
 constexpr float kRescaleThreshold = 8.f;     // log2 units
 
+// Division of a numerator below 2^31 by a divisor fixed for the launch as one multiply and one
+// shift (Granlund and Montgomery, "Division by invariant integers using multiplication", 1994,
+// with 31-bit numerators): l = ceil(log2 d), m = ceil(2^(31+l) / d) < 2^32, then
+// n / d = (n m) >> (31 + l).  The work-item decode at a CTA's start runs a chain of such
+// divisions before its first load can be addressed.
+struct FastDiv {
+  uint32_t d, m, s;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  const unsigned long long num = 1ull << (31 + l);
+  return FastDiv{d, (uint32_t)((num + d - 1) / d), 31 + l};
+}
+CP_DEV uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  return (uint32_t)(((unsigned long long)n * f.m) >> f.s);
+}
+// n / f.d, by the multiply and shift (FAST) or by plain integer division: the fused pass-Q
+// kernel keeps the plain division, measured faster there (with the constants its spills grew).
+template <bool FAST>
+CP_DEV uint32_t udiv(uint32_t n, const FastDiv& f) {
+  if constexpr (FAST) return fdiv(n, f);
+  else return n / f.d;
+}
+
 struct TcParams {
   int mode, B, Hq, Hkv, cp, I, max_blocks, q_shard, kv_shard, TPC, Nq, debug;
+  // divisors of the work-item decode: item groups of heads, q slots (2 cp TPC), cp, TPC, 2 cp
+  // (chunk bounds), G (q heads per kv head)
+  FastDiv f_groups, f_nslot, f_cp, f_tpc, f_2cp, f_G;
   long long pool, budget;
   float scale_log2;
   const int32_t* cu_q;
@@ -166,29 +194,43 @@ CP_DEV void walk_next(RankWalk& k, long long kv_end, int cp, int I, int r_end) {
 // Slots run heaviest first (last chunk, last tile) so long items start early.
 // `span` query rows per item: BM (one tile; head pairs) or 2 BM (two tiles of one head).
 // Fused pass-Q items walk ranks [r_lo, r_hi) (all of them unless the item is split).
+// Chunk bound floor(k T / 2cp) (as chunk_bound) with the launch's divisor constants.
+template <bool FAST>
+CP_DEV int chunk_bound_f(int k, int T, const TcParams& p) {
+  if constexpr (FAST) {
+    const unsigned long long num = (unsigned long long)k * (unsigned)T;
+    if (num < 0x80000000ull) return (int)fdiv((uint32_t)num, p.f_2cp);
+  }
+  return chunk_bound(k, T, p.cp);
+}
+
+template <bool FAST = true>
 CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = BM, int r_lo = 0,
                            int r_hi = 1 << 30) {
   Work w;
   w.valid = 0;
   w.r_lo = r_lo;
   w.r_hi = min(r_hi, p.cp);
-  // 32-bit divisions: the item space is below 2^31
+  // the item space is below 2^31; p.f_groups divides by Hq / hpc
   const unsigned groups = (unsigned)(p.Hq / hpc);
   const unsigned nslot = 2u * (unsigned)p.cp * (unsigned)p.TPC;
-  w.h = (int)(lin % groups) * hpc;
-  lin /= groups;
+  unsigned q = udiv<FAST>(lin, p.f_groups);
+  w.h = (int)(lin - q * groups) * hpc;
+  lin = q;
   int slot;
   if (p.mode == CP_PASS_Q) {
     // pass-Q items cost about the same (every query sees its rank's whole cached context), so
     // they run sequence by sequence and rank by rank: the CTAs resident at one time read the
     // pages of one or two (sequence, rank) pairs, which stay in L2
-    slot = (int)(lin % nslot);
-    lin /= nslot;
+    q = udiv<FAST>(lin, p.f_nslot);
+    slot = (int)(lin - q * nslot);
+    lin = q;
     if (p.kv_shard >= 0 || p.fused) {
       w.p = p.fused ? 0 : p.kv_shard;
     } else {
-      w.p = (int)(lin % (unsigned)p.cp);
-      lin /= (unsigned)p.cp;
+      q = udiv<FAST>(lin, p.f_cp);
+      w.p = (int)(lin - q * (unsigned)p.cp);
+      lin = q;
     }
     w.b = (int)lin;
   } else {
@@ -197,24 +239,27 @@ CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = 
     if (p.kv_shard >= 0 || p.fused) {
       w.p = p.fused ? 0 : p.kv_shard;
     } else {
-      w.p = (int)(lin % (unsigned)p.cp);
-      lin /= (unsigned)p.cp;
+      q = udiv<FAST>(lin, p.f_cp);
+      w.p = (int)(lin - q * (unsigned)p.cp);
+      lin = q;
     }
-    slot = (int)(lin % nslot);
-    w.b = (int)(lin / nslot);
+    q = udiv<FAST>(lin, p.f_nslot);
+    slot = (int)(lin - q * nslot);
+    w.b = (int)q;
   }
-  const int c = 2 * p.cp - 1 - slot / p.TPC;
-  const int j = p.TPC - 1 - slot % p.TPC;
+  const unsigned sq = udiv<FAST>((unsigned)slot, p.f_tpc);
+  const int c = 2 * p.cp - 1 - (int)sq;
+  const int j = p.TPC - 1 - (slot - (int)sq * p.TPC);
   const int q0 = p.cu_q[w.b];
   const int Tq = p.cu_q[w.b + 1] - q0;
   if (Tq <= 0) return w;
-  const int cs = chunk_bound(c, Tq, p.cp), ce = chunk_bound(c + 1, Tq, p.cp);
+  const int cs = chunk_bound_f<FAST>(c, Tq, p), ce = chunk_bound_f<FAST>(c + 1, Tq, p);
   w.q_lo = cs + j * span;
   if (w.q_lo >= ce) return w;
   w.q_hi = min(w.q_lo + span, ce);
   if (p.q_shard >= 0 && shard_of_chunk(c, p.cp) != p.q_shard) return w;
   w.valid = 1;
-  w.g = w.h / (p.Hq / p.Hkv);
+  w.g = (int)udiv<FAST>((unsigned)w.h, p.f_G);
   w.q_row0 = q0 + w.q_lo;
   w.ntiles = 0;
   if (p.mode == CP_PASS_KV) {
@@ -242,8 +287,8 @@ CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = 
 #pragma unroll
       for (int i = 0; i < 2; ++i) {  // kv chunks s and 2cp-1-s, positions < C + q_hi
         const int ch = i == 0 ? w.p : 2 * p.cp - 1 - w.p;
-        w.ks[i] = chunk_bound(ch, Tkv, p.cp);
-        w.ke[i] = min(chunk_bound(ch + 1, Tkv, p.cp), C + w.q_hi);
+        w.ks[i] = chunk_bound_f<FAST>(ch, Tkv, p);
+        w.ke[i] = min(chunk_bound_f<FAST>(ch + 1, Tkv, p), C + w.q_hi);
         if (w.ke[i] < w.ks[i]) w.ke[i] = w.ks[i];
         w.nt[i] = (w.ke[i] - w.ks[i] + BN - 1) / BN;
         w.ntiles += w.nt[i];
@@ -272,6 +317,7 @@ CP_DEV Work decode_work(const TcParams& p, int hpc, int span = BM) {
   return decode_work_at(p, blockIdx.x, hpc, span);
 }
 // Fused pass-Q: this CTA's item, or (piece >= 0) one rank range of a split item.
+template <bool FAST>
 CP_DEV Work decode_split_work(const TcParams& p, int hpc, int span, int& piece) {
   unsigned lin = blockIdx.x;
   int r_lo = 0, r_hi = p.cp;
@@ -283,7 +329,7 @@ CP_DEV Work decode_split_work(const TcParams& p, int hpc, int span, int& piece) 
     r_lo = part * p.cp / p.split_k;
     r_hi = (part + 1) * p.cp / p.split_k;
   }
-  return decode_work_at(p, lin, hpc, span, r_lo, r_hi);
+  return decode_work_at<FAST>(p, lin, hpc, span, r_lo, r_hi);
 }
 
 CP_DEV uint32_t pack_bf16(float lo, float hi) {
@@ -867,7 +913,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int piece = -1;  // fused pass-Q: >= 0 when this CTA runs one rank range of a split item
-  const Work w = FQ ? decode_split_work(p, TT ? 1 : 2, TT ? 2 * BM : BM, piece)
+  const Work w = FQ ? decode_split_work<false>(p, TT ? 1 : 2, TT ? 2 * BM : BM, piece)
                     : (TT ? decode_work(p, 1, 2 * BM) : decode_work(p, 2));
   if (!w.valid) return;
 
@@ -1205,7 +1251,7 @@ template <int D, bool TT>
 __global__ void __launch_bounds__(256) fq_split_merge_kernel(const TcParams p) {
   constexpr int E = D / 32;  // values per lane
   griddep_wait();
-  const Work w = decode_work_at(p, (unsigned)p.n_whole + blockIdx.x, TT ? 1 : 2, TT ? 2 * BM : BM);
+  const Work w = decode_work_at<false>(p, (unsigned)p.n_whole + blockIdx.x, TT ? 1 : 2, TT ? 2 * BM : BM);
   if (!w.valid) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int u = warp; u < 2 * BM; u += 8) {
@@ -1404,6 +1450,12 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   p.debug = a.debug;
   p.budget = (a.debug & 1) ? (1ll << 21) : kBudget;
   p.TPC = sh.TPC;
+  p.f_groups = make_fastdiv((uint32_t)(a.num_q_heads / (pair && !tiles ? 2 : 1)));
+  p.f_nslot = make_fastdiv(2u * (uint32_t)a.cp * (uint32_t)(sh.TPC > 0 ? sh.TPC : 1));
+  p.f_cp = make_fastdiv((uint32_t)a.cp);
+  p.f_tpc = make_fastdiv((uint32_t)(sh.TPC > 0 ? sh.TPC : 1));
+  p.f_2cp = make_fastdiv(2u * (uint32_t)a.cp);
+  p.f_G = make_fastdiv((uint32_t)(a.num_q_heads / a.num_kv_heads));
   p.Nq = a.total_q;
   p.pool = a.pool_pages;
   p.scale_log2 = scale * kLog2e;
