@@ -1252,8 +1252,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const long long frow = (long long)(w.q_row0 + rofs + row) * p.Hq + hcol;
       const long long orow = ((long long)w.p * p.Nq + w.q_row0 + rofs + row) * p.Hq + hcol;
       if (piece >= 0) {  // one rank range of a split item: its partial for the merge kernel
-        const long long wrow = ((long long)piece * 2 + tile) * BM + row;
-        write_row<D>(tO, m, l, row_valid, p.ws_out + wrow * D, p.ws_lse + wrow);
+        // the workspace holds all 32 rows of every warp (rows past the item and rows that saw
+        // no key are written as well, and never read), so they always go out as whole rows
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const uint32_t sb = (tile == 0 ? sQ : sKV) + (uint32_t)(q4 * 32 * D * 4);
+        stage_rows_f32<D>(tO, inv_l, sb, lane);
+        __syncwarp();
+        const long long wrow0 = ((long long)piece * 2 + tile) * BM + q4 * 32;
+        store_staged_f32<D>(sb, lane, p.ws_out + wrow0 * D, D);
+        if (row_valid) p.ws_lse[wrow0 + lane] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       } else if (p.row_out && w.q_lo + rofs + q4 * 32 + 32 <= w.q_hi) {
         // all 32 rows of this warp are real: stage them in shared memory (128-byte-swizzled
         // boxes, conflict-free both ways) and read them back so that each warp-wide store
