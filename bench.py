@@ -866,68 +866,94 @@ def prefill_kernel_name(runner):
             else "cp_partial_attn_prefill (pass-KV)")
 
 
-def measure_prefill_form(runner, fused, steps, flush, dev, stream, pk):
-    """One prefill form (partials + merge, or the fused launch) of a runner: step value and the
-    dominant kernel's roofline."""
+def measure_prefill_form(runner, fused, steps, flush, dev, stream, pk, clocks=None):
+    """One prefill form (partials + merge, or the fused launch) of a runner: step value, the
+    dominant kernel's roofline and the SM clocks sampled while it ran."""
     runner.fused = fused
-    st, dm, _ = time_steps(runner, steps, 3, flush, dev, stream)
+    st, dm, win = time_steps(runner, steps, 3, flush, dev, stream)
     d_s = statistics.mean(dm) / 1e3
-    return {"value": runner.metric(statistics.mean(st) / 1e3), "unit": "TFLOP/s",
-            "ms_per_step": statistics.mean(st),
-            "roofline": roofline("tensor", prefill_kernel_name(runner), runner.flops, d_s, pk,
-                                 traffic=ncu_traffic(*traffic_key(runner)),
-                                 algorithmic=f"{runner.flops:.4e} causal FLOP per launch")}
+    e = {"value": runner.metric(statistics.mean(st) / 1e3), "unit": "TFLOP/s",
+         "ms_per_step": statistics.mean(st),
+         "roofline": roofline("tensor", prefill_kernel_name(runner), runner.flops, d_s, pk,
+                              traffic=ncu_traffic(*traffic_key(runner)),
+                              algorithmic=f"{runner.flops:.4e} causal FLOP per launch")}
+    if clocks is not None:
+        e["clocks"] = clocks.summary(*win)
+    return e
 
 
-def secondaries(args, primary, w, dev, stream, flush, pk, ws):
-    """Every other form and workload of the path, each with its dominant kernel's roofline."""
+def settle(fn, dev, seconds):
+    """Runs `fn` back to back for about `seconds`: after an idle host-side pause (the CPU oracle)
+    a burst of GPU work met power-management transients (sw_power_cap with SM clocks at
+    1.93-1.99 GHz for ~0.4 s), so each series of secondary measurements starts after a busy
+    lead-in rather than straight after the pause."""
+    t = time.time()
+    while time.time() - t < seconds:
+        for _ in range(4):
+            fn()
+        torch.cuda.synchronize(dev)
+
+
+def secondaries(args, primary, w, dev, stream, flush, pk, ws, clocks=None):
+    """Every other form and workload of the path, each with its dominant kernel's roofline and
+    the SM clocks sampled over its timed steps."""
     sec = {}
     n = max(10, args.steps // 2)
     cpa = primary.cpa
     if isinstance(primary, PrefillRunner) and w.dtype == torch.bfloat16:
+        primary.fused = True
+        settle(primary.step, dev, 1.0)
         sec[f"{w.name}_prefill_fused"] = dict(
-            measure_prefill_form(primary, True, n, flush, dev, stream, pk), config=primary.config())
+            measure_prefill_form(primary, True, n, flush, dev, stream, pk, clocks),
+            config=primary.config())
         primary.fused = False
         # the LSE merge alone over the primary's partials
         primary.step()
         mb = primary.merge_bytes()
-        st, _, _ = time_steps(primary, n, 3, flush, dev, stream, dominant=False,
-                              fn=primary.merge_only)
+        st, _, win = time_steps(primary, n, 3, flush, dev, stream, dominant=False,
+                                fn=primary.merge_only)
         m_s = statistics.mean(st) / 1e3
         sec["lse_merge"] = {"value": mb / m_s / 1e9, "unit": "GB/s", "config": primary.config(),
                             "roofline": roofline("hbm", "cp_lse_merge (merge_small_kernel)", mb, m_s, pk,
                                                  algorithmic=f"{mb:.4e} B per launch (every partial "
                                                              "LSE, non-empty partial rows, bf16 out + LSE)")}
+        if clocks is not None:
+            sec["lse_merge"]["clocks"] = clocks.summary(*win)
     if w.name != "full":
         fr = PrefillRunner(wl.WORKLOADS["full"], dev, cpa)
+        settle(fr.step, dev, 0.5)
         for fused in (False, True):
             sec["full_prefill_fused" if fused else "full_prefill"] = dict(
-                measure_prefill_form(fr, fused, n, flush, dev, stream, pk),
+                measure_prefill_form(fr, fused, n, flush, dev, stream, pk, clocks),
                 config=fr.config())
         del fr
     if w.name != "chunked":
         qr = PassQRunner(wl.WORKLOADS["chunked"], dev, cpa)
-        e = measure_prefill_form(qr, False, n, flush, dev, stream, pk)
+        settle(qr.step, dev, 0.5)
+        e = measure_prefill_form(qr, False, n, flush, dev, stream, pk, clocks)
         rows, Om, Lm = oracle_pass_q(qr.w, qr.x, 32, 4242)
         e["parity"] = parity_block(qr.buf["out"], qr.buf["olse"], rows, Om, Lm,
                                    f"{len(rows)} stratified new-query rows x all heads")
         e["e2e"] = e2e_block(qr, n, stream, ws, dev, "TFLOP/s")
         e["config"] = qr.config()
         sec["chunked_pass_q"] = e
-        sec["chunked_pass_q_fused"] = dict(measure_prefill_form(qr, True, n, flush, dev, stream, pk),
-                                           config=qr.config())
+        sec["chunked_pass_q_fused"] = dict(
+            measure_prefill_form(qr, True, n, flush, dev, stream, pk, clocks), config=qr.config())
         del qr
     torch.cuda.empty_cache()
     dr = DecodeRunner(wl.WORKLOADS["decode"], dev, cpa)
+    settle(dr.step, dev, 0.5)
     for fused in (False, True):
         dr.fused = fused
-        ds, dd, _ = time_steps(dr, max(10, args.steps // 5), 3, flush, dev, stream)
+        ds, dd, win = time_steps(dr, max(10, args.steps // 5), 3, flush, dev, stream)
         d_s = statistics.mean(dd) / 1e3
         e = {"value": dr.metric(statistics.mean(ds) / 1e3), "unit": "GB/s", "config": dr.config(),
              "roofline": roofline("hbm", "cp_decode_attention (partials + merge, one launch)" if fused
                                   else "cp_partial_attn_decode", dr.bytes, d_s, pk,
                                   traffic=ncu_traffic(*traffic_key(dr)),
                                   algorithmic=f"{dr.bytes:.4e} B per launch (KV once + q + out + tables)")}
+        if clocks is not None:
+            e["clocks"] = clocks.summary(*win)
         seqs = [0, 1, 2, 3, 4, 5]
         Om, Lm = oracle_decode(dr, seqs)
         e["parity"] = parity_block(dr.buf["out"], dr.buf["olse"], seqs, Om, Lm,
@@ -1003,7 +1029,6 @@ def main():
     torch.cuda.synchronize(dev)
     barrier(ws)
     clk = clocks.summary(t0, t1)
-    clocks.stop()
 
     total_s = max_over_ranks(sum(step_ms) / 1e3, ws, dev)
     value = runner.metric(total_s / args.steps) * ws
@@ -1050,10 +1075,12 @@ def main():
                                           + f" x {w.num_q_heads} heads of the {w.name} workload, "
                                           f"float64 NumPy oracle, {t:.1f} s"}
     if not args.no_e2e and not (isinstance(runner, PrefillRunner) and runner.fused):
+        settle(runner.step, dev, 1.0)  # after the oracle's host-side pause
         line["e2e"] = e2e_block(runner, args.steps, stream, ws, dev, unit)
 
     if not args.no_secondary and w.kind != "decode":
-        line["secondary"] = secondaries(args, runner, w, dev, stream, flush, pk, ws)
+        line["secondary"] = secondaries(args, runner, w, dev, stream, flush, pk, ws, clocks)
+    clocks.stop()
 
     if rank == 0:
         print(json.dumps(line))
