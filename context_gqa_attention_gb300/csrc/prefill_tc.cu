@@ -173,10 +173,20 @@ CP_DEV void page_rows(const int (&id)[NP], int t, int n_local, long long pool, i
 struct RankWalk {
   int r, tr, nt_r, n_r;
 };
+// Tokens of rank r among positions [0, L) of the round-robin deal (as rank_local_len) for the
+// positions the kernel sees: L <= seq_lens_kv < 2^31, with g = min(I cp, 2^31), so one 32-bit
+// division and no 64-bit fallback in the loops that walk ranks.
+CP_DEV int rank_len32(long long L, int r, int I, uint32_t g) {
+  const uint32_t l = (uint32_t)L, q = l / g, rem = l - q * g;
+  const long long x = (long long)rem - (long long)r * I;
+  return (int)(q * (uint32_t)I) + (int)(x < 0 ? 0 : (x > I ? I : x));
+}
+
 CP_DEV void walk_settle(RankWalk& k, long long kv_end, int cp, int I, int r_end) {
+  const uint32_t g = (long long)I * cp < (1ll << 31) ? (uint32_t)(I * cp) : (1u << 31);
   while (k.tr >= k.nt_r && k.r + 1 < r_end) {
     ++k.r;
-    k.n_r = rank_local_len(kv_end, k.r, cp, I);
+    k.n_r = rank_len32(kv_end, k.r, I, g);
     k.nt_r = (k.n_r + BN - 1) / BN;
     k.tr = 0;
   }
@@ -1204,10 +1214,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
     int nvis = 0;
     constexpr bool walk = FQ;  // fused pass-Q: rank after rank
     const long long kv_end = w.qpos0 - w.q_lo + w.q_hi;
+    const uint32_t g_rr = (long long)p.I * p.cp < (1ll << 31) ? (uint32_t)(p.I * p.cp) : (1u << 31);
     RankWalk kw{0, 0, 0, 0};
     if constexpr (walk) {
       kw = walk_start(kv_end, p.cp, p.I, w.r_lo, w.r_hi);
-      nvis = min(kw.n_r, rank_local_len(qpos + 1, kw.r, p.cp, p.I));
+      nvis = min(kw.n_r, rank_len32(qpos + 1, kw.r, p.I, g_rr));
     } else {
       if (p.mode == CP_PASS_Q) nvis = min(w.n_local, rank_local_len(qpos + 1, w.p, p.cp, p.I));
     }
@@ -1228,7 +1239,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       } else if constexpr (!walk) {
         lim = nvis - 1 - t * BN;
       } else {
-        if (kw.tr == 0 && t > 0) nvis = min(kw.n_r, rank_local_len(qpos + 1, kw.r, p.cp, p.I));
+        if (kw.tr == 0 && t > 0) nvis = min(kw.n_r, rank_len32(qpos + 1, kw.r, p.I, g_rr));
         lim = nvis - 1 - kw.tr * BN;
         walk_next(kw, kv_end, p.cp, p.I, w.r_hi);
       }
