@@ -43,24 +43,24 @@ import workloads as wl  # noqa: E402
 # command of that form, 3 warm-up steps) at the recorded source SHA-1.  A figure is reported only
 # while that source file still has this SHA-1; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # prefill_tc2_kernel<128,0,0,0>, pass-KV partials: dram read 42.03 MB + write 59.49 MB
+    # prefill_tc2_kernel<128,0,0,0>, pass-KV partials: dram read 42.06 MB + write 59.13 MB
     ("prefill", "full"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                         "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 101520384},
-    # the same kernel, fused pass-KV: read 42.03 MB + write 1.18 MB (the bf16 output is still in L2)
+                         "sha1": "0685401626de1ea968aa3c50d59d59a1a0fab1e3", "bytes": 101186048},
+    # the same kernel, fused pass-KV: read 42.03 MB + write 1.23 MB (the bf16 output is still in L2)
     ("prefill_fused", "full"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                               "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 43211520},
-    # long prefill partials: read 374.6 MB + write 1711.4 MB
+                               "sha1": "0685401626de1ea968aa3c50d59d59a1a0fab1e3", "bytes": 43261440},
+    # long prefill partials: read 374.6 MB + write 1708.8 MB
     ("prefill", "long"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                         "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 2086081280},
-    # long prefill fused: read 345.7 MB + write 234.4 MB
+                         "sha1": "0685401626de1ea968aa3c50d59d59a1a0fab1e3", "bytes": 2083377408},
+    # long prefill fused: read 345.8 MB + write 233.8 MB
     ("prefill_fused", "long"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                               "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 580104704},
-    # prefill_tc2_kernel<128,1,0,0>, pass-Q partials: read 172.2 MB + write 223.3 MB
+                               "sha1": "0685401626de1ea968aa3c50d59d59a1a0fab1e3", "bytes": 579624704},
+    # prefill_tc2_kernel<128,1,0,0>, pass-Q partials: read 172.6 MB + write 222.9 MB
     ("pass_q", "chunked"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                           "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 395576064},
-    # prefill_tc2_kernel<128,1,0,1>, fused pass-Q (split tail): read 225.5 MB + write 25.5 MB
+                           "sha1": "0685401626de1ea968aa3c50d59d59a1a0fab1e3", "bytes": 395523072},
+    # prefill_tc2_kernel<128,1,0,1>, fused pass-Q (split tail): read 226.0 MB + write 25.4 MB
     ("pass_q_fused", "chunked"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                                 "sha1": "0a698096e62733771d5a3ea0d6ec5c86373f2563", "bytes": 251002624},
+                                 "sha1": "0685401626de1ea968aa3c50d59d59a1a0fab1e3", "bytes": 251427072},
     # decode_mma_kernel<128,4,0>, 64-sequence decode: read 4.402 GB + write 23.5 MB
     ("decode", "decode"): {"file": "context_gqa_attention_gb300/csrc/decode.cu",
                           "sha1": "b5c01eaf5355f8808871d81349446501c2511cb0", "bytes": 4425172736},
@@ -822,11 +822,17 @@ def select_workload(args):
     return w
 
 
-def roofline(bound, kernel, work, dom_s, pk, traffic=None, algorithmic=""):
+def roofline(bound, kernel, work, dom_s, pk, traffic=None, algorithmic="", clk=None):
+    """Dominant-kernel roofline.  A tensor-bound kernel is held against the burst bf16 peak,
+    or against the sustained one when the clock samples of its own timed steps show the power
+    cap engaged (as the sustained figure was measured)."""
     if bound == "tensor":
-        peak, src = pk["bf16"]
+        capped = clk is not None and "sw_power_cap" in (clk.get("reasons") or [])
+        peak, src = pk["bf16_sustained"] if capped else pk["bf16"]
         achieved = work / dom_s / 1e12
-        unit, psrc = "TFLOP/s", f"{src} bf16 dense (burst)"
+        unit = "TFLOP/s"
+        psrc = (f"{src} bf16 dense (sustained: sw_power_cap during these steps)" if capped
+                else f"{src} bf16 dense (burst)")
     else:
         peak, src = pk["hbm"]
         achieved = work / dom_s / 1e9
@@ -872,13 +878,14 @@ def measure_prefill_form(runner, fused, steps, flush, dev, stream, pk, clocks=No
     runner.fused = fused
     st, dm, win = time_steps(runner, steps, 3, flush, dev, stream)
     d_s = statistics.mean(dm) / 1e3
+    clk = clocks.summary(*win) if clocks is not None else None
     e = {"value": runner.metric(statistics.mean(st) / 1e3), "unit": "TFLOP/s",
          "ms_per_step": statistics.mean(st),
          "roofline": roofline("tensor", prefill_kernel_name(runner), runner.flops, d_s, pk,
                               traffic=ncu_traffic(*traffic_key(runner)),
-                              algorithmic=f"{runner.flops:.4e} causal FLOP per launch")}
-    if clocks is not None:
-        e["clocks"] = clocks.summary(*win)
+                              algorithmic=f"{runner.flops:.4e} causal FLOP per launch", clk=clk)}
+    if clk is not None:
+        e["clocks"] = clk
     return e
 
 
@@ -1043,7 +1050,7 @@ def main():
     else:
         roof = roofline("tensor", prefill_kernel_name(runner), runner.flops, dom_s, pk,
                         traffic=ncu_traffic(*traffic_key(runner)),
-                        algorithmic=f"{runner.flops:.4e} causal FLOP per launch")
+                        algorithmic=f"{runner.flops:.4e} causal FLOP per launch", clk=clk)
         metric = (PREFILL_METRIC if isinstance(runner, PrefillRunner) and not runner.fused else
                   "causal GQA prefill TFLOP/s (" + prefill_kernel_name(runner) + ")")
         unit = "TFLOP/s"

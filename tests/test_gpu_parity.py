@@ -342,6 +342,42 @@ def test_fused_pass_q_parity(lib, case, split):
     check_merged(out, lse, Om, Lm, what=f"fused pass-Q split={split}")
 
 
+@pytest.mark.parametrize("interleave", [(1 << 29) - 1, 1 << 30])
+def test_pass_q_huge_interleave(lib, interleave):
+    """An interleave size above every position deals all tokens to rank 0 (the others hold
+    none): interleave x cp just below 2^31 and far above it, the two forms of the kernel's
+    32-bit rank lengths.  Partials and the fused launch (with and without the tail split)."""
+    q_lens, kv_lens, Hq, Hkv, d, cp = [300, 77], [900, 400], 8, 2, 128, 4
+    g = torch.Generator().manual_seed(77)
+    pages = [-(-L // 16) for L in kv_lens]
+    pool = sum(pages)
+    tables = torch.full((cp, len(q_lens), max(pages)), -1, dtype=torch.int32)
+    perm = torch.randperm(pool, generator=g).to(torch.int32)
+    o = 0
+    for b, n in enumerate(pages):  # rank 0 holds every token; the other ranks have no pages
+        tables[0, b, :n] = perm[o:o + n]
+        o += n
+    q = wl.normal((sum(q_lens), Hq, d), torch.bfloat16, g)
+    kc = wl.normal((cp, pool, Hkv, 16, d), torch.bfloat16, g)
+    vc = wl.normal((cp, pool, Hkv, 16, d), torch.bfloat16, g)
+    cu, sl = _cu(q_lens), torch.tensor(kv_lens, dtype=torch.int32)
+    kw = dict(mode=lib.CP_PASS_Q, k_cache=kc.to(DEV), v_cache=vc.to(DEV), block_tables=tables.to(DEV),
+              seq_lens_kv=sl.to(DEV), interleave=interleave, max_seqlen_q=max(q_lens))
+    O, L = orc.pass_q_partials(q, kc, vc, tables, cu, sl, cp, interleave, 16, 1 / math.sqrt(d))
+    assert np.isneginf(L[1:]).all()   # ranks 1.. hold nothing
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = lib.cp_partial_attn_prefill(q.to(DEV), cu.to(DEV), cp, err=err, **kw)
+    check_partials(out, lse, O, L, what=f"pass-Q I={interleave}")
+    Om, Lm = orc.lse_merge(O, L)
+    for split in (True, False):
+        need = lib.cp_prefill_fused_workspace_size(len(q_lens), Hq, Hkv, d, cp, max(q_lens))
+        ws = torch.empty(need if split else 0, dtype=torch.uint8, device=DEV)
+        fo, fl = lib.cp_attn_prefill_fused(q.to(DEV), cu.to(DEV), cp, workspace=ws, **kw)
+        check_merged(fo, fl, Om, Lm, what=f"fused pass-Q I={interleave} split={split}")
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+
 # ------------------------------------------------------------------------------------ decode
 
 DECODE_CASES = [
