@@ -15,11 +15,13 @@
 //               columns, then O += P V with P read from TMEM; order per key tile
 //               PV0(t) | QK0(t+1) | PV1(t) | QK1(t+1), so each tile's softmax overlaps the
 //               other tile's two MMAs.
-//   warps 2-9   two softmax warpgroups, one per tile: thread i owns query row i (TMEM lane i),
+//   warps 2-3   idle (they complete the first warpgroup, whose register budget is lowered so
+//               that the softmax warpgroups can raise theirs)
+//   warps 4-11  two softmax warpgroups, one per tile: thread i owns query row i (TMEM lane i),
 //               reads its S row with tcgen05.ld, masks by position, keeps the running max /
 //               sum, rescales O in TMEM only when the max grows by more than 2^8, writes P
 //               (bf16) back over its S columns, and finally normalises O and writes the output
-//               and its LSE (TMA bulk stores of staged 32-row boxes).
+//               and its LSE (rows staged in shared memory, then one whole row per warp store).
 // prefill_tc1_kernel (CP_IMPL_TCGEN05_SINGLE) runs one head per CTA with a 2-stage ring and P
 // in shared memory.
 // Every wait is bounded; on expiry the CTA raises CP_ERR_TIMEOUT, drains its own copies and
