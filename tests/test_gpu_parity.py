@@ -378,6 +378,71 @@ def test_pass_q_huge_interleave(lib, interleave):
     assert int(err.item()) == 0
 
 
+def test_max_cp(lib):
+    """cp = 64, the largest the boundary accepts: 128 chunks per sequence (most a few tokens or
+    empty), 64-rank walks, the fused pass-Q split plan over 64 ranks, and a fused decode at its
+    limit of 256 partials (64 ranks x 4 splits)."""
+    cp, d, bf = 64, 128, torch.bfloat16
+    # pass-KV: partials (both tensor-core kernels) and the fused launch
+    lens = [1000, 200, 3]
+    x = wl.prefill_inputs(lens, 8, 2, d, bf, seed=640)
+    # partials of 8-token chunks are dominated by a few keys: the outputs get the bound of the
+    # probabilities' bf16 rounding, 2^-8 x the oracle's attention of |V|
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], cp, 1 / math.sqrt(d))
+    Oa, _ = orc.pass_kv_partials(x["q"], x["k"], x["v"].abs(), x["cu_seqlens"], cp, 1 / math.sqrt(d))
+    Om, Lm = orc.lse_merge(O, L)
+    Oam, _ = orc.lse_merge(Oa, L)
+    args = (x["q"].to(DEV), x["cu_seqlens"].to(DEV), cp)
+    for impl in (lib.CP_IMPL_TCGEN05, lib.CP_IMPL_TCGEN05_SINGLE):
+        out, lse = lib.cp_partial_attn_prefill(*args, k=x["k"].to(DEV), v=x["v"].to(DEV),
+                                               max_seqlen_q=max(lens), impl=impl)
+        check_partials(out, lse, O, L, what=f"pass-KV cp=64 impl={impl}", o_abs=Oa)
+    fo, fl = lib.cp_attn_prefill_fused(*args, x["k"].to(DEV), x["v"].to(DEV), max_seqlen_q=max(lens))
+    check_merged(fo, fl, Om, Lm, what="fused pass-KV cp=64", o_abs=Oam)
+    # pass-Q over a paged round-robin cache, interleave 4
+    q_lens, kv_lens, I = [100, 40], [3000, 900], 4
+    z = _paged_case(2, q_lens, kv_lens, 8, 2, d, bf, cp, I, 641)
+    kw = dict(mode=lib.CP_PASS_Q, k_cache=z["k_cache"].to(DEV), v_cache=z["v_cache"].to(DEV),
+              block_tables=z["block_tables"].to(DEV), seq_lens_kv=z["seq_lens"].to(DEV),
+              interleave=I, max_seqlen_q=max(q_lens))
+    Oq, Lq = orc.pass_q_partials(z["q"], z["k_cache"], z["v_cache"], z["block_tables"],
+                                 z["cu_seqlens_q"], z["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
+    Oqa, _ = orc.pass_q_partials(z["q"], z["k_cache"], z["v_cache"].abs(), z["block_tables"],
+                                 z["cu_seqlens_q"], z["seq_lens"], cp, I, 16, 1 / math.sqrt(d))
+    out, lse = lib.cp_partial_attn_prefill(z["q"].to(DEV), z["cu_seqlens_q"].to(DEV), cp, **kw)
+    check_partials(out, lse, Oq, Lq, what="pass-Q cp=64", o_abs=Oqa)
+    Oqm, Lqm = orc.lse_merge(Oq, Lq)
+    Oqam, _ = orc.lse_merge(Oqa, Lq)
+    need = lib.cp_prefill_fused_workspace_size(2, 8, 2, d, cp, max(q_lens))
+    for ws in (torch.empty(need, dtype=torch.uint8, device=DEV),
+               torch.empty(0, dtype=torch.uint8, device=DEV)):
+        fo, fl = lib.cp_attn_prefill_fused(z["q"].to(DEV), z["cu_seqlens_q"].to(DEV), cp,
+                                           workspace=ws, **kw)
+        check_merged(fo, fl, Oqm, Lqm, what=f"fused pass-Q cp=64 workspace={ws.numel()}",
+                     o_abs=Oqam)
+    # decode: 64 ranks x 4 splits = 256 partials, the fused form's limit
+    dl = [4000, 100, 1]
+    y = wl.paged_inputs(3, 1, dl, 8, 2, d, bf, cp, 2, 16, 642, 643, q_is_decode=True)
+    dev = {n: y[n].to(DEV) for n in ("q", "k_cache", "v_cache", "block_tables", "seq_lens")}
+    ns, st = lib.cp_decode_plan(3, 2, cp, 2, 16, max(dl))
+    assert cp * ns <= 256
+    Od, Ld = orc.decode_partials(y["q"], y["k_cache"], y["v_cache"], y["block_tables"],
+                                 y["seq_lens"], cp, 2, 16, 1 / math.sqrt(d))
+    Odm, Ldm = orc.lse_merge(Od, Ld)
+    Oda, _ = orc.decode_partials(y["q"], y["k_cache"], y["v_cache"].abs(), y["block_tables"],
+                                 y["seq_lens"], cp, 2, 16, 1 / math.sqrt(d))
+    Odam, _ = orc.lse_merge(Oda, Ld)
+    po, pl = lib.cp_partial_attn_decode(dev["q"], dev["k_cache"], dev["v_cache"],
+                                        dev["block_tables"], dev["seq_lens"], cp, 2,
+                                        num_splits=ns, split_tokens=st)
+    mo, ml = lib.cp_lse_merge(po, pl, out_dtype=bf)
+    check_merged(mo, ml, Odm, Ldm, what="decode cp=64", o_abs=Odam)
+    fd, fdl = lib.cp_decode_attention(dev["q"], dev["k_cache"], dev["v_cache"],
+                                      dev["block_tables"], dev["seq_lens"], cp, 2,
+                                      num_splits=ns, split_tokens=st)
+    check_merged(fd, fdl, Odm, Ldm, what="fused decode cp=64", o_abs=Odam)
+
+
 # ------------------------------------------------------------------------------------ decode
 
 DECODE_CASES = [
