@@ -443,6 +443,41 @@ def test_max_cp(lib):
     check_merged(fd, fdl, Odm, Ldm, what="fused decode cp=64", o_abs=Odam)
 
 
+def test_many_short_sequences(lib):
+    """300 sequences of 1-40 tokens (most chunks a token or two, many empty): the work-item
+    decode over a long sequence index, pass-KV and pass-Q, partials and fused."""
+    g = torch.Generator().manual_seed(650)
+    lens = (torch.randint(1, 41, (300,), generator=g)).tolist()
+    cp, d, bf = 3, 128, torch.bfloat16
+    x = wl.prefill_inputs(lens, 8, 2, d, bf, seed=651)
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], cp, 1 / math.sqrt(d))
+    Oa, _ = orc.pass_kv_partials(x["q"], x["k"], x["v"].abs(), x["cu_seqlens"], cp, 1 / math.sqrt(d))
+    args = (x["q"].to(DEV), x["cu_seqlens"].to(DEV), cp)
+    out, lse = lib.cp_partial_attn_prefill(*args, k=x["k"].to(DEV), v=x["v"].to(DEV),
+                                           max_seqlen_q=max(lens))
+    check_partials(out, lse, O, L, what="pass-KV 300 sequences", o_abs=Oa)
+    Om, Lm = orc.lse_merge(O, L)
+    Oam, _ = orc.lse_merge(Oa, L)
+    fo, fl = lib.cp_attn_prefill_fused(*args, x["k"].to(DEV), x["v"].to(DEV), max_seqlen_q=max(lens))
+    check_merged(fo, fl, Om, Lm, what="fused pass-KV 300 sequences", o_abs=Oam)
+    # the same new tokens as chunks of longer paged sequences (pass-Q)
+    kv_lens = [n + int(c) for n, c in zip(lens, torch.randint(0, 200, (300,), generator=g))]
+    z = _paged_case(300, lens, kv_lens, 8, 2, d, bf, cp, 8, 652)
+    kw = dict(mode=lib.CP_PASS_Q, k_cache=z["k_cache"].to(DEV), v_cache=z["v_cache"].to(DEV),
+              block_tables=z["block_tables"].to(DEV), seq_lens_kv=z["seq_lens"].to(DEV),
+              interleave=8, max_seqlen_q=max(lens))
+    Oq, Lq = orc.pass_q_partials(z["q"], z["k_cache"], z["v_cache"], z["block_tables"],
+                                 z["cu_seqlens_q"], z["seq_lens"], cp, 8, 16, 1 / math.sqrt(d))
+    Oqa, _ = orc.pass_q_partials(z["q"], z["k_cache"], z["v_cache"].abs(), z["block_tables"],
+                                 z["cu_seqlens_q"], z["seq_lens"], cp, 8, 16, 1 / math.sqrt(d))
+    out, lse = lib.cp_partial_attn_prefill(z["q"].to(DEV), z["cu_seqlens_q"].to(DEV), cp, **kw)
+    check_partials(out, lse, Oq, Lq, what="pass-Q 300 sequences", o_abs=Oqa)
+    Oqm, Lqm = orc.lse_merge(Oq, Lq)
+    Oqam, _ = orc.lse_merge(Oqa, Lq)
+    fo, fl = lib.cp_attn_prefill_fused(z["q"].to(DEV), z["cu_seqlens_q"].to(DEV), cp, **kw)
+    check_merged(fo, fl, Oqm, Lqm, what="fused pass-Q 300 sequences", o_abs=Oqam)
+
+
 # ------------------------------------------------------------------------------------ decode
 
 DECODE_CASES = [
