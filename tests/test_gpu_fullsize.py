@@ -88,3 +88,24 @@ def test_decode_full_size(lib):
                                      dev["seq_lens"], w.cp, w.interleave, num_splits=ns,
                                      split_tokens=st)
     check_merged(fo, fl, Om, Lm, what="fused decode")
+
+
+def test_pass_kv_single_128k_sequence(lib):
+    """One sequence of 131072 tokens at cp = 8 (16 chunks of 8192 tokens, ~32K work items,
+    8.6 GB of f32 partials): index arithmetic at the large end, checked on 256 stratified rows."""
+    T, cp, Hq, Hkv, d = 131072, 8, 16, 2, 128
+    x = wl.prefill_inputs([T], Hq, Hkv, d, torch.bfloat16, seed=660)
+    q, k, v, cu = (x[n].cuda() for n in ("q", "k", "v", "cu_seqlens"))
+    out, lse = lib.cp_partial_attn_prefill(q, cu, cp, k=k, v=v, max_seqlen_q=T)
+    bnd = orc.chunk_bounds(T, cp).tolist()
+    rows = wl.sample_rows(T, bnd, 256, 661)
+    O, L = orc.pass_kv_partials(x["q"], x["k"], x["v"], x["cu_seqlens"], cp, 1 / math.sqrt(d),
+                                rows=rows)
+    check_partials(out, lse, O, L, rows=rows, what="128K partials")
+    Om, Lm = orc.lse_merge(O, L)
+    idx = torch.as_tensor(rows, device="cuda")
+    mo, ml = lib.cp_lse_merge(out, lse, out_dtype=torch.bfloat16)
+    check_merged(mo.index_select(0, idx), ml.index_select(0, idx), Om, Lm, what="128K merged")
+    del out, lse, mo, ml
+    fo, fl = lib.cp_attn_prefill_fused(q, cu, cp, k, v, max_seqlen_q=T)
+    check_merged(fo.index_select(0, idx), fl.index_select(0, idx), Om, Lm, what="128K fused")
