@@ -72,6 +72,8 @@ CP_DEV uint32_t udiv(uint32_t n, const FastDiv& f) {
 
 struct TcParams {
   int mode, B, Hq, Hkv, cp, I, max_blocks, q_shard, kv_shard, TPC, Nq, debug;
+  // pass-KV partials: head groups outermost within a sequence (see decode_work_at)
+  int heads_outer;
   // divisors of the work-item decode: item groups of heads, q slots (2 cp TPC), cp, TPC, 2 cp
   // (chunk bounds), G (q heads per kv head)
   FastDiv f_groups, f_nslot, f_cp, f_tpc, f_2cp, f_G;
@@ -203,10 +205,6 @@ CP_DEV void walk_next(RankWalk& k, long long kv_end, int cp, int I, int r_end) {
   walk_settle(k, kv_end, cp, I, r_end);
 }
 
-// Work item index -> (q tile slot, sequence, kv shard, head group of `hpc` consecutive q heads).
-// Slots run heaviest first (last chunk, last tile) so long items start early.
-// `span` query rows per item: BM (one tile; head pairs) or 2 BM (two tiles of one head).
-// Fused pass-Q items walk ranks [r_lo, r_hi) (all of them unless the item is split).
 // Chunk bound floor(k T / 2cp) (as chunk_bound) with the launch's divisor constants.
 template <bool FAST>
 CP_DEV int chunk_bound_f(int k, int T, const TcParams& p) {
@@ -217,6 +215,10 @@ CP_DEV int chunk_bound_f(int k, int T, const TcParams& p) {
   return chunk_bound(k, T, p.cp);
 }
 
+// Work item index -> (q tile slot, sequence, kv shard, head group of `hpc` consecutive q heads).
+// Slots run heaviest first (last chunk, last tile) so long items start early.
+// `span` query rows per item: BM (one tile; head pairs) or 2 BM (two tiles of one head).
+// Fused pass-Q items walk ranks [r_lo, r_hi) (all of them unless the item is split).
 template <bool FAST = true>
 CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = BM, int r_lo = 0,
                            int r_hi = 1 << 30) {
@@ -227,10 +229,25 @@ CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = 
   // the item space is below 2^31; p.f_groups divides by Hq / hpc
   const unsigned groups = (unsigned)(p.Hq / hpc);
   const unsigned nslot = 2u * (unsigned)p.cp * (unsigned)p.TPC;
-  unsigned q = udiv<FAST>(lin, p.f_groups);
+  unsigned q;
+  int slot;
+  if (p.heads_outer) {
+    // pass-KV partials with a sequence's K/V larger than L2 can hold beside the outgoing
+    // partial rows: kv shard fastest, then slot (heaviest first), then head group, so the CTAs
+    // resident at one time read one kv head's K/V of one sequence
+    q = udiv<FAST>(lin, p.f_cp);
+    w.p = (int)(lin - q * (unsigned)p.cp);
+    lin = q;
+    q = udiv<FAST>(lin, p.f_nslot);
+    slot = (int)(lin - q * nslot);
+    lin = q;
+    q = udiv<FAST>(lin, p.f_groups);
+    w.h = (int)(lin - q * groups) * hpc;
+    w.b = (int)q;
+  } else {
+  q = udiv<FAST>(lin, p.f_groups);
   w.h = (int)(lin - q * groups) * hpc;
   lin = q;
-  int slot;
   if (p.mode == CP_PASS_Q) {
     // pass-Q items cost about the same (every query sees its rank's whole cached context), so
     // they run sequence by sequence and rank by rank: the CTAs resident at one time read the
@@ -259,6 +276,7 @@ CP_DEV Work decode_work_at(const TcParams& p, unsigned lin, int hpc, int span = 
     q = udiv<FAST>(lin, p.f_nslot);
     slot = (int)(lin - q * nslot);
     w.b = (int)q;
+  }
   }
   const unsigned sq = udiv<FAST>((unsigned)slot, p.f_tpc);
   const int c = 2 * p.cp - 1 - (int)sq;
@@ -1447,6 +1465,25 @@ Shape shape_of(const cp_prefill_args& a, bool fused) {
   return sh;
 }
 
+// Pass-KV partials: the item order that keeps the CTAs resident at one time on one kv head of a
+// sequence (head groups outermost) when one sequence's K/V is too large for L2 next to the
+// outgoing partial rows (>= 64 MB), provided every SM gets many items (>= 32), so that each head
+// group's heaviest items starting late does not stretch the grid's tail.  Measured on GB300 at
+// 2 x 32768 tokens, cp = 4: 16/16 heads 1339 -> 1554 TFLOP/s, 24/8 +6%, 32/8 +4%, 64/8 +2%;
+// at 1 x 8192 (7 items per SM) the same order lost 5-8%, and the fused launch (whose items walk
+// a sequence's whole K/V) did not gain.
+bool heads_outer_order(const cp_prefill_args& a, const Shape& sh, bool fused, int D) {
+  if (a.mode != CP_PASS_KV || fused || a.kv_shard >= 0) return false;
+  const double kv_tokens = a.cu_seqlens_kv != nullptr && a.num_seqs > 0
+                               ? (double)a.total_kv / a.num_seqs : (double)a.max_seqlen_q;
+  if (kv_tokens * a.num_kv_heads * D * 2.0 * 2.0 < 64e6) return false;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  return sh.items >= 32ll * sms;
+}
+
 // Split plan of a fused pass-Q launch on the current device (no split for anything else).
 SplitPlan fused_split_plan(const cp_prefill_args& a) {
   const Shape sh = shape_of(a, true);
@@ -1524,6 +1561,7 @@ cudaError_t launch(const cp_prefill_args& a, float scale, cudaStream_t s, void* 
   p.fused = fused_out != nullptr;
   p.out_final = static_cast<__nv_bfloat16*>(fused_out);
   p.lse_final = fused_lse;
+  p.heads_outer = heads_outer_order(a, sh, p.fused, D) ? 1 : 0;
   p.row_out = (reinterpret_cast<uintptr_t>(p.fused ? fused_out : static_cast<void*>(a.out)) & 15u) == 0;
   long long grid = sh.items;
   if (grid == 0) return cudaSuccess;
