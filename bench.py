@@ -41,28 +41,26 @@ import workloads as wl  # noqa: E402
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of a dominant kernel,
 # each from one ncu capture (one pass, a warm launch: "-k regex:<kernel> -s 2 -c 1" on the bench
 # command of that form, 3 warm-up steps) at the recorded source SHA-1.  A figure is reported only
-# while that source file still has this SHA-1; otherwise traffic is null.  (The prefill figures
-# were captured on prefill_tc.cu 0685401626de1ea968aa3c50d59d59a1a0fab1e3; the recorded file
-# differs from it only in its header comment.)
+# while that source file still has this SHA-1; otherwise traffic is null.
 NCU_TRAFFIC = {
-    # prefill_tc2_kernel<128,0,0,0>, pass-KV partials: dram read 42.06 MB + write 59.13 MB
+    # prefill_tc2_kernel<128,0,0,0>, pass-KV partials: dram read 42.03 MB + write 59.00 MB
     ("prefill", "full"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                         "sha1": "0269186f5707079d4b0d4f4abacbce499b4e83f9", "bytes": 101186048},
-    # the same kernel, fused pass-KV: read 42.03 MB + write 1.23 MB (the bf16 output is still in L2)
+                         "sha1": "e7cab9b56d6dd9a314e745bf2f0e2bc48b0516d5", "bytes": 101029632},
+    # the same kernel, fused pass-KV: read 42.03 MB + write 1.17 MB (the bf16 output is still in L2)
     ("prefill_fused", "full"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                               "sha1": "0269186f5707079d4b0d4f4abacbce499b4e83f9", "bytes": 43261440},
-    # long prefill partials: read 374.6 MB + write 1708.8 MB
+                               "sha1": "e7cab9b56d6dd9a314e745bf2f0e2bc48b0516d5", "bytes": 43200512},
+    # long prefill partials: read 373.7 MB + write 1708.7 MB
     ("prefill", "long"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                         "sha1": "0269186f5707079d4b0d4f4abacbce499b4e83f9", "bytes": 2083377408},
-    # long prefill fused: read 345.8 MB + write 233.8 MB
+                         "sha1": "e7cab9b56d6dd9a314e745bf2f0e2bc48b0516d5", "bytes": 2082401024},
+    # long prefill fused: read 344.8 MB + write 234.3 MB
     ("prefill_fused", "long"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                               "sha1": "0269186f5707079d4b0d4f4abacbce499b4e83f9", "bytes": 579624704},
-    # prefill_tc2_kernel<128,1,0,0>, pass-Q partials: read 172.6 MB + write 222.9 MB
+                               "sha1": "e7cab9b56d6dd9a314e745bf2f0e2bc48b0516d5", "bytes": 579085312},
+    # prefill_tc2_kernel<128,1,0,0>, pass-Q partials: read 172.1 MB + write 222.7 MB
     ("pass_q", "chunked"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                           "sha1": "0269186f5707079d4b0d4f4abacbce499b4e83f9", "bytes": 395523072},
-    # prefill_tc2_kernel<128,1,0,1>, fused pass-Q (split tail): read 226.0 MB + write 25.4 MB
+                           "sha1": "e7cab9b56d6dd9a314e745bf2f0e2bc48b0516d5", "bytes": 394838528},
+    # prefill_tc2_kernel<128,1,0,1>, fused pass-Q (split tail): read 226.4 MB + write 24.8 MB
     ("pass_q_fused", "chunked"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
-                                 "sha1": "0269186f5707079d4b0d4f4abacbce499b4e83f9", "bytes": 251427072},
+                                 "sha1": "e7cab9b56d6dd9a314e745bf2f0e2bc48b0516d5", "bytes": 251136512},
     # decode_mma_kernel<128,4,0>, 64-sequence decode: read 4.402 GB + write 23.5 MB
     ("decode", "decode"): {"file": "context_gqa_attention_gb300/csrc/decode.cu",
                           "sha1": "b5c01eaf5355f8808871d81349446501c2511cb0", "bytes": 4425172736},
