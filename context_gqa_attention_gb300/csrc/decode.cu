@@ -82,10 +82,12 @@ CP_DEV int live_partials(const DecodeParams& p, int L) {
   for (int r = 0; r < p.cp; ++r) c += min(p.S, (rank_local_len(L, r, p.cp, p.I) + p.ST - 1) / p.ST);
   return c;
 }
+// s_w: shared scratch of kMaxFusedPartials * G floats, per (partial, head): log2 LSE, then
+// weight.  The tensor-core kernel passes its K/V ring, idle by then, so that the merge adds no
+// shared memory to the CTA (three CTAs per SM still fit at G = 16).
 template <typename T, int D, int G>
-CP_DEV void fused_tail(const DecodeParams& p, int b, int g, int L) {
+CP_DEV void fused_tail(const DecodeParams& p, int b, int g, int L, float* s_w) {
   __shared__ int s_last;
-  __shared__ float s_w[kMaxFusedPartials * G];  // per (partial, head): log2 LSE, then weight
   __shared__ float s_M[G], s_L[G];
   __syncthreads();
   const int P = p.cp * p.S;
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_kernel(const DecodePara
   __shared__ __align__(16) float p_s[kWarps][kPage][G];
   __shared__ float m_w[kWarps][G], l_w[kWarps][G];
   __shared__ __align__(16) float o_w[kWarps][G][D];
+  __shared__ float fused_w[FUSED ? kMaxFusedPartials * G : 1];  // the fused merge's weights
 
   const int split = blockIdx.x, g = blockIdx.y;
   // the cp ranks of a sequence are adjacent in launch order, so a (sequence, kv head) group's
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) decode_kernel(const DecodePara
       p.lse[obase + hh] = -INFINITY;
     }
   }
-  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g, L);
+  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g, L, fused_w);
 
 }
 
@@ -396,7 +399,8 @@ struct MLayout {
   static constexpr int kBytes = oFlag + (kCW * kST + 1) * 4;
   static constexpr int kAlloc = kBytes + 1024;      // base rounded up to the 1 KB swizzle atom
   static_assert(kCW * 16 * D * 4 <= kRing, "warp partials reuse the ring");
-  static_assert(kAlloc + 16 * 1024 + 64 <= 232448, "shared memory (incl. the fused merge) per CTA");
+  static_assert(kMaxFusedPartials * 16 * 4 <= kRing, "the fused merge's weights reuse the ring");
+  static_assert(kAlloc + 1024 <= 232448, "shared memory per CTA");
 };
 
 CP_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -706,7 +710,9 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 3)
       p.lse[obase + hh] = -INFINITY;
     }
   }
-  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g, L);
+  // the merge weights go to the K/V ring: free once every warp has passed fused_tail's barrier
+  // (the warp partials read above live there too)
+  if constexpr (FUSED) fused_tail<T, D, G>(p, b, g, L, reinterpret_cast<float*>(sb + Ly::oRing));
 }
 
 template <int D, bool F>
