@@ -61,12 +61,12 @@ NCU_TRAFFIC = {
     # prefill_tc2_kernel<128,1,0,1>, fused pass-Q (split tail): read 226.4 MB + write 24.8 MB
     ("pass_q_fused", "chunked"): {"file": "context_gqa_attention_gb300/csrc/prefill_tc.cu",
                                  "sha1": "e7cab9b56d6dd9a314e745bf2f0e2bc48b0516d5", "bytes": 251136512},
-    # decode_mma_kernel<128,4,0>, 64-sequence decode: read 4.402 GB + write 23.5 MB
+    # decode_mma_kernel<128,4,0>, 64-sequence decode: read 4.401 GB + write 23.6 MB
     ("decode", "decode"): {"file": "context_gqa_attention_gb300/csrc/decode.cu",
-                          "sha1": "b5c01eaf5355f8808871d81349446501c2511cb0", "bytes": 4425172736},
-    # decode_mma_kernel<128,4,1> (fused merge): read 4.403 GB + write 18.1 MB
+                          "sha1": "04b21175c45ac2e18e4f0cfc55d0f73c550df2ff", "bytes": 4425008128},
+    # decode_mma_kernel<128,4,1> (fused merge): read 4.402 GB + write 16.1 MB
     ("decode_fused", "decode"): {"file": "context_gqa_attention_gb300/csrc/decode.cu",
-                                "sha1": "b5c01eaf5355f8808871d81349446501c2511cb0", "bytes": 4420925696},
+                                "sha1": "04b21175c45ac2e18e4f0cfc55d0f73c550df2ff", "bytes": 4418197248},
 }
 
 FALLBACK_HBM_GBS = 6800.0
