@@ -842,16 +842,21 @@ def roofline(bound, kernel, work, dom_s, pk, traffic=None, algorithmic="", clk=N
             "algorithmic": algorithmic, "launch_ms": dom_s * 1e3}
 
 
-def e2e_block(runner, steps, stream, ws, dev, unit):
+def e2e_block(runner, steps, stream, ws, dev, unit, clocks=None):
     runner.e2e_run(3, stream)
+    t0 = time.time()
     e2e_s = max_over_ranks(runner.e2e_run(steps, stream), ws, dev)
+    t1 = time.time()
     if not runner.e2e_check():
         raise RuntimeError("end-to-end output differs from the device-only step")
     h2d, d2h = runner.e2e_bytes()
-    return {"value": runner.metric(e2e_s / steps) * ws, "unit": unit,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipelining": runner.e2e_note,
-            "checked": "last host output == device-only step (bitwise)"}
+    e = {"value": runner.metric(e2e_s / steps) * ws, "unit": unit,
+         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+         "pipelining": runner.e2e_note,
+         "checked": "last host output == device-only step (bitwise)"}
+    if clocks is not None:
+        e["clocks"] = clocks.summary(t0, t1)
+    return e
 
 
 def traffic_key(runner):
@@ -941,7 +946,7 @@ def secondaries(args, primary, w, dev, stream, flush, pk, ws, clocks=None):
         rows, Om, Lm = oracle_pass_q(qr.w, qr.x, 32, 4242)
         e["parity"] = parity_block(qr.buf["out"], qr.buf["olse"], rows, Om, Lm,
                                    f"{len(rows)} stratified new-query rows x all heads")
-        e["e2e"] = e2e_block(qr, n, stream, ws, dev, "TFLOP/s")
+        e["e2e"] = e2e_block(qr, n, stream, ws, dev, "TFLOP/s", clocks)
         e["config"] = qr.config()
         sec["chunked_pass_q"] = e
         sec["chunked_pass_q_fused"] = dict(
@@ -966,7 +971,7 @@ def secondaries(args, primary, w, dev, stream, flush, pk, ws, clocks=None):
         e["parity"] = parity_block(dr.buf["out"], dr.buf["olse"], seqs, Om, Lm,
                                    f"{len(seqs)} sequences x all heads")
         if not fused:
-            e["e2e"] = e2e_block(dr, max(10, args.steps // 5), stream, ws, dev, "GB/s")
+            e["e2e"] = e2e_block(dr, max(10, args.steps // 5), stream, ws, dev, "GB/s", clocks)
         sec["decode_fused" if fused else "decode"] = e
     del dr
     torch.cuda.empty_cache()
@@ -1083,7 +1088,7 @@ def main():
                                           f"float64 NumPy oracle, {t:.1f} s"}
     if not args.no_e2e and not (isinstance(runner, PrefillRunner) and runner.fused):
         settle(runner.step, dev, 1.0)  # after the oracle's host-side pause
-        line["e2e"] = e2e_block(runner, args.steps, stream, ws, dev, unit)
+        line["e2e"] = e2e_block(runner, args.steps, stream, ws, dev, unit, clocks)
 
     if not args.no_secondary and w.kind != "decode":
         line["secondary"] = secondaries(args, runner, w, dev, stream, flush, pk, ws, clocks)
