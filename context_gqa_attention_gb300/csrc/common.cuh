@@ -68,11 +68,6 @@ CP_DEV int rank_local_len(long long L, int r, int cp, int I) {
   return (int)(full + rem);
 }
 
-// Global position of local index l on rank r.
-CP_DEV long long rank_local_pos(long long l, int r, int cp, int I) {
-  return (l / I) * (long long)I * cp + (long long)r * I + (l % I);
-}
-
 // Sequence of a row: largest b with cu[b] <= row (cu non-decreasing, cu[0] = 0).
 CP_DEV int seq_of_row(const int32_t* __restrict__ cu, int num_seqs, int row) {
   int lo = 0, hi = num_seqs - 1;

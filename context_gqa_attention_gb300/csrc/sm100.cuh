@@ -75,19 +75,6 @@ SM100_DEV void tma_load_2d(uint32_t dst, const void* map, int x, int y, uint32_t
       : "memory");
 }
 
-// 3D tiled bulk store shared -> global (bulk-group completion); the source box must already be
-// visible to the async proxy (fence.proxy.async.shared::cta after the generic writes).
-SM100_DEV void tma_store_3d(const void* map, uint32_t src, int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-SM100_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until every committed bulk store of this thread has finished reading shared memory.
-SM100_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
 // 3D tiled bulk copy global -> shared completing on an mbarrier (same rules as the 2D form).
 SM100_DEV void tma_load_3d(uint32_t dst, const void* map, int x, int y, int z, uint32_t bar) {
   asm volatile(
@@ -103,15 +90,6 @@ SM100_DEV void tma_load_4d(uint32_t dst, const void* map, int x, int y, int z, i
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
-      : "memory");
-}
-
-// 1D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16) completing on an
-// mbarrier.
-SM100_DEV void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 
